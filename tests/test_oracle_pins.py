@@ -1,0 +1,307 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each test ties one part of the oracle to a library routine, a closed form, an
+invariant the pages' definitions imply, or brute force, so that a dropped
+term, a wrong sign or index, or a transposed operand fails at least one:
+
+  I1  1x1x1 conv == matmul (numpy), non-square so a transposed weight fails.
+  I2  delta kernels: identity, T/H/W shifts with zero borders, cache frames,
+      channel permutation (pins tap order, causal pad, o/c indexing).
+  I3  causality of the whole block.
+  I4  full-T == frame-by-frame with feat_cache (chunks 1, 2, 5, save/resume).
+  I5  whole block vs torch.nn.functional (conv3d, normalize, silu) in fp64.
+  I6  norm invariants and the eps clamp in closed form.
+  I7  closed form of the block at x = 0.
+  +   sampled-point oracle == whole-tensor oracle, bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from video_vae_causal_gb300 import synth
+
+
+def rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def torch_resblock(x, p, eps=1e-12):
+    """The block written with torch.nn.functional in fp64 (NCDHW inside)."""
+    xt = torch.from_numpy(x).permute(0, 4, 1, 2, 3)
+
+    def norm(v, g):
+        g = torch.from_numpy(g).view(1, -1, 1, 1, 1)
+        return F.normalize(v, p=2, dim=1, eps=eps) * math.sqrt(v.shape[1]) * g
+
+    def conv3(v, w, b):
+        v = F.pad(v, (1, 1, 1, 1, 2, 0))  # W: 1|1, H: 1|1, T: 2 leading frames
+        return F.conv3d(v, torch.from_numpy(w).permute(0, 4, 1, 2, 3), torch.from_numpy(b))
+
+    a1 = F.silu(norm(xt, p.gamma1))
+    h = conv3(a1, p.wA, p.bA)
+    a2 = F.silu(norm(h, p.gamma2))
+    r = conv3(a2, p.wB, p.bB)
+    if p.wS is None:
+        s = xt
+    else:
+        s = F.conv3d(xt, torch.from_numpy(p.wS).permute(0, 4, 1, 2, 3), torch.from_numpy(p.bS))
+    return (r + s).permute(0, 2, 3, 4, 1).numpy()
+
+
+def make_params(ci, co, seed, shortcut=None):
+    g = torch.Generator().manual_seed(seed)
+    return oracle.Params.from_dict(synth.make_params(ci, co, g, shortcut=shortcut))
+
+
+# ---------------------------------------------------------------- I1
+def test_I1_pointwise_conv_is_matmul():
+    x = rand((2, 3, 4, 5, 6), 1)
+    w = rand((5, 1, 1, 1, 6), 2)
+    b = rand((5,), 3)
+    got = oracle.causal_conv3d(x, w, b)
+    ref = x.reshape(-1, 6) @ w.reshape(5, 6).T + b
+    np.testing.assert_allclose(got.reshape(-1, 5), ref, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- I2
+def delta_w(C, kt, kh, kw, perm=None):
+    w = np.zeros((C, 3, 3, 3, C))
+    for o in range(C):
+        w[o, kt, kh, kw, o if perm is None else perm[o]] = 1.0
+    return w
+
+
+def test_I2_delta_identity_exact():
+    a = rand((1, 4, 5, 6, 3), 4)
+    got = oracle.causal_conv3d(a, delta_w(3, 2, 1, 1), np.zeros(3))
+    assert np.array_equal(got, a)
+
+
+@pytest.mark.parametrize("kt", [0, 1])
+def test_I2_delta_time_shift_causal(kt):
+    a = rand((2, 5, 3, 4, 2), 5)
+    got = oracle.causal_conv3d(a, delta_w(2, kt, 1, 1), np.zeros(2))
+    shift = 2 - kt
+    assert np.array_equal(got[:, shift:], a[:, :5 - shift])
+    assert np.all(got[:, :shift] == 0)
+
+
+@pytest.mark.parametrize("kh,kw", [(0, 1), (2, 1), (1, 0), (1, 2), (0, 0), (2, 2)])
+def test_I2_delta_spatial_shift_zero_border(kh, kw):
+    a = rand((1, 2, 5, 6, 2), 6)
+    got = oracle.causal_conv3d(a, delta_w(2, 2, kh, kw), np.zeros(2))
+    dy, dx = kh - 1, kw - 1
+    ref = np.zeros_like(a)
+    H, W = 5, 6
+    for y in range(H):
+        for x in range(W):
+            if 0 <= y + dy < H and 0 <= x + dx < W:
+                ref[:, :, y, x] = a[:, :, y + dy, x + dx]
+    assert np.array_equal(got, ref)
+
+
+def test_I2_delta_reads_cache_frames():
+    a = rand((1, 3, 2, 3, 2), 7)
+    cache = rand((1, 2, 2, 3, 2), 8)
+    got = oracle.causal_conv3d(a, delta_w(2, 0, 1, 1), np.zeros(2), cache=cache)
+    assert np.array_equal(got[:, 0], cache[:, 0])
+    assert np.array_equal(got[:, 1], cache[:, 1])
+    assert np.array_equal(got[:, 2], a[:, 0])
+
+
+def test_I2_channel_permutation_pins_o_c_order():
+    perm = [2, 0, 3, 1]
+    a = rand((1, 2, 3, 3, 4), 9)
+    got = oracle.causal_conv3d(a, delta_w(4, 2, 1, 1, perm), np.zeros(4))
+    assert np.array_equal(got, a[..., perm])
+
+
+# ---------------------------------------------------------------- I3
+@pytest.mark.parametrize("ci,co", [(8, 8), (8, 16)])
+def test_I3_block_is_causal(ci, co):
+    p = make_params(ci, co, 10)
+    x = rand((1, 6, 4, 5, ci), 11)
+    y = oracle.resblock_forward(x, p)
+    for t in range(5):
+        x2 = x.copy()
+        x2[:, t + 1:] += rand(x2[:, t + 1:].shape, 12 + t)
+        y2 = oracle.resblock_forward(x2, p)
+        assert np.array_equal(y2[:, :t + 1], y[:, :t + 1])
+        assert not np.array_equal(y2[:, t + 1:], y[:, t + 1:])
+
+
+# ---------------------------------------------------------------- I4
+@pytest.mark.parametrize("chunks", [[1] * 7, [2, 2, 2, 1], [5, 2], [3, 1, 3]])
+@pytest.mark.parametrize("ci,co", [(8, 8), (16, 8)])
+def test_I4_fullT_equals_streaming(chunks, ci, co):
+    p = make_params(ci, co, 20)
+    x = rand((2, 7, 4, 5, ci), 21)
+    full = oracle.resblock_forward(x, p)
+    cA = cB = None
+    outs, t0 = [], 0
+    for n in chunks:
+        y, cA, cB = oracle.resblock_forward(x[:, t0:t0 + n], p, cA, cB, streaming=True)
+        outs.append(y)
+        t0 += n
+    assert np.array_equal(np.concatenate(outs, axis=1), full)
+
+
+def test_I4_save_and_resume_cache():
+    p = make_params(8, 8, 22)
+    x = rand((1, 6, 3, 4, 8), 23)
+    cA = cB = None
+    ys = []
+    for t in range(3):
+        y, cA, cB = oracle.resblock_forward(x[:, t:t + 1], p, cA, cB, streaming=True)
+        ys.append(y)
+    saved = (cA.copy(), cB.copy())
+    # an interruption: unrelated work through a fresh cache, then resume
+    oracle.resblock_forward(rand((1, 2, 3, 4, 8), 24), p, None, np.zeros((1, 2, 3, 4, 8)))
+    cA, cB = saved
+    for t in range(3, 6):
+        y, cA, cB = oracle.resblock_forward(x[:, t:t + 1], p, cA, cB, streaming=True)
+        ys.append(y)
+    assert np.array_equal(np.concatenate(ys, axis=1), oracle.resblock_forward(x, p))
+
+
+def test_I4_cache_next_definition():
+    c = rand((1, 2, 2, 2, 3), 25)
+    x1 = rand((1, 1, 2, 2, 3), 26)
+    n1 = oracle.cache_next(c, x1)
+    assert np.array_equal(n1[:, 0], c[:, 1]) and np.array_equal(n1[:, 1], x1[:, 0])
+    x3 = rand((1, 3, 2, 2, 3), 27)
+    assert np.array_equal(oracle.cache_next(c, x3), x3[:, 1:])
+    assert np.array_equal(oracle.cache_next(None, x1)[:, 0], np.zeros((1, 2, 2, 3)))
+
+
+# ---------------------------------------------------------------- I5
+@pytest.mark.parametrize("B,T,H,W,ci,co", [
+    (1, 3, 4, 5, 4, 4), (2, 4, 3, 6, 8, 8), (1, 2, 5, 3, 8, 4), (2, 3, 4, 4, 4, 8),
+    (1, 1, 1, 1, 8, 8), (1, 4, 6, 2, 2, 6),
+])
+def test_I5_block_matches_torch_functional(B, T, H, W, ci, co):
+    p = make_params(ci, co, 30 + ci + co)
+    x = rand((B, T, H, W, ci), 31)
+    np.testing.assert_allclose(oracle.resblock_forward(x, p), torch_resblock(x, p),
+                               rtol=1e-11, atol=1e-11)
+
+
+def test_I5_conv_with_shortcut_param_but_equal_channels():
+    # a 1x1x1 shortcut conv is also legal when c_in == c_out
+    p = make_params(8, 8, 33, shortcut=True)
+    x = rand((1, 3, 4, 4, 8), 34)
+    np.testing.assert_allclose(oracle.resblock_forward(x, p), torch_resblock(x, p),
+                               rtol=1e-11, atol=1e-11)
+
+
+def test_I5_brute_force_tiny_workload():
+    """The 'tiny' workload ([1,3,16,16,32], seed 0) end to end, every element."""
+    dims, ci, co, _ = synth.WORKLOADS["tiny"]
+    x, pd = synth.make_resblock_inputs(dims, ci, co, seed=0)
+    p = oracle.Params.from_dict(pd)
+    xd = x.double().numpy()
+    np.testing.assert_allclose(oracle.resblock_forward(xd, p), torch_resblock(xd, p),
+                               rtol=1e-11, atol=1e-11)
+
+
+def test_I5_conv3_matches_torch():
+    x = rand((2, 4, 5, 3, 6), 35)
+    w = rand((7, 3, 3, 3, 6), 36)
+    b = rand((7,), 37)
+    ref = F.conv3d(F.pad(torch.from_numpy(x).permute(0, 4, 1, 2, 3), (1, 1, 1, 1, 2, 0)),
+                   torch.from_numpy(w).permute(0, 4, 1, 2, 3), torch.from_numpy(b))
+    np.testing.assert_allclose(oracle.causal_conv3d(x, w, b),
+                               ref.permute(0, 2, 3, 4, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- I6
+def test_I6_norm_invariants():
+    C = 12
+    x = rand((50, C), 40)
+    g = np.random.default_rng(41).uniform(0.5, 1.5, C)
+    n = oracle.rms_norm_silu(x, g, silu=False)
+    np.testing.assert_allclose(np.sum((n / (math.sqrt(C) * g)) ** 2, axis=1), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.rms_norm_silu(3.7 * x, g, silu=False), n, rtol=1e-13)
+    assert np.array_equal(oracle.rms_norm_silu(np.zeros((2, C)), g), np.zeros((2, C)))
+
+
+def test_I6_norm_closed_form_and_eps_clamp():
+    # x = (3, 4): |x| = 5, sqrt(D) = sqrt(2)
+    g = np.array([1.0, 2.0])
+    z = np.array([3 / 5 * math.sqrt(2) * 1.0, 4 / 5 * math.sqrt(2) * 2.0])
+    np.testing.assert_allclose(oracle.rms_norm_silu(np.array([[3.0, 4.0]]), g, silu=False)[0],
+                               z, rtol=1e-15)
+    np.testing.assert_allclose(oracle.rms_norm_silu(np.array([[3.0, 4.0]]), g)[0],
+                               z / (1 + np.exp(-z)), rtol=1e-15)
+    # below eps the clamp divides by eps itself: 1e-13 * 2 / 1e-12 = 0.2
+    tiny = np.full((1, 4), 1e-13)
+    np.testing.assert_allclose(oracle.rms_norm_silu(tiny, np.ones(4), eps=1e-12, silu=False),
+                               np.full((1, 4), 0.2), rtol=1e-12)
+
+
+def test_I6_silu_sign_and_limits():
+    v = np.array([[-30.0, 0.0, 30.0]])
+    s = oracle.rms_norm_silu(v, np.ones(3), silu=True)
+    zn = oracle.rms_norm_silu(v, np.ones(3), silu=False)
+    assert s[0, 0] < 0 and abs(s[0, 0]) < 0.3 and s[0, 1] == 0
+    np.testing.assert_allclose(s[0, 2], zn[0, 2] / (1 + math.exp(-zn[0, 2])), rtol=1e-15)
+
+
+# ---------------------------------------------------------------- I7
+@pytest.mark.parametrize("ci,co", [(6, 6), (6, 4)])
+def test_I7_closed_form_at_zero_input(ci, co):
+    p = make_params(ci, co, 50)
+    B, T, H, W = 1, 4, 4, 5
+    x = np.zeros((B, T, H, W, ci))
+    y = oracle.resblock_forward(x, p)
+    # a1 = 0, so h = bA at every voxel and a2 = silu(norm(bA)) is one vector
+    nb = np.linalg.norm(p.bA)
+    z = p.bA / nb * math.sqrt(co) * p.gamma2
+    a2 = z / (1 + np.exp(-z))
+    ref = np.zeros((B, T, H, W, co))
+    for t in range(T):
+        for yy in range(H):
+            for xx in range(W):
+                acc = p.bB.copy()
+                for kt in range(3):
+                    for kh in range(3):
+                        for kw in range(3):
+                            if t + kt - 2 >= 0 and 0 <= yy + kh - 1 < H and 0 <= xx + kw - 1 < W:
+                                acc += p.wB[:, kt, kh, kw, :] @ a2
+                ref[0, t, yy, xx] = acc + (0.0 if p.wS is None else p.bS)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- points
+@pytest.mark.parametrize("ci,co", [(8, 8), (8, 4)])
+def test_points_equal_full_forward_bitwise(ci, co):
+    p = make_params(ci, co, 60)
+    x = rand((2, 6, 5, 7, ci), 61)
+    y = oracle.resblock_forward(x, p)
+    rng = np.random.default_rng(62)
+    for b in range(2):
+        pts = [(t, yy, xx) for t in (0, 1, 5) for yy in (0, 2, 4) for xx in (0, 6)]
+        pts += [tuple(rng.integers([0, 0, 0], [6, 5, 7])) for _ in range(6)]
+        got = oracle.resblock_points(torch.from_numpy(x), p, pts, b=b)
+        ref = np.stack([y[b, t, yy, xx] for t, yy, xx in pts])
+        assert np.array_equal(got, ref)
+
+
+def test_points_with_cache_equal_streaming_call():
+    p = make_params(8, 8, 63)
+    x = rand((1, 5, 4, 4, 8), 64)
+    _, cA, cB = oracle.resblock_forward(x[:, :3], p, streaming=True)
+    y, _, _ = oracle.resblock_forward(x[:, 3:], p, cA, cB)
+    pts = [(t, yy, xx) for t in (0, 1) for yy in (0, 3) for xx in (0, 1, 3)]
+    got = oracle.resblock_points(torch.from_numpy(x[:, 3:].copy()), p, pts, cA, cB)
+    assert np.array_equal(got, np.stack([y[0, t, yy, xx] for t, yy, xx in pts]))
+
+
+def test_bf16_widening_is_exact():
+    t = synth.make_tensor((64,), seed=3)
+    v = t.float().numpy().astype(np.float64)
+    assert np.array_equal(oracle._f64(t), v)
