@@ -1,0 +1,184 @@
+/*
+ * wanvae.h -- C ABI of libwanvae.so: the Wan 2.2 VAE decoder ResidualBlock
+ * forward pass on one NVIDIA GB300 (sm_103a), NDHWC bf16 end to end.
+ *
+ * The block ("Sharding of WAN 2.2 VAE", section "Channel sharding (in
+ * Megatron style)", ResidualBlock listing and op-sequence figure):
+ *
+ *     a1 = SiLU(RMS_norm(x;  gamma1))            RMS over channels, C = c_in
+ *     h  = CausalConv3d_A(a1)                    3x3x3, c_in  -> c_out
+ *     a2 = SiLU(RMS_norm(h;  gamma2))            C = c_out
+ *     r  = CausalConv3d_B(a2)                    3x3x3, c_out -> c_out
+ *     y  = r + shortcut(x)                       1x1x1 conv, or Identity when
+ *                                                c_in == c_out and no wS given
+ *
+ * RMS_norm ("Closing the gap: Wan 2.2 14B VAE decoder", section 4) is
+ *     RMS_norm(v)[c] = v[c] / max(||v||_2, eps) * sqrt(C) * gamma[c]
+ * with the L2 norm taken over the channels of one voxel and no bias.
+ * CausalConv3d ("Closing the gap", section 2; "Sharding of WAN 2.2 VAE",
+ * Conv3D strategy table) is a stride-1 3x3x3 convolution that pads two
+ * leading frames in T (zeros, or the feat_cache frames) and one element on
+ * each side of H and W (zeros):
+ *     out[b,t,y,x,o] = bias[o] + sum_{kt,kh,kw,c} w[o,kt,kh,kw,c]
+ *                          * in[b, t+kt-2, y+kh-1, x+kw-1, c].
+ * kt = 2 is the current frame, kt = 0 is frame t-2.
+ *
+ * Conventions for every call:
+ *  - Layout: activations are NDHWC ([B][T][H][W][C], C fastest, densely
+ *    packed); conv weights are [c_out][kT][kH][kW][c_in] bf16 (k = 3 or 1);
+ *    gammas and biases are fp32.  bf16 pointers are typed `void *` so that
+ *    the header needs no CUDA include; they hold IEEE bfloat16 bit patterns.
+ *  - Memory: every pointer argument is DEVICE memory owned by the caller,
+ *    except where a comment says "host".  The library never allocates,
+ *    frees or synchronises on these calls; all work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream).
+ *  - Requirements: C (each of c_in, c_out) a multiple of 16 and at most 512;
+ *    all device pointers 16-byte aligned; outputs must not alias inputs;
+ *    every dimension >= 1 and B*T*H*W < 2^31 voxels.
+ *  - Errors: argument errors are returned synchronously, before any launch,
+ *    and nothing is enqueued.  A failed launch returns WANVAE_ERR_CUDA.
+ *    Every device-side wait is bounded; a wait that runs out sets a device
+ *    flag that wanvae_sync_status() reports as WANVAE_ERR_TIMEOUT.
+ *  - The library never prints and never exits the process.
+ */
+#ifndef WANVAE_H
+#define WANVAE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WANVAE_OK = 0,
+    WANVAE_ERR_INVALID_ARG = 1, /* null pointer, bad size, aliasing, bad enum */
+    WANVAE_ERR_UNSUPPORTED = 2, /* legal block, but a size this build rejects */
+    WANVAE_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+    WANVAE_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required */
+    WANVAE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+    WANVAE_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out */
+} wanvae_status;
+
+typedef enum { WANVAE_BF16 = 0, WANVAE_F32 = 1 } wanvae_dtype;
+
+/* The CUDA stream type, declared without including the CUDA headers
+ * (identical to cudaStream_t). */
+typedef struct CUstream_st *wanvae_stream;
+
+/* Clip extent; the channel count is passed separately. */
+typedef struct {
+    int64_t B, T, H, W;
+} wanvae_dims;
+
+/* ResidualBlock parameters (all device pointers, caller-owned). */
+typedef struct {
+    int64_t c_in, c_out;
+    float eps;            /* RMS_norm clamp; 1e-12 reproduces F.normalize */
+    const float *gamma1;  /* [c_in]  RMS_norm 1 scale */
+    const float *gamma2;  /* [c_out] RMS_norm 2 scale */
+    const void *wA;       /* bf16 [c_out][3][3][3][c_in]  conv A */
+    const float *bA;      /* [c_out] */
+    const void *wB;       /* bf16 [c_out][3][3][3][c_out] conv B */
+    const float *bB;      /* [c_out] */
+    const void *wS;       /* bf16 [c_out][1][1][1][c_in] shortcut, or NULL =
+                             Identity (then c_in must equal c_out) */
+    const float *bS;      /* [c_out] shortcut bias, or NULL (= zeros) */
+} wanvae_resblock_params;
+
+/* feat_cache of one ResidualBlock for frame-by-frame decode ("Sharding of
+ * WAN 2.2 VAE", section "Why depth sharding is not beneficial": the cache
+ * holds the last frames of each CausalConv3d's input).  Each buffer holds
+ * the two frames that precede the call's first frame, of that conv's input
+ * (post norm+SiLU): convA_in bf16 [B][2][H][W][c_in], convB_in bf16
+ * [B][2][H][W][c_out], frame 0 = t-2, frame 1 = t-1.  The caller zero-fills
+ * both before the clip's first frame.  A call reads them and then replaces
+ * them, in stream order, with the last two frames of concat(cache, this
+ * call's conv input). */
+typedef struct {
+    void *convA_in;
+    void *convB_in;
+} wanvae_resblock_cache;
+
+/* Human-readable name of a status (static string, never NULL). */
+const char *wanvae_status_string(wanvae_status s);
+
+/* Library ABI version: 100 * major + minor. */
+int wanvae_version(void);
+
+/* SiLU(RMS_norm(x)) over the channels of n_voxels voxels ("Closing the gap",
+ * section 4: one fused norm + SiLU kernel).
+ *   x, y    : [n_voxels][C] of type dt (bf16 or fp32), y may not alias x.
+ *   gamma   : fp32 [C].
+ *   Math in fp32; bf16 outputs are rounded to nearest-even.
+ * Errors: INVALID_ARG (null, n_voxels < 1, C < 16 or C % 16, C > 4096, bad
+ * dt), MISALIGNED, CUDA. */
+wanvae_status wanvae_rmsnorm_silu(const void *x, void *y, const float *gamma,
+                                  wanvae_dtype dt, int64_t n_voxels, int64_t C,
+                                  float eps, wanvae_stream stream);
+
+/* One CausalConv3d (definition above), bf16 in/out, fp32 accumulate.
+ *   x     : bf16 [B][T][H][W][c_in]      y: bf16 [B][T][H][W][c_out]
+ *   w     : bf16 [c_out][k][k][k][c_in]  bias: fp32 [c_out] (NULL = zeros)
+ *   k     : 3 (causal 3x3x3) or 1 (pointwise; cache must be NULL)
+ *   cache : NULL for a whole clip (zero causal pad), or bf16 [B][2][H][W][c_in]
+ *           holding the two frames before x (read, then replaced in stream
+ *           order by the last two frames of concat(cache, x)).
+ * Errors: INVALID_ARG, UNSUPPORTED (c_in or c_out not a multiple of 16 or
+ * above 512), MISALIGNED, CUDA. */
+wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bias,
+                                   void *y, wanvae_dims d, int64_t c_in, int64_t c_out,
+                                   int k, void *cache, wanvae_stream stream);
+
+/* Bytes of device workspace wanvae_resblock_forward needs for these sizes
+ * (the bf16 conv inputs a1 and a2, 256-byte aligned).  0 on invalid sizes. */
+size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out);
+
+/* The whole ResidualBlock forward.
+ *   x : bf16 [B][T][H][W][c_in];  y : bf16 [B][T][H][W][c_out]
+ *   cache : NULL for full-T (the whole clip at once, zero causal pad), or a
+ *           feat_cache (see wanvae_resblock_cache) for one streaming call of
+ *           T frames (T = 1 for frame-by-frame decode).
+ *   workspace : device buffer of at least
+ *               wanvae_resblock_workspace_size(d, c_in, c_out) bytes, 256-byte
+ *               aligned; contents on entry are ignored.
+ * Kernels: fused RMS_norm1+SiLU; conv A with RMS_norm2+SiLU fused into its
+ * epilogue; conv B with bias, shortcut GEMM and residual add fused into it.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+wanvae_status wanvae_resblock_forward(const wanvae_resblock_params *p, const void *x,
+                                      void *y, wanvae_dims d,
+                                      const wanvae_resblock_cache *cache,
+                                      void *workspace, size_t ws_bytes,
+                                      wanvae_stream stream);
+
+/* Same as wanvae_resblock_forward, and records four caller-created CUDA
+ * events (cudaEvent_t values passed as void *, host array of 4) on `stream`:
+ * [0] before RMS_norm1, [1] before conv A, [2] before conv B, [3] after the
+ * last kernel.  Used to time each kernel inside a whole step. */
+wanvae_status wanvae_resblock_forward_profiled(const wanvae_resblock_params *p,
+                                               const void *x, void *y, wanvae_dims d,
+                                               const wanvae_resblock_cache *cache,
+                                               void *workspace, size_t ws_bytes,
+                                               void *const *events, wanvae_stream stream);
+
+/* Synchronises `stream`, then returns WANVAE_ERR_TIMEOUT (and clears the
+ * flag) if any kernel of this library on the current device gave up a
+ * bounded wait since the last call, WANVAE_ERR_CUDA if the stream reports an
+ * error, else WANVAE_OK.  Not for the hot path. */
+wanvae_status wanvae_sync_status(wanvae_stream stream);
+
+/* Upper bound, in nanoseconds, of every device-side wait in later launches
+ * (default 1e9, i.e. one second).  0 makes the first wait that is not
+ * already satisfied give up at once: a test hook for the timeout path.
+ * Host-side setting, process-wide. */
+void wanvae_set_wait_limit_ns(uint64_t ns);
+
+/* Number of kernels this library has enqueued since load (host counter). */
+uint64_t wanvae_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WANVAE_H */

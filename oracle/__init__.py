@@ -43,8 +43,8 @@ def lib():
         L.oracle_resblock_forward.argtypes = [vp, ctypes.POINTER(OracleParams), i64, i64, i64,
                                               i64, vp, vp, vp]
         L.oracle_resblock_forward.restype = ci
-        L.oracle_resblock_points.argtypes = [vp, i64, i64, i64, i64, i64, i64, i64, i64,
-                                             ctypes.POINTER(OracleParams), vp, vp, i64, vp, vp]
+        L.oracle_resblock_points.argtypes = [vp, vp, i64, i64, ctypes.POINTER(OracleParams), vp,
+                                             vp, i64, vp, vp]
         L.oracle_resblock_points.restype = ci
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
@@ -150,10 +150,10 @@ def resblock_forward(x, params: Params, cacheA=None, cacheB=None, streaming=None
 def resblock_points(x, params: Params, pts, cacheA=None, cacheB=None, b=0):
     """ResidualBlock output at sampled voxels pts [(t,y,x), ...] of batch b.
 
-    x may be a torch tensor of any float dtype with the full clip
-    [B,T,H,W,Ci]; only each point's receptive field is widened to fp64.
+    x may be a torch tensor (CPU or CUDA, any float dtype) with the whole
+    clip [B,T,H,W,Ci]; only each point's receptive field is widened to fp64.
     cacheA/cacheB: [B,2,H,W,C] caches at the start of the call, or None.
-    Returns [npts, c_out] fp64.
+    Returns [npts, c_out] fp64.  Points run in parallel in the C oracle.
     """
     pts = np.asarray(pts, dtype=np.int64).reshape(-1, 3)
     B, T, H, W, Ci = x.shape
@@ -161,14 +161,15 @@ def resblock_points(x, params: Params, pts, cacheA=None, cacheB=None, b=0):
     ps = params.c_struct()
     cA = _f64(cacheA[b]) if cacheA is not None else None
     cB = _f64(cacheB[b]) if cacheB is not None else None
+    wins, meta = [], np.empty((len(pts), 6), dtype=np.int64)
     for i, (t, yy, xx) in enumerate(pts):
         t0, y0, x0 = max(0, t - 4), max(0, yy - 2), max(0, xx - 2)
         t1, y1, x1 = t + 1, min(H, yy + 3), min(W, xx + 3)
-        win = _f64(x[b, t0:t1, y0:y1, x0:x1])
-        pt = np.array([t, yy, xx], dtype=np.int64)
-        rc = lib().oracle_resblock_points(_ptr(win), t0, y0, x0, t1 - t0, y1 - y0, x1 - x0,
-                                          H, W, ctypes.byref(ps), _ptr(cA), _ptr(cB), 1,
-                                          _ptr(pt), _ptr(out[i]))
-        if rc:
-            raise ValueError("oracle_resblock_points rejected its arguments")
+        wins.append(_f64(x[b, t0:t1, y0:y1, x0:x1]))
+        meta[i] = (t0, y0, x0, t1 - t0, y1 - y0, x1 - x0)
+    ptrs = (ctypes.c_void_p * max(1, len(wins)))(*[w.ctypes.data for w in wins])
+    rc = lib().oracle_resblock_points(ptrs, _ptr(meta), H, W, ctypes.byref(ps), _ptr(cA),
+                                      _ptr(cB), len(pts), _ptr(pts), _ptr(out))
+    if rc:
+        raise ValueError("oracle_resblock_points rejected its arguments")
     return out

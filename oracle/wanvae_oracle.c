@@ -265,16 +265,16 @@ done:
 /* each of those needs a1 on its own 3x3x3 neighbourhood, so x on       */
 /* t-4..t, y-2..y+2, x-2..x+2).  Same arithmetic, in the same order, as */
 /* oracle_resblock_forward, so the two agree bit for bit.               */
-/*   xwin: x of batch element b on frames [xt0, xt0+xnT), rows          */
-/*         [xy0, xy0+xnH), columns [xx0, xx0+xnW), channels c_in; it    */
-/*         must cover the receptive field of every point clipped to the */
-/*         clip.  cacheA/cacheB: this batch element's caches            */
-/*         ([2][H][W][C]) as they were at the start of the call, or     */
-/*         NULL for full-T.  pts: npts (t, y, x) triples, relative to   */
+/*   xwins[i]: x of point i's batch element on frames [t0, t0+nT), rows */
+/*         [y0, y0+nH), columns [x0, x0+nW) (win[6*i..6*i+5] = t0, y0,  */
+/*         x0, nT, nH, nW), channels c_in; it must cover the point's    */
+/*         receptive field clipped to the clip.  cacheA/cacheB: the     */
+/*         point's batch element's caches ([2][H][W][C]) as they were   */
+/*         at the start of the call, or NULL for full-T (one cache pair */
+/*         for all points).  pts: npts (t, y, x) triples, relative to   */
 /*         the call's first frame.  out: [npts][c_out].                 */
-API int oracle_resblock_points(const double *xwin, int64_t xt0, int64_t xy0, int64_t xx0,
-                               int64_t xnT, int64_t xnH, int64_t xnW, int64_t H, int64_t W,
-                               const oracle_params *p, const double *cacheA,
+API int oracle_resblock_points(const double *const *xwins, const int64_t *win, int64_t H,
+                               int64_t W, const oracle_params *p, const double *cacheA,
                                const double *cacheB, int64_t npts, const int64_t *pts,
                                double *out)
 {
@@ -290,7 +290,8 @@ API int oracle_resblock_points(const double *xwin, int64_t xt0, int64_t xy0, int
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (int64_t i = 0; i < npts; ++i) {
         int64_t t = pts[3 * i], y = pts[3 * i + 1], x = pts[3 * i + 2];
-        field fx = {xwin, NULL, xnT, xnH, xnW, xt0, xy0, xx0, H, W, Ci, NULL};
+        const int64_t *wi = win + 6 * i;
+        field fx = {xwins[i], NULL, wi[3], wi[4], wi[5], wi[0], wi[1], wi[2], H, W, Ci, NULL};
         /* a1 on the 5x5x5 window t-4..t, y-2..y+2, x-2..x+2 (frames >= 0) */
         double *a1 = (double *)malloc(sizeof(double) * 125 * (size_t)Ci);
         unsigned char va1[125];

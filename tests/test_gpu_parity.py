@@ -1,0 +1,258 @@
+"""GPU parity: every kernel, called through the C ABI, against the fp64 oracle
+on the same seeded inputs.  Bar: max|err| <= 2e-2 and relative L2 <= 1e-2
+(bf16 in / fp32 accumulate); fp32-mode norm: relative L2 <= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _util import compare, sample_points, to_f64
+from video_vae_causal_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def dev(d):
+    return {k: v.to(DEV) for k, v in d.items()}
+
+
+# ------------------------------------------------------------------ norm
+@pytest.mark.parametrize("C,n", [(16, 33), (32, 1000), (48, 517), (96, 4099), (192, 2001),
+                                 (384, 6241), (4096, 37)])
+def test_rmsnorm_silu_bf16(cuda_lib, C, n):
+    x = synth.make_tensor((n, C), seed=C + n)
+    g = synth.make_tensor((C,), seed=7, dtype=torch.float32, kind="uniform", lo=0.5, hi=1.5)
+    y = cuda_lib.rmsnorm_silu(x.to(DEV), g.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.rms_norm_silu(x, g), what=f"norm bf16 C={C}")
+
+
+@pytest.mark.parametrize("C,n", [(32, 1000), (96, 777), (384, 3001)])
+def test_rmsnorm_silu_f32(cuda_lib, C, n):
+    x = synth.make_tensor((n, C), seed=C, dtype=torch.float32)
+    g = synth.make_tensor((C,), seed=8, dtype=torch.float32, kind="uniform", lo=0.5, hi=1.5)
+    y = cuda_lib.rmsnorm_silu(x.to(DEV), g.to(DEV))
+    cuda_lib.sync_status()
+    ref = oracle.rms_norm_silu(x, g)
+    got = to_f64(y)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= 1e-3, rel
+    assert np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3)) < 1e-3
+
+
+def test_rmsnorm_zero_voxels_give_zero(cuda_lib):
+    x = torch.zeros((64, 32), dtype=torch.bfloat16, device=DEV)
+    x[1::2] = 1.0
+    g = torch.ones(32, device=DEV)
+    y = cuda_lib.rmsnorm_silu(x, g)
+    cuda_lib.sync_status()
+    assert torch.all(y[0::2] == 0)
+
+
+# ------------------------------------------------------------------ conv
+CONV_CASES = [
+    # (B, T, H, W, c_in, c_out): several tiles per frame and a ragged tail
+    (1, 3, 12, 20, 64, 64),
+    (2, 2, 9, 15, 32, 48),
+    (1, 4, 5, 7, 96, 96),
+    (1, 2, 16, 16, 384, 384),
+    (1, 3, 11, 13, 64, 192),
+    (1, 2, 10, 10, 16, 16),
+    (1, 1, 3, 200, 128, 96),
+]
+
+
+def conv_inputs(B, T, H, W, ci, co, k, seed):
+    x = synth.make_tensor((B, T, H, W, ci), seed=seed)
+    bound = 1.0 / np.sqrt(k * k * k * ci)
+    w = synth.make_tensor((co, k, k, k, ci), seed=seed + 1, kind="uniform", lo=-bound, hi=bound)
+    b = synth.make_tensor((co,), seed=seed + 2, dtype=torch.float32, kind="uniform", lo=-.1, hi=.1)
+    return x, w, b
+
+
+@pytest.mark.parametrize("case", CONV_CASES)
+def test_conv3d_k3_full_clip(cuda_lib, case):
+    B, T, H, W, ci, co = case
+    x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=sum(case))
+    y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.causal_conv3d(x, w, b), what=f"conv3 {case}")
+
+
+@pytest.mark.parametrize("case", [(1, 3, 12, 20, 64, 64), (2, 2, 9, 15, 32, 48),
+                                  (1, 2, 7, 9, 384, 192)])
+def test_conv3d_k1(cuda_lib, case):
+    B, T, H, W, ci, co = case
+    x, w, b = conv_inputs(B, T, H, W, ci, co, 1, seed=5 + sum(case))
+    y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.causal_conv3d(x, w, b), what=f"conv1 {case}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_conv3d_with_cache_reads_and_updates_cache(cuda_lib, T):
+    B, H, W, ci, co = 2, 9, 14, 64, 32
+    x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=40 + T)
+    cache = synth.make_tensor((B, 2, H, W, ci), seed=50 + T)
+    cache_d = cache.to(DEV)
+    y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV), cache=cache_d)
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.causal_conv3d(x, w, b, cache=cache), what=f"conv3 cache T={T}")
+    assert np.array_equal(to_f64(cache_d), oracle.cache_next(cache, x))
+
+
+def test_conv3d_no_bias_and_output_guard_bands(cuda_lib):
+    B, T, H, W, ci, co = 1, 2, 9, 11, 32, 32
+    x, w, _ = conv_inputs(B, T, H, W, ci, co, 3, seed=60)
+    n = B * T * H * W * co
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 12345.0, dtype=torch.bfloat16, device=DEV)
+    y = buf[guard:guard + n].view(B, T, H, W, co)
+    cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), None, y=y)
+    cuda_lib.sync_status()
+    assert torch.all(buf[:guard] == 12345.0) and torch.all(buf[guard + n:] == 12345.0)
+    compare(to_f64(y), oracle.causal_conv3d(x, w, np.zeros(co)), what="conv no bias")
+
+
+# ------------------------------------------------------------------ block
+BLOCK_CASES = [
+    # (B, T, H, W, c_in, c_out)
+    (1, 3, 16, 16, 32, 32),     # the 'tiny' workload
+    (1, 5, 20, 24, 64, 64),
+    (2, 3, 10, 13, 64, 32),     # channel-reducing, 1x1x1 shortcut
+    (1, 3, 10, 12, 384, 384),
+    (1, 2, 8, 8, 384, 192),
+    (1, 4, 9, 11, 96, 96),
+    (1, 1, 1, 1, 32, 32),       # one voxel: every spatial/temporal tap but one is padding
+]
+
+
+def block_inputs(case, seed):
+    B, T, H, W, ci, co = case
+    return synth.make_resblock_inputs((B, T, H, W), ci, co, seed=seed)
+
+
+@pytest.mark.parametrize("case", BLOCK_CASES)
+def test_resblock_fullT(cuda_lib, case):
+    x, p = block_inputs(case, seed=0)
+    y = cuda_lib.resblock_forward(x.to(DEV), dev(p))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
+            what=f"block {case}")
+
+
+def test_resblock_with_shortcut_and_equal_channels(cuda_lib):
+    x, p = synth.make_resblock_inputs((1, 3, 9, 10), 64, 64, seed=3, shortcut=True)
+    y = cuda_lib.resblock_forward(x.to(DEV), dev(p))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.resblock_forward(x, oracle.Params.from_dict(p)), what="block wS")
+
+
+@pytest.mark.parametrize("case,chunks", [((1, 6, 12, 14, 64, 64), [1] * 6),
+                                         ((2, 5, 9, 10, 64, 32), [2, 2, 1]),
+                                         ((1, 4, 8, 8, 384, 384), [1, 3])])
+def test_resblock_streaming_equals_fullT(cuda_lib, case, chunks):
+    B, T, H, W, ci, co = case
+    x, p = block_inputs(case, seed=11)
+    xd, pd = x.to(DEV), dev(p)
+    full = cuda_lib.resblock_forward(xd, pd)
+    cA = torch.zeros((B, 2, H, W, ci), dtype=torch.bfloat16, device=DEV)
+    cB = torch.zeros((B, 2, H, W, co), dtype=torch.bfloat16, device=DEV)
+    outs, t0 = [], 0
+    for n in chunks:
+        outs.append(cuda_lib.resblock_forward(xd[:, t0:t0 + n].contiguous(), pd, cache=(cA, cB)))
+        t0 += n
+    stream = torch.cat(outs, dim=1)
+    cuda_lib.sync_status()
+    # Same rounding points and accumulation order in both modes: bit-exact.
+    assert torch.equal(stream, full)
+    compare(to_f64(stream), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
+            what=f"stream {case}")
+
+
+def test_resblock_deterministic(cuda_lib):
+    x, p = block_inputs((1, 4, 16, 20, 64, 64), seed=12)
+    xd, pd = x.to(DEV), dev(p)
+    y1 = cuda_lib.resblock_forward(xd, pd)
+    y2 = cuda_lib.resblock_forward(xd, pd)
+    cuda_lib.sync_status()
+    assert torch.equal(y1, y2)
+
+
+def test_resblock_causal_on_gpu(cuda_lib):
+    case = (1, 5, 8, 12, 64, 64)
+    x, p = block_inputs(case, seed=13)
+    pd = dev(p)
+    y = cuda_lib.resblock_forward(x.to(DEV), pd)
+    x2 = x.clone()
+    x2[:, 3:] = synth.make_tensor(x2[:, 3:].shape, seed=99)
+    y2 = cuda_lib.resblock_forward(x2.to(DEV), pd)
+    cuda_lib.sync_status()
+    assert torch.equal(y[:, :3], y2[:, :3])
+
+
+# ------------------------------------------------------------------ full sizes, sampled
+FULL = [
+    ("latent_fullT", 48),
+    ("reduce_384_192", 24),
+    ("fullres_96", 48),
+]
+
+
+@pytest.mark.parametrize("name,nrand", FULL)
+def test_full_size_sampled(cuda_lib, name, nrand):
+    dims, ci, co, _ = synth.WORKLOADS[name]
+    B, T, H, W = dims
+    x, p = synth.make_resblock_inputs(dims, ci, co, seed=0, device=DEV)
+    y = cuda_lib.resblock_forward(x, p)
+    cuda_lib.sync_status()
+    pts = sample_points(T, H, W, nrand, seed=1)
+    op = oracle.Params.from_dict(p)
+    ref = oracle.resblock_points(x, op, pts)
+    idx = torch.tensor(pts, device=DEV)
+    got = y[0, idx[:, 0], idx[:, 1], idx[:, 2]]
+    compare(to_f64(got), ref, what=name)
+    assert torch.isfinite(y).all()
+
+
+def test_streaming_720p_21_calls_sampled(cuda_lib):
+    dims, ci, co, calls = synth.WORKLOADS["stream_720p"]
+    B, T, H, W = dims
+    x, p = synth.make_resblock_inputs(dims, ci, co, seed=0, device=DEV)
+    cA = torch.zeros((B, 2, H, W, ci), dtype=torch.bfloat16, device=DEV)
+    cB = torch.zeros((B, 2, H, W, co), dtype=torch.bfloat16, device=DEV)
+    ws = cuda_lib.make_workspace((B, 1, H, W), ci, co)
+    outs = [cuda_lib.resblock_forward(x[:, t:t + 1].contiguous(), p, cache=(cA, cB), workspace=ws)
+            for t in range(calls)]
+    y = torch.cat(outs, dim=1)
+    full = cuda_lib.resblock_forward(x, p)
+    cuda_lib.sync_status()
+    assert torch.equal(y, full)  # output must equal full-T
+    pts = sample_points(T, H, W, 24, seed=2)
+    ref = oracle.resblock_points(x, oracle.Params.from_dict(p), pts)
+    idx = torch.tensor(pts, device=DEV)
+    compare(to_f64(y[0, idx[:, 0], idx[:, 1], idx[:, 2]]), ref, what="stream 720p")
+
+
+# ------------------------------------------------------------------ failure path
+def test_bounded_wait_timeout_reports_and_context_survives(cuda_lib):
+    """A zero wait bound makes the conv's first unsatisfied wait give up: the
+    kernel drains its in-flight copies, frees TMEM, returns, and the host
+    reads WANVAE_ERR_TIMEOUT.  The context must stay usable."""
+    B, T, H, W, ci, co = 1, 2, 16, 16, 64, 64
+    x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=70)
+    xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
+    cuda_lib.sync_status()
+    try:
+        cuda_lib.set_wait_limit_ns(0)
+        cuda_lib.causal_conv3d(xd, wd, bd)
+        with pytest.raises(cuda_lib.WanvaeError) as ei:
+            cuda_lib.sync_status()
+        assert ei.value.status == cuda_lib.ERR_TIMEOUT
+    finally:
+        cuda_lib.set_wait_limit_ns(10 ** 9)
+    y = cuda_lib.causal_conv3d(xd, wd, bd)
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.causal_conv3d(x, w, b), what="after timeout")

@@ -1,0 +1,326 @@
+// api.cu -- the C ABI declared in include/wanvae.h: argument checks, the
+// per-device error word, and the composition of the ResidualBlock
+// ("Sharding of WAN 2.2 VAE", ResidualBlock listing: norm1, SiLU, conv A,
+// norm2, SiLU, conv B, shortcut, residual add) out of the kernels.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/wanvae.h"
+#include "kernels.h"
+
+using namespace wanvae;
+
+// Device error word: kernels OR error bits into it; wanvae_sync_status reads
+// and clears it.
+__device__ unsigned g_wanvae_err;
+
+namespace {
+
+std::atomic<uint64_t> g_wait_ns{1000000000ull};
+std::atomic<uint64_t> g_launches{0};
+
+struct DeviceState {
+    bool ready;
+    int num_sms;
+    unsigned *err;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+wanvae_status device_state(DeviceState &out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return WANVAE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0;
+        void *p = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaGetSymbolAddress(&p, g_wanvae_err) != cudaSuccess)
+            return WANVAE_ERR_CUDA;
+        d.num_sms = sms;
+        d.err = static_cast<unsigned *>(p);
+        d.ready = true;
+    }
+    out = d;
+    return WANVAE_OK;
+}
+
+wanvae_status make_ctx(LaunchCtx &ctx, wanvae_stream s) {
+    DeviceState d;
+    const wanvae_status st = device_state(d);
+    if (st != WANVAE_OK) return st;
+    ctx.stream = reinterpret_cast<cudaStream_t>(s);
+    ctx.err = d.err;
+    ctx.wait_ns = g_wait_ns.load();
+    ctx.num_sms = d.num_sms;
+    return WANVAE_OK;
+}
+
+wanvae_status from_cuda(cudaError_t e) { return e == cudaSuccess ? WANVAE_OK : WANVAE_ERR_CUDA; }
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool dims_ok(const wanvae_dims &d) {
+    if (d.B < 1 || d.T < 1 || d.H < 1 || d.W < 1) return false;
+    if (d.H > (1 << 20) || d.W > (1 << 20) || d.T > (1 << 20) || d.B > (1 << 20)) return false;
+    const int64_t hw = d.H * d.W;
+    if (hw > INT32_MAX) return false;
+    const int64_t vox = d.B * d.T * hw;
+    return vox > 0 && vox < INT32_MAX;
+}
+
+int64_t voxels(const wanvae_dims &d) { return d.B * d.T * d.H * d.W; }
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char *wanvae_status_string(wanvae_status s) {
+    switch (s) {
+        case WANVAE_OK: return "ok";
+        case WANVAE_ERR_INVALID_ARG: return "invalid argument";
+        case WANVAE_ERR_UNSUPPORTED: return "unsupported size";
+        case WANVAE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case WANVAE_ERR_WORKSPACE: return "workspace missing or too small";
+        case WANVAE_ERR_CUDA: return "CUDA error";
+        case WANVAE_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int wanvae_version(void) { return 100; }
+
+void wanvae_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
+
+uint64_t wanvae_launch_count(void) { return g_launches.load(); }
+
+wanvae_status wanvae_rmsnorm_silu(const void *x, void *y, const float *gamma, wanvae_dtype dt,
+                                  int64_t n_voxels, int64_t C, float eps, wanvae_stream stream) {
+    if (!x || !y || !gamma) return WANVAE_ERR_INVALID_ARG;
+    if (dt != WANVAE_BF16 && dt != WANVAE_F32) return WANVAE_ERR_INVALID_ARG;
+    if (n_voxels < 1 || n_voxels >= INT32_MAX || C < 16 || C % 16 || C > 4096)
+        return WANVAE_ERR_INVALID_ARG;
+    if (!(eps >= 0.f)) return WANVAE_ERR_INVALID_ARG;
+    if (misaligned(x) || misaligned(y) || misaligned(gamma)) return WANVAE_ERR_MISALIGNED;
+    const size_t bytes = (size_t)n_voxels * C * (dt == WANVAE_F32 ? 4 : 2);
+    if (overlap(x, bytes, y, bytes)) return WANVAE_ERR_INVALID_ARG;
+    LaunchCtx ctx;
+    const wanvae_status st = make_ctx(ctx, stream);
+    if (st != WANVAE_OK) return st;
+    g_launches++;
+    return from_cuda(launch_rmsnorm_silu(x, y, gamma, dt == WANVAE_F32, n_voxels, (int)C, eps, ctx));
+}
+
+wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bias, void *y,
+                                   wanvae_dims d, int64_t c_in, int64_t c_out, int k, void *cache,
+                                   wanvae_stream stream) {
+    if (!x || !w || !y) return WANVAE_ERR_INVALID_ARG;
+    if (k != 1 && k != 3) return WANVAE_ERR_INVALID_ARG;
+    if (k == 1 && cache) return WANVAE_ERR_INVALID_ARG;
+    if (!dims_ok(d) || c_in < 1 || c_out < 1) return WANVAE_ERR_INVALID_ARG;
+    if (c_in % 16 || c_out % 16 || c_in > 512 || c_out > 512) return WANVAE_ERR_UNSUPPORTED;
+    if (misaligned(x) || misaligned(w) || misaligned(y) || misaligned(bias) || misaligned(cache))
+        return WANVAE_ERR_MISALIGNED;
+    const int64_t M = voxels(d);
+    const size_t xb = (size_t)M * c_in * 2, yb = (size_t)M * c_out * 2;
+    const size_t cb = (size_t)d.B * 2 * d.H * d.W * c_in * 2;
+    if (overlap(x, xb, y, yb)) return WANVAE_ERR_INVALID_ARG;
+    if (cache && (overlap(cache, cb, y, yb) || overlap(cache, cb, x, xb)))
+        return WANVAE_ERR_INVALID_ARG;
+
+    ConvSpec s;
+    memset(&s, 0, sizeof(s));
+    s.in = x;
+    s.cache = cache;
+    s.w = w;
+    s.bias = bias;
+    s.out = y;
+    s.B = (int)d.B;
+    s.T = (int)d.T;
+    s.H = (int)d.H;
+    s.W = (int)d.W;
+    s.c_in = (int)c_in;
+    s.c_out = (int)c_out;
+    s.k = k;
+    s.epi = kEpiBias;
+    if (conv3d_supported(s)) return WANVAE_ERR_UNSUPPORTED;
+
+    LaunchCtx ctx;
+    const wanvae_status st = make_ctx(ctx, stream);
+    if (st != WANVAE_OK) return st;
+    g_launches++;
+    cudaError_t e = launch_conv3d(s, ctx);
+    if (e == cudaSuccess && cache) {
+        g_launches++;
+        e = launch_cache_update(cache, x, s.B, s.T, (int64_t)d.H * d.W * c_in * 2, ctx);
+    }
+    return from_cuda(e);
+}
+
+size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out) {
+    if (!dims_ok(d) || c_in < 1 || c_out < 1 || c_in > 4096 || c_out > 4096) return 0;
+    const size_t M = (size_t)voxels(d);
+    return align256(M * c_in * 2) + align256(M * c_out * 2);
+}
+
+static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *x, void *y,
+                                   wanvae_dims d, const wanvae_resblock_cache *cache,
+                                   void *workspace, size_t ws_bytes, void *const *events,
+                                   wanvae_stream stream) {
+    if (!p || !x || !y) return WANVAE_ERR_INVALID_ARG;
+    if (!p->gamma1 || !p->gamma2 || !p->wA || !p->wB) return WANVAE_ERR_INVALID_ARG;
+    if (!dims_ok(d) || p->c_in < 1 || p->c_out < 1) return WANVAE_ERR_INVALID_ARG;
+    if (!(p->eps >= 0.f)) return WANVAE_ERR_INVALID_ARG;
+    if (!p->wS && p->c_in != p->c_out) return WANVAE_ERR_INVALID_ARG;
+    if (!p->wS && p->bS) return WANVAE_ERR_INVALID_ARG;
+    if (cache && (!cache->convA_in || !cache->convB_in)) return WANVAE_ERR_INVALID_ARG;
+    if (p->c_in % 16 || p->c_out % 16 || p->c_in > 512 || p->c_out > 512)
+        return WANVAE_ERR_UNSUPPORTED;
+    const void *ptrs[] = {x, y, p->gamma1, p->gamma2, p->wA, p->bA, p->wB, p->bB, p->wS, p->bS,
+                          workspace, cache ? cache->convA_in : nullptr,
+                          cache ? cache->convB_in : nullptr};
+    for (const void *q : ptrs)
+        if (misaligned(q)) return WANVAE_ERR_MISALIGNED;
+
+    const int64_t M = voxels(d);
+    const size_t xb = (size_t)M * p->c_in * 2, yb = (size_t)M * p->c_out * 2;
+    const size_t need = wanvae_resblock_workspace_size(d, p->c_in, p->c_out);
+    if (!workspace || ws_bytes < need) return WANVAE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return WANVAE_ERR_MISALIGNED;
+    if (overlap(x, xb, y, yb) || overlap(workspace, need, x, xb) || overlap(workspace, need, y, yb))
+        return WANVAE_ERR_INVALID_ARG;
+    const size_t cab = (size_t)d.B * 2 * d.H * d.W * p->c_in * 2;
+    const size_t cbb = (size_t)d.B * 2 * d.H * d.W * p->c_out * 2;
+    if (cache) {
+        const void *ca = cache->convA_in, *cbp = cache->convB_in;
+        if (overlap(ca, cab, cbp, cbb) || overlap(ca, cab, x, xb) || overlap(ca, cab, y, yb) ||
+            overlap(cbp, cbb, x, xb) || overlap(cbp, cbb, y, yb) ||
+            overlap(ca, cab, workspace, need) || overlap(cbp, cbb, workspace, need))
+            return WANVAE_ERR_INVALID_ARG;
+    }
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *a1 = ws;
+    void *a2 = ws + align256((size_t)M * p->c_in * 2);
+
+    ConvSpec sA;
+    memset(&sA, 0, sizeof(sA));
+    sA.in = a1;
+    sA.cache = cache ? cache->convA_in : nullptr;
+    sA.w = p->wA;
+    sA.bias = p->bA;
+    sA.gamma = p->gamma2;
+    sA.eps = p->eps;
+    sA.out = a2;
+    sA.B = (int)d.B;
+    sA.T = (int)d.T;
+    sA.H = (int)d.H;
+    sA.W = (int)d.W;
+    sA.c_in = (int)p->c_in;
+    sA.c_out = (int)p->c_out;
+    sA.k = 3;
+    sA.epi = kEpiNormSilu;
+
+    ConvSpec sB = sA;
+    sB.in = a2;
+    sB.cache = cache ? cache->convB_in : nullptr;
+    sB.w = p->wB;
+    sB.bias = p->bB;
+    sB.gamma = nullptr;
+    sB.out = y;
+    sB.c_in = (int)p->c_out;
+    if (p->wS) {
+        sB.epi = kEpiBias;
+        sB.bias2 = p->bS;
+        sB.sc_in = x;
+        sB.sc_w = p->wS;
+        sB.c_sc = (int)p->c_in;
+    } else {
+        sB.epi = kEpiResidual;
+        sB.resid = x;
+    }
+    if (conv3d_supported(sA) || conv3d_supported(sB)) return WANVAE_ERR_UNSUPPORTED;
+
+    LaunchCtx ctx;
+    const wanvae_status st = make_ctx(ctx, stream);
+    if (st != WANVAE_OK) return st;
+    auto rec = [&](int i) -> cudaError_t {
+        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), ctx.stream)
+                      : cudaSuccess;
+    };
+    const int64_t frA = d.H * d.W * p->c_in * 2, frB = d.H * d.W * p->c_out * 2;
+    cudaError_t e = rec(0);
+    if (e == cudaSuccess) {
+        g_launches++;
+        e = launch_rmsnorm_silu(x, a1, p->gamma1, false, M, (int)p->c_in, p->eps, ctx);
+    }
+    if (e == cudaSuccess) e = rec(1);
+    if (e == cudaSuccess) {
+        g_launches++;
+        e = launch_conv3d(sA, ctx);
+    }
+    if (e == cudaSuccess && cache) {
+        g_launches++;
+        e = launch_cache_update(cache->convA_in, a1, (int)d.B, (int)d.T, frA, ctx);
+    }
+    if (e == cudaSuccess) e = rec(2);
+    if (e == cudaSuccess) {
+        g_launches++;
+        e = launch_conv3d(sB, ctx);
+    }
+    if (e == cudaSuccess && cache) {
+        g_launches++;
+        e = launch_cache_update(cache->convB_in, a2, (int)d.B, (int)d.T, frB, ctx);
+    }
+    if (e == cudaSuccess) e = rec(3);
+    return from_cuda(e);
+}
+
+wanvae_status wanvae_resblock_forward(const wanvae_resblock_params *p, const void *x, void *y,
+                                      wanvae_dims d, const wanvae_resblock_cache *cache,
+                                      void *workspace, size_t ws_bytes, wanvae_stream stream) {
+    return resblock_impl(p, x, y, d, cache, workspace, ws_bytes, nullptr, stream);
+}
+
+wanvae_status wanvae_resblock_forward_profiled(const wanvae_resblock_params *p, const void *x,
+                                               void *y, wanvae_dims d,
+                                               const wanvae_resblock_cache *cache,
+                                               void *workspace, size_t ws_bytes,
+                                               void *const *events, wanvae_stream stream) {
+    if (!events || !events[0] || !events[1] || !events[2] || !events[3])
+        return WANVAE_ERR_INVALID_ARG;
+    return resblock_impl(p, x, y, d, cache, workspace, ws_bytes, events, stream);
+}
+
+wanvae_status wanvae_sync_status(wanvae_stream stream) {
+    DeviceState d;
+    const wanvae_status st = device_state(d);
+    if (st != WANVAE_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return WANVAE_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wanvae_err, sizeof(v)) != cudaSuccess) return WANVAE_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_wanvae_err, &zero, sizeof(zero)) != cudaSuccess)
+            return WANVAE_ERR_CUDA;
+        return WANVAE_ERR_TIMEOUT;
+    }
+    return WANVAE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,635 @@
+// conv3d_tcgen05.cu -- CausalConv3d as an implicit GEMM on the sm_103a
+// tensor cores (tcgen05 MMA, accumulators in TMEM, operands staged by TMA).
+//
+// The operation ("Closing the gap: Wan 2.2 14B VAE decoder", sections 2 and 6;
+// "Sharding of WAN 2.2 VAE", Conv3D strategy table):
+//     out[b,t,y,x,o] = bias[o] + sum_{kt,kh,kw,c} w[o,kt,kh,kw,c]
+//                                  * in[b, t+kt-2, y+kh-1, x+kw-1, c]
+// with zeros (or the feat_cache frames) for t+kt-2 < 0 and zeros outside H, W.
+// GEMM view: M = B*T*H*W output voxels, N = c_out, K = 27 * c_in; the K loop
+// walks the 27 taps, each tap in chunks of channels.
+//
+// Tiling.  A CTA tile is 128 consecutive voxels of ONE frame (b, t) -- the
+// frames are tiled separately, the last tile of a frame is ragged -- by all
+// c_out channels (the accumulator is 128 TMEM lanes x c_out fp32 columns, so
+// an epilogue thread owns every channel of one voxel, which is what lets the
+// next RMS_norm run inside the epilogue).  Because a tile never spans frames,
+// every tap of a tile reads a single source frame: the conv input, the
+// feat_cache, or nothing (a zero causal-pad tap is skipped).
+//
+// A operand: one TMA im2col load per (tap, channel chunk) over the NHWC view
+// [frames][H][W][C] of the input.  The map's bounding box is the H x W frame
+// shrunk by the conv's one-element pad on each side; walking 128 pixels from
+// the tile's first voxel and reading each at (pixel + (kw, kh)) gives exactly
+// the tap-shifted rows, with out-of-frame reads filled with zeros by TMA (the
+// spatial zero pad).  B operand: the weights as a K-major [c_out][27*c_in]
+// matrix, one tiled TMA box per (chunk, N-piece).  Both land in smem with the
+// hardware swizzle that the UMMA descriptors name.
+//
+// Warp roles (192 threads, one persistent CTA per SM): warp 0 = TMA producer,
+// warp 1 = MMA issuer (and TMEM owner), warps 2-5 = epilogue, one TMEM lane
+// quarter each.  An mbarrier ring of `stages` smem buffers links producer and
+// MMA; up to two accumulators in TMEM let the epilogue of tile i overlap the
+// MMAs of tile i+1 when 2 * c_out fits in TMEM's 512 columns.  Every wait is
+// bounded (ptx.cuh).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace wanvae {
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kThreads = 192;
+constexpr int kSmemBudget = 227 * 1024;
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // cleanup waits after an abort
+
+struct ConvArgs {
+    int T, H, W, HW;
+    int c_in, c_out;
+    int taps;            // 27 or 1
+    int has_cache;
+    int sw;              // channels per swizzled sub-tile (64, 32 or 16)
+    int nsub;            // sub-tiles per pipeline stage
+    int kc_main;         // stages per tap
+    int kc_short;        // stages of the shortcut segment (0 = none)
+    int n_pieces, piece_n;
+    uint32_t layout;     // UMMA swizzle mode matching sw
+    int tiles_per_frame, num_tiles;
+    int stages;
+    uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
+    uint32_t off_bars, off_misc, off_vec;
+    int acc_cols, nacc, tmem_cols;
+    int epi;
+    float eps, sqrt_c;
+    const float *bias, *bias2, *gamma;
+    const __nv_bfloat16 *resid;
+    __nv_bfloat16 *out;
+    unsigned *err;
+    uint64_t wait_ns;
+};
+
+struct TileInfo {
+    int frame, pos, n, t, h0, w0, row0;
+};
+
+__device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
+    TileInfo ti;
+    ti.frame = tile / p.tiles_per_frame;
+    ti.pos = (tile - ti.frame * p.tiles_per_frame) * kBlockM;
+    ti.n = ti.frame / p.T;
+    ti.t = ti.frame - ti.n * p.T;
+    ti.h0 = ti.pos / p.W;
+    ti.w0 = ti.pos - ti.h0 * p.W;
+    ti.row0 = ti.frame * p.HW + ti.pos;
+    return ti;
+}
+
+// First temporal tap with a source frame: taps reading t+kt-2 < 0 are zero
+// (skipped) unless a feat_cache supplies those frames.
+__device__ __forceinline__ int first_kt(const TileInfo &ti, const ConvArgs &p) {
+    if (p.taps != 27 || p.has_cache) return 0;
+    return ti.t >= 2 ? 0 : 2 - ti.t;
+}
+
+__device__ __forceinline__ int tile_stages(const TileInfo &ti, const ConvArgs &p) {
+    const int main_taps = p.taps == 27 ? (3 - first_kt(ti, p)) * 9 : 1;
+    return main_taps * p.kc_main + p.kc_short;
+}
+
+struct Bars {
+    uint32_t base;
+    int stages;
+    __device__ uint32_t full(int s) const { return base + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + 8u * (stages + s); }
+    __device__ uint32_t accf(int a) const { return base + 8u * (2 * stages + a); }
+    __device__ uint32_t acce(int a) const { return base + 8u * (2 * stages + 2 + a); }
+    __device__ uint32_t drain() const { return base + 8u * (2 * stages + 4); }
+};
+
+__device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
+                              const CUtensorMap *mapB, const CUtensorMap *mapSA,
+                              const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
+                              const Bars &bars, const WaitCtl &wc) {
+    int stage = 0;
+    uint32_t phase = 0, fills = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileInfo ti = tile_info(tile, p);
+        const int kt0 = first_kt(ti, p);
+        const int nseg = p.taps == 27 ? (3 - kt0) * 9 : 1;
+        const int segs = nseg + (p.kc_short > 0 ? 1 : 0);
+        for (int seg = 0; ok && seg < segs; ++seg) {
+            const bool shortcut = seg == nseg;
+            int tap = 0, kh = 1, kw = 1, fidx = 0;
+            const CUtensorMap *am = mapA;
+            if (!shortcut && p.taps == 27) {
+                tap = kt0 * 9 + seg;
+                const int kt = tap / 9;
+                kh = (tap / 3) % 3;
+                kw = tap % 3;
+                const int tt = ti.t + kt - 2;
+                if (tt >= 0) {
+                    fidx = ti.n * p.T + tt;
+                } else {
+                    am = mapC;
+                    fidx = ti.n * 2 + tt + 2;
+                }
+            }
+            const int nkc = shortcut ? p.kc_short : p.kc_main;
+            for (int kc = 0; kc < nkc; ++kc) {
+                if (!mbar_wait(bars.empty(stage), phase ^ 1u, wc)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bars.full(stage);
+                mbar_arrive_expect_tx(fb, p.stage_tx);
+                const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
+                const uint32_t sb = sa + p.a_bytes;
+                for (int s = 0; s < p.nsub; ++s) {
+                    const int c0 = (kc * p.nsub + s) * p.sw;
+                    const uint32_t da = sa + (uint32_t)s * p.a_sub_bytes;
+                    if (shortcut)
+                        tma_load_2d(da, mapSA, fb, c0, ti.row0);
+                    else if (p.taps == 27)
+                        tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
+                                           (uint16_t)kw, (uint16_t)kh);
+                    else
+                        tma_load_2d(da, mapA, fb, c0, ti.row0);
+                    for (int j = 0; j < p.n_pieces; ++j) {
+                        const uint32_t db = sb + (uint32_t)s * p.b_sub_bytes +
+                                            (uint32_t)(j * p.piece_n * p.sw * 2);
+                        if (shortcut)
+                            tma_load_2d(db, mapSB, fb, c0, j * p.piece_n);
+                        else
+                            tma_load_2d(db, mapB, fb, tap * p.c_in + c0, j * p.piece_n);
+                    }
+                }
+                ++fills;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    if (!ok) {
+        // Aborted: let the newest fill of every stage land before the CTA
+        // (and its shared memory) goes away.
+        volatile int no_abort = 0;
+        const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+        const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
+        for (uint32_t f = fills - n; f < fills; ++f)
+            mbar_wait(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
+    }
+}
+
+__device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, const Bars &bars,
+                         const WaitCtl &wc) {
+    const uint32_t idesc = idesc_bf16_f32(kBlockM, p.piece_n);
+    const uint32_t row_bytes = (uint32_t)p.sw * 2u;
+    int stage = 0, it = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int a = it % p.nacc;
+        const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
+        if (!mbar_wait(bars.acce(a), aph ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_cols);
+        const int nst = tile_stages(tile_info(tile, p), p);
+        for (int k = 0; k < nst; ++k) {
+            if (!mbar_wait(bars.full(stage), phase, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
+            const uint32_t sb = sa + p.a_bytes;
+            for (int s = 0; s < p.nsub; ++s) {
+                for (int kk = 0; kk < p.sw / 16; ++kk) {
+                    const uint64_t ad =
+                        sdesc_kmajor(sa + (uint32_t)s * p.a_sub_bytes + 32u * kk, row_bytes, p.layout);
+                    const uint32_t accum = (k > 0 || s > 0 || kk > 0) ? 1u : 0u;
+                    for (int j = 0; j < p.n_pieces; ++j) {
+                        const uint64_t bd = sdesc_kmajor(
+                            sb + (uint32_t)s * p.b_sub_bytes + (uint32_t)j * p.piece_n * row_bytes +
+                                32u * kk,
+                            row_bytes, p.layout);
+                        mma_bf16_ss(dacc + (uint32_t)(j * p.piece_n), ad, bd, idesc, accum);
+                    }
+                }
+            }
+            mma_commit(bars.empty(stage));  // frees the smem stage when these MMAs finish
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        mma_commit(bars.accf(a));  // accumulator ready for the epilogue
+    }
+    // Every MMA issued above completes before TMEM is released.
+    volatile int no_abort = 0;
+    const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+    mma_commit(bars.drain());
+    mbar_wait(bars.drain(), 0u, dc);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
+                              const float *s_gamma, const Bars &bars, const WaitCtl &wc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const int a = it % p.nacc;
+        const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
+        if (!mbar_wait_warp(bars.accf(a), aph, wc)) break;
+        tc_fence_after();
+        const TileInfo ti = tile_info(tile, p);
+        const bool valid = ti.pos + row < p.HW;
+        const int64_t g = (int64_t)ti.row0 + row;
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols);
+        uint4 *out = reinterpret_cast<uint4 *>(p.out + g * p.c_out);
+        if (p.epi == kEpiNormSilu) {
+            // RMS_norm over all c_out channels of this voxel, then SiLU.
+            float ss = 0.f;
+            for (int c = 0; c < p.c_out; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tb + (uint32_t)c, r);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float v = __uint_as_float(r[i]) + s_bias[c + i];
+                    ss += v * v;
+                }
+            }
+            const float scale = p.sqrt_c / fmaxf(sqrtf(ss), p.eps);
+            for (int c = 0; c < p.c_out; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tb + (uint32_t)c, r);
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float z0 = (__uint_as_float(r[2 * i]) + s_bias[c + 2 * i]) * scale *
+                               s_gamma[c + 2 * i];
+                    float z1 = (__uint_as_float(r[2 * i + 1]) + s_bias[c + 2 * i + 1]) * scale *
+                               s_gamma[c + 2 * i + 1];
+                    z0 = z0 / (1.0f + __expf(-z0));
+                    z1 = z1 / (1.0f + __expf(-z1));
+                    o[i] = pack_bf16x2(z0, z1);
+                }
+                if (valid) {
+                    out[c / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+                    out[c / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        } else {
+            const uint4 *res = p.epi == kEpiResidual
+                                   ? reinterpret_cast<const uint4 *>(p.resid + g * p.c_out)
+                                   : nullptr;
+            for (int c = 0; c < p.c_out; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tb + (uint32_t)c, r);
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + s_bias[c + i];
+                if (res && valid) {
+                    const uint4 x0 = res[c / 8], x1 = res[c / 8 + 1];
+                    const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        v[2 * i] += __uint_as_float(xs[i] << 16);
+                        v[2 * i + 1] += __uint_as_float(xs[i] & 0xffff0000u);
+                    }
+                }
+                if (valid) {
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                    out[c / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+                    out[c / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.acce(a));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
+                      const __grid_constant__ CUtensorMap mapC,
+                      const __grid_constant__ CUtensorMap mapB,
+                      const __grid_constant__ CUtensorMap mapSA,
+                      const __grid_constant__ CUtensorMap mapSB, const ConvArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Bars bars{sbase + p.off_bars, p.stages};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_misc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_misc + 4);
+    float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
+    float *s_gamma = s_bias + p.c_out;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bars.accf(a), 1);
+            mbar_init(bars.acce(a), 4);
+        }
+        mbar_init(bars.drain(), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB);
+        if (p.has_cache) tma_prefetch_desc(&mapC);
+        if (p.kc_short) {
+            tma_prefetch_desc(&mapSA);
+            tma_prefetch_desc(&mapSB);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i < p.c_out; i += kThreads) {
+        float b = p.bias ? p.bias[i] : 0.f;
+        if (p.bias2) b += p.bias2[i];
+        s_bias[i] = b;
+        s_gamma[i] = p.gamma ? p.gamma[i] : 1.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl wc{p.wait_ns, p.err, abort_flag};
+
+    if (warp == 0) {
+        if (lane == 0) conv_producer(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc);
+    } else if (warp == 1) {
+        if (lane == 0) conv_mma(p, sbase, tmem_base, bars, wc);
+    } else {
+        conv_epilogue(p, tmem_base, s_bias, s_gamma, bars, wc);
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+}
+
+// ------------------------------------------------------------------ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const int *,
+                                   const int *, cuuint32_t, cuuint32_t, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode_tiled = nullptr;
+EncodeIm2colFn g_encode_im2col = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encoders() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<EncodeTiledFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(fn);
+    });
+    return g_encode_tiled && g_encode_im2col;
+}
+
+CUtensorMapSwizzle swizzle_for(int sw) {
+    return sw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : (sw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+// 2-D bf16 matrix [rows][cols] (cols contiguous), box (box_cols x box_rows).
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows, int sw) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// NHWC im2col view of `frames` frames of H x W x C, bounding box shrunk by 1
+// on every side of H and W (the 3x3 window's one-element pad), 128 pixels of
+// `sw` channels per load.
+bool encode_im2col(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int sw) {
+    cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)frames};
+    cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
+    int lower[2] = {-1, -1};
+    int upper[2] = {-1, -1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode_im2col(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                           strides, lower, upper, (cuuint32_t)sw, (cuuint32_t)kBlockM, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pick_sw(int c) { return c % 64 == 0 ? 64 : (c % 32 == 0 ? 32 : 16); }
+
+struct Plan {
+    int sw, nsub, kc_main, kc_short, n_pieces, piece_n, stages;
+    uint32_t a_sub, b_sub, a_bytes, stage_bytes;
+    uint32_t off_bars, off_misc, off_vec, smem_bytes;
+    int acc_cols, nacc, tmem_cols;
+};
+
+bool make_plan(const ConvSpec &s, Plan &pl) {
+    int sw = pick_sw(s.c_in);
+    if (s.sc_in) {
+        const int sw2 = pick_sw(s.c_sc);
+        if (sw2 < sw) sw = sw2;
+    }
+    pl.sw = sw;
+    // N split into equal pieces of at most 256 columns, each a multiple of 16.
+    pl.n_pieces = 0;
+    for (int np = 1; np <= s.c_out / 16; ++np) {
+        if (s.c_out % np == 0 && (s.c_out / np) % 16 == 0 && s.c_out / np <= 256) {
+            pl.n_pieces = np;
+            break;
+        }
+    }
+    if (!pl.n_pieces) return false;
+    pl.piece_n = s.c_out / pl.n_pieces;
+    pl.acc_cols = (s.c_out + 31) / 32 * 32;
+    pl.nacc = 2 * pl.acc_cols <= 512 ? 2 : 1;
+    int cols = pl.nacc * pl.acc_cols;
+    pl.tmem_cols = 32;
+    while (pl.tmem_cols < cols) pl.tmem_cols *= 2;
+    if (pl.tmem_cols > 512) return false;
+
+    const uint32_t reserve = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out;
+    const int g_main = s.c_in / sw, g_sc = s.sc_in ? s.c_sc / sw : g_main;
+    pl.nsub = 1;
+    for (int d = 4; d >= 1; --d) {
+        if (d * sw > 128 || g_main % d || g_sc % d) continue;
+        const uint32_t sb = (uint32_t)d * (kBlockM + s.c_out) * sw * 2;
+        if (3 * sb + reserve <= (uint32_t)kSmemBudget) {
+            pl.nsub = d;
+            break;
+        }
+    }
+    pl.kc_main = g_main / pl.nsub;
+    pl.kc_short = s.sc_in ? g_sc / pl.nsub : 0;
+    pl.a_sub = (uint32_t)kBlockM * sw * 2;
+    pl.b_sub = (uint32_t)s.c_out * sw * 2;
+    pl.a_bytes = pl.a_sub * pl.nsub;
+    pl.stage_bytes = (pl.a_bytes + pl.b_sub * pl.nsub + 1023u) & ~1023u;
+    pl.stages = (int)((kSmemBudget - reserve) / pl.stage_bytes);
+    if (pl.stages > 8) pl.stages = 8;
+    if (pl.stages < 2) return false;
+    pl.off_bars = pl.stage_bytes * pl.stages;
+    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 5);
+    pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
+    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out;
+    // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
+    if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
+    return pl.smem_bytes <= (uint32_t)kSmemBudget;
+}
+
+// The dynamic shared-memory opt-in is per device; remember which devices
+// already have it.
+std::mutex g_attr_mu;
+uint64_t g_attr_done = 0;
+
+cudaError_t ensure_smem_attr() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (g_attr_done & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(conv3d_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBudget);
+    if (e == cudaSuccess) g_attr_done |= bit;
+    return e;
+}
+
+}  // namespace
+
+int conv3d_supported(const ConvSpec &s) {
+    if (s.k != 1 && s.k != 3) return -1;
+    if (s.c_in < 16 || s.c_in % 16 || s.c_out < 16 || s.c_out % 16 || s.c_out > 512) return -1;
+    if (s.c_in > 4096) return -1;
+    if (s.sc_in && (s.c_sc < 16 || s.c_sc % 16 || s.c_sc > 4096)) return -1;
+    Plan pl;
+    return make_plan(s, pl) ? 0 : -1;
+}
+
+cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
+    Plan pl;
+    if (!make_plan(s, pl)) return cudaErrorInvalidValue;
+    if (!load_encoders()) return cudaErrorInvalidValue;
+    const cudaError_t ae = ensure_smem_attr();
+    if (ae != cudaSuccess) return ae;
+
+    const int HW = s.H * s.W;
+    const int frames = s.B * s.T;
+    const int64_t M = (int64_t)frames * HW;
+    CUtensorMap mA, mC, mB, mSA, mSB;
+    memset(&mC, 0, sizeof(mC));
+    memset(&mSA, 0, sizeof(mSA));
+    memset(&mSB, 0, sizeof(mSB));
+    bool ok = true;
+    if (s.k == 3) {
+        ok = ok && encode_im2col(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw);
+        if (s.cache) ok = ok && encode_im2col(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, pl.sw);
+    } else {
+        ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
+    }
+    ok = ok && encode_2d(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, (uint64_t)s.c_out, pl.sw,
+                         pl.piece_n, pl.sw);
+    if (s.sc_in) {
+        ok = ok && encode_2d(&mSA, s.sc_in, (uint64_t)s.c_sc, (uint64_t)M, pl.sw, kBlockM, pl.sw);
+        ok = ok && encode_2d(&mSB, s.sc_w, (uint64_t)s.c_sc, (uint64_t)s.c_out, pl.sw, pl.piece_n,
+                             pl.sw);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+
+    ConvArgs a;
+    memset(&a, 0, sizeof(a));
+    a.T = s.T;
+    a.H = s.H;
+    a.W = s.W;
+    a.HW = HW;
+    a.c_in = s.c_in;
+    a.c_out = s.c_out;
+    a.taps = s.k == 3 ? 27 : 1;
+    a.has_cache = s.cache != nullptr && s.k == 3;
+    a.sw = pl.sw;
+    a.nsub = pl.nsub;
+    a.kc_main = pl.kc_main;
+    a.kc_short = pl.kc_short;
+    a.n_pieces = pl.n_pieces;
+    a.piece_n = pl.piece_n;
+    a.layout = pl.sw == 64 ? kLayoutSw128 : (pl.sw == 32 ? kLayoutSw64 : kLayoutSw32);
+    a.tiles_per_frame = (HW + kBlockM - 1) / kBlockM;
+    a.num_tiles = a.tiles_per_frame * frames;
+    a.stages = pl.stages;
+    a.a_sub_bytes = pl.a_sub;
+    a.b_sub_bytes = pl.b_sub;
+    a.a_bytes = pl.a_bytes;
+    a.stage_bytes = pl.stage_bytes;
+    a.stage_tx = (pl.a_sub + pl.b_sub) * pl.nsub;
+    a.off_bars = pl.off_bars;
+    a.off_misc = pl.off_misc;
+    a.off_vec = pl.off_vec;
+    a.acc_cols = pl.acc_cols;
+    a.nacc = pl.nacc;
+    a.tmem_cols = pl.tmem_cols;
+    a.epi = s.epi;
+    a.eps = s.eps;
+    a.sqrt_c = sqrtf((float)s.c_out);
+    a.bias = s.bias;
+    a.bias2 = s.bias2;
+    a.gamma = s.gamma;
+    a.resid = static_cast<const __nv_bfloat16 *>(s.resid);
+    a.out = static_cast<__nv_bfloat16 *>(s.out);
+    a.err = ctx.err;
+    a.wait_ns = ctx.wait_ns;
+
+    const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
+    conv3d_tcgen05_kernel<<<grid, kThreads, pl.smem_bytes, ctx.stream>>>(mA, mC, mB, mSA, mSB, a);
+    return cudaGetLastError();
+}
+
+}  // namespace wanvae

@@ -1,0 +1,66 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernels (rmsnorm_silu.cu, conv3d_tcgen05.cu).  Not installed, not exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wanvae {
+
+// Per-launch context every kernel needs: the device error word and the
+// bound on device-side waits.
+struct LaunchCtx {
+    cudaStream_t stream;
+    unsigned *err;      // device address of the error word
+    uint64_t wait_ns;   // bound of every device-side wait
+    int num_sms;
+};
+
+// SiLU(RMS_norm(x)) over C channels of n voxels; is_f32 selects fp32 in/out
+// (else bf16).  Returns a cudaError_t.
+cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool is_f32,
+                                int64_t n, int C, float eps, const LaunchCtx &ctx);
+
+// cache[b] <- last two frames of concat(cache[b], src[b]) along T, for bf16
+// tensors of frame_bytes bytes per frame (a multiple of 16).
+cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,
+                                const LaunchCtx &ctx);
+
+// Epilogue of the implicit-GEMM conv.
+enum EpiMode : int {
+    kEpiBias = 0,      // out = acc + bias (+ bias2)
+    kEpiNormSilu = 1,  // out = SiLU(RMS_norm(acc + bias) * gamma) over all c_out
+    kEpiResidual = 2,  // out = acc + bias (+ bias2) + resid  (resid: [M][c_out])
+};
+
+// One CausalConv3d as an implicit GEMM on tcgen05 (M = voxels, N = c_out,
+// K = taps * c_in), optionally followed in the same accumulator by a 1x1x1
+// shortcut segment (K += c_sc over sc_in with weights sc_w).
+struct ConvSpec {
+    const void *in;      // bf16 [B][T][H][W][c_in]
+    const void *cache;   // bf16 [B][2][H][W][c_in] frames t-2, t-1, or NULL (zeros)
+    const void *w;       // bf16 [c_out][k][k][k][c_in]
+    const float *bias;   // [c_out] or NULL
+    const float *bias2;  // [c_out] or NULL (added to bias)
+    const float *gamma;  // [c_out], kEpiNormSilu only
+    float eps;
+    const void *resid;   // bf16 [M][c_out], kEpiResidual only
+    const void *sc_in;   // bf16 [M][c_sc] or NULL (no shortcut segment)
+    const void *sc_w;    // bf16 [c_out][c_sc]
+    void *out;           // bf16 [B][T][H][W][c_out]
+    int B, T, H, W;
+    int c_in, c_out, c_sc;
+    int k;               // 3 or 1
+    int epi;             // EpiMode
+};
+
+// Host-side validation of a ConvSpec this build can run (channel counts,
+// sizes); returns 0 if supported.
+int conv3d_supported(const ConvSpec &s);
+
+// Enqueue the conv; returns a cudaError_t (cudaErrorInvalidValue when a
+// tensor map cannot be encoded).
+cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx);
+
+}  // namespace wanvae

@@ -1,0 +1,185 @@
+// rmsnorm_silu.cu -- fused RMS_norm over channels + SiLU on NDHWC voxels, and
+// the feat_cache frame update.  Both are HBM-bound streaming passes.
+//
+// RMS_norm follows "Closing the gap: Wan 2.2 14B VAE decoder", section 4:
+// the L2 norm over the channels of one voxel, clamped below by eps, divides
+// the voxel, which is then scaled by sqrt(C) * gamma; tt-metal's fused
+// rms_norm + SiLU kernel is the model for doing the activation in the same
+// pass.  SiLU(z) = z * sigmoid(z).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace wanvae {
+namespace {
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+
+// One group of L lanes owns one voxel; each lane holds VPT 16-byte vectors
+// of it (vector j of the voxel lives in lane j % L, slot j / L), so every
+// warp-wide load covers 32 consecutive 16-byte vectors of (32 / L) voxels.
+// The channel sum of squares is reduced with xor-shuffles inside the group.
+template <bool F32, int VPT>
+__global__ void __launch_bounds__(256)
+rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
+                    const float *__restrict__ gamma, int64_t n, int C, int L, float eps,
+                    float sqrt_c) {
+    constexpr int E = F32 ? 4 : 8;  // channels per 16-byte vector
+    const int V = C / E;            // vectors per voxel
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (L - 1);
+    const int grp = lane / L;
+    const int gpw = 32 / L;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+
+    for (int64_t v0 = warp_id * gpw; v0 < n; v0 += nwarps * gpw) {
+        const int64_t v = v0 + grp;
+        const bool active = v < n;
+        uint4 buf[VPT];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            if (active) {
+                buf[i] = __ldg(x + v * V + sub + i * L);
+                if (F32) {
+                    float a = __uint_as_float(buf[i].x), b = __uint_as_float(buf[i].y);
+                    float c = __uint_as_float(buf[i].z), d = __uint_as_float(buf[i].w);
+                    ss += a * a + b * b + c * c + d * d;
+                } else {
+                    const uint32_t w4[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float a = bf16lo(w4[k]), b = bf16hi(w4[k]);
+                        ss += a * a + b * b;
+                    }
+                }
+            }
+        }
+        for (int off = L >> 1; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float scale = sqrt_c / fmaxf(sqrtf(ss), eps);
+        if (!active) continue;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            const int j = sub + i * L;
+            const float4 *g4 = reinterpret_cast<const float4 *>(gamma + j * E);
+            uint4 o;
+            if (F32) {
+                const float4 g = __ldg(g4);
+                o.x = __float_as_uint(silu(__uint_as_float(buf[i].x) * scale * g.x));
+                o.y = __float_as_uint(silu(__uint_as_float(buf[i].y) * scale * g.y));
+                o.z = __float_as_uint(silu(__uint_as_float(buf[i].z) * scale * g.z));
+                o.w = __float_as_uint(silu(__uint_as_float(buf[i].w) * scale * g.w));
+            } else {
+                const float4 ga = __ldg(g4), gb = __ldg(g4 + 1);
+                o.x = pack_bf16x2(silu(bf16lo(buf[i].x) * scale * ga.x),
+                                  silu(bf16hi(buf[i].x) * scale * ga.y));
+                o.y = pack_bf16x2(silu(bf16lo(buf[i].y) * scale * ga.z),
+                                  silu(bf16hi(buf[i].y) * scale * ga.w));
+                o.z = pack_bf16x2(silu(bf16lo(buf[i].z) * scale * gb.x),
+                                  silu(bf16hi(buf[i].z) * scale * gb.y));
+                o.w = pack_bf16x2(silu(bf16lo(buf[i].w) * scale * gb.z),
+                                  silu(bf16hi(buf[i].w) * scale * gb.w));
+            }
+            y[v * V + j] = o;
+        }
+    }
+}
+
+template <bool F32>
+cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n, int C, float eps,
+                          const LaunchCtx &ctx) {
+    constexpr int E = F32 ? 4 : 8;
+    const int V = C / E;
+    int L = 1;
+    while (L < 32 && V % (2 * L) == 0) L *= 2;  // largest power of two dividing V
+    const int vpt = V / L;
+    const int threads = 256;
+    const int64_t voxels_per_block = (threads / 32) * (32 / L);
+    int64_t blocks = (n + voxels_per_block - 1) / voxels_per_block;
+    const int64_t cap = (int64_t)ctx.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    const float sqrt_c = sqrtf((float)C);
+    auto *xi = static_cast<const uint4 *>(x);
+    auto *yo = static_cast<uint4 *>(y);
+#define WANVAE_NORM_CASE(K)                                                              \
+    case K:                                                                              \
+        rmsnorm_silu_kernel<F32, K><<<(unsigned)blocks, threads, 0, ctx.stream>>>(       \
+            xi, yo, gamma, n, C, L, eps, sqrt_c);                                        \
+        break;
+    switch (vpt) {
+        WANVAE_NORM_CASE(1)
+        WANVAE_NORM_CASE(2)
+        WANVAE_NORM_CASE(3)
+        WANVAE_NORM_CASE(4)
+        WANVAE_NORM_CASE(5)
+        WANVAE_NORM_CASE(6)
+        WANVAE_NORM_CASE(7)
+        WANVAE_NORM_CASE(8)
+        WANVAE_NORM_CASE(9)
+        WANVAE_NORM_CASE(10)
+        WANVAE_NORM_CASE(11)
+        WANVAE_NORM_CASE(12)
+        WANVAE_NORM_CASE(13)
+        WANVAE_NORM_CASE(14)
+        WANVAE_NORM_CASE(15)
+        WANVAE_NORM_CASE(16)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef WANVAE_NORM_CASE
+    return cudaGetLastError();
+}
+
+// cache[b] <- last two frames of concat(cache[b], src[b]).  For T >= 2 both
+// frames come from src; for T == 1 frame 1 moves to frame 0 and src's only
+// frame becomes frame 1 (each element is read before it is overwritten by
+// the same thread, so the in-place shift has no race).
+__global__ void cache_update_kernel(uint4 *__restrict__ cache, const uint4 *__restrict__ src,
+                                    int B, int T, int64_t fv) {
+    const int64_t total = (int64_t)B * fv;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i / fv, e = i - b * fv;
+        uint4 *c = cache + b * 2 * fv + e;
+        const uint4 *s = src + b * (int64_t)T * fv + e;
+        if (T >= 2) {
+            c[0] = s[(int64_t)(T - 2) * fv];
+            c[fv] = s[(int64_t)(T - 1) * fv];
+        } else {
+            const uint4 keep = c[fv];
+            c[0] = keep;
+            c[fv] = s[0];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool is_f32,
+                                int64_t n, int C, float eps, const LaunchCtx &ctx) {
+    return is_f32 ? dispatch_norm<true>(x, y, gamma, n, C, eps, ctx)
+                  : dispatch_norm<false>(x, y, gamma, n, C, eps, ctx);
+}
+
+cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,
+                                const LaunchCtx &ctx) {
+    const int64_t fv = frame_bytes / 16;
+    const int threads = 256;
+    int64_t blocks = ((int64_t)B * fv + threads - 1) / threads;
+    const int64_t cap = (int64_t)ctx.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    cache_update_kernel<<<(unsigned)blocks, threads, 0, ctx.stream>>>(
+        static_cast<uint4 *>(cache), static_cast<const uint4 *>(src), B, T, fv);
+    return cudaGetLastError();
+}
+
+}  // namespace wanvae
