@@ -88,6 +88,23 @@ def profiled_traffic():
     return None
 
 
+def max_over_ranks(value, ws, device=None):
+    """Max of a per-rank float over all ranks of the default process group
+    (identity at world size 1).  Timing only: no data-path collective."""
+    if ws <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, ws, steps, max_ms):
+    """Whole-job units/s when every rank processed units_per_rank per step."""
+    return ws * units_per_rank * steps / (max_ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -267,13 +284,9 @@ def bench_ours(args):
     norm_ms = [e[0].elapsed_time(e[1]) for e in evs]
     convA_ms = [e[1].elapsed_time(e[2]) for e in evs]
     convB_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), ws, dev)
     ms_per_step = total_ms / K
-    value = ws * M * K / (total_ms / 1e3)
+    value = replica_throughput(M, ws, K, total_ms)
 
     # ---- end to end through the public API with host buffers
     x_host = x_cpu.pin_memory()
@@ -293,12 +306,8 @@ def bench_ours(args):
         y_host.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = ws * M * E / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    e2e_value = replica_throughput(M, ws, E, e2e_ms)
 
     # ---- roofline of the dominant kernel (the conv)
     peaks = load_peaks()

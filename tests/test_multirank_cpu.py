@@ -1,0 +1,68 @@
+"""bench.py's multi-rank host logic on CPU: world_size 2 over gloo.
+
+Each rank runs its own replica; the only cross-rank step is the max of the
+per-rank times (no data-path collective), and the job's value is the units
+of all ranks over that max."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    local_ms = 10.0 * (rank + 1)  # rank 1 is the slow one
+    m = bench.max_over_ranks(local_ms, ws)
+    v = bench.replica_throughput(1000, ws, 5, m)
+    dist.barrier()
+    dist.destroy_process_group()
+    q.put((rank, m, v))
+
+
+def test_max_over_ranks_and_weak_scaling_value_gloo():
+    ws, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, ws, port, q)) for r in range(ws)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(ws))
+    for rank, m, v in res:
+        assert m == 20.0                      # the slowest rank's time
+        assert v == pytest.approx(2 * 1000 * 5 / 0.020)
+
+
+def test_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.replica_throughput(10, 1, 2, 1000.0) == pytest.approx(20.0)
+
+
+def test_reference_arm_non_zero_rank_exits_without_output():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
