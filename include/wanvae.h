@@ -162,6 +162,32 @@ wanvae_status wanvae_resblock_forward_profiled(const wanvae_resblock_params *p,
                                                void *workspace, size_t ws_bytes,
                                                void *const *events, wanvae_stream stream);
 
+/* Size of the library's own device workspace used by
+ * wanvae_resblock_forward_static: 32 MiB, enough for one frame-by-frame call
+ * (T = 1) of a 384-channel block on a 90 x 160 latent frame. */
+#define WANVAE_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/* wanvae_resblock_forward without a caller workspace, for callers that cannot
+ * allocate device memory where they run the block (for example a plugin that
+ * is handed only its input and output buffers, or a real-time decode loop in
+ * which cudaMalloc would synchronise the device).  The source pages have no
+ * counterpart: this is a packaging variant, the computation is the same.
+ *   The workspace is a 256-byte aligned array of WANVAE_STATIC_WORKSPACE_BYTES
+ *   inside the library, one per device, kept until the process exits.  Calls
+ *   whose wanvae_resblock_workspace_size() exceeds it return
+ *   WANVAE_ERR_WORKSPACE and enqueue nothing.  The call allocates nothing.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents;
+ *   nothing in it needs to start at zero (every byte read is written earlier
+ *   in the same call).  Calls that overlap on the GPU (other streams, other
+ *   host threads) race on it: serialise them.
+ * Errors: as wanvae_resblock_forward. */
+wanvae_status wanvae_resblock_forward_static(const wanvae_resblock_params *p, const void *x,
+                                             void *y, wanvae_dims d,
+                                             const wanvae_resblock_cache *cache,
+                                             wanvae_stream stream);
+
 /* Synchronises `stream`, then returns WANVAE_ERR_TIMEOUT (and clears the
  * flag) if any kernel of this library on the current device gave up a
  * bounded wait since the last call, WANVAE_ERR_CUDA if the stream reports an

@@ -324,3 +324,54 @@ wanvae_status wanvae_sync_status(wanvae_stream stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free ResidualBlock forward.
+//
+// Some callers cannot call cudaMalloc at the point where they run the block:
+// a plugin of an inference runtime that is handed only its input and output
+// buffers, or a real-time frame-by-frame decode loop where an allocation
+// would synchronise the device or is forbidden after start-up.  For them the
+// workspace (the bf16 conv inputs a1 and a2) lives in this file-scope device
+// array instead of a caller buffer.  Every GPU that loads the library holds
+// it until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_wanvae_static_ws[WANVAE_STATIC_WORKSPACE_BYTES];
+
+namespace {
+std::mutex g_static_mu;
+void *g_static_ws_ptr[kMaxDevices];  // device address of the array, per device
+
+// Host code must not pass the array's name to a kernel (on the host it is a
+// stand-in symbol, not a device address); look the device address up once
+// per device, with that device current.
+wanvae_status static_workspace(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return WANVAE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ws_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_wanvae_static_ws) != cudaSuccess || !p)
+            return WANVAE_ERR_CUDA;
+        g_static_ws_ptr[dev] = p;
+    }
+    *out = g_static_ws_ptr[dev];
+    return WANVAE_OK;
+}
+}  // namespace
+
+extern "C" wanvae_status wanvae_resblock_forward_static(const wanvae_resblock_params *p,
+                                                        const void *x, void *y, wanvae_dims d,
+                                                        const wanvae_resblock_cache *cache,
+                                                        wanvae_stream stream) {
+    if (!p) return WANVAE_ERR_INVALID_ARG;
+    const size_t need = wanvae_resblock_workspace_size(d, p->c_in, p->c_out);
+    if (need == 0) return WANVAE_ERR_INVALID_ARG;
+    if (need > (size_t)WANVAE_STATIC_WORKSPACE_BYTES) return WANVAE_ERR_WORKSPACE;
+    void *ws = nullptr;
+    const wanvae_status st = static_workspace(&ws);
+    if (st != WANVAE_OK) return st;
+    return resblock_impl(p, x, y, d, cache, ws, (size_t)WANVAE_STATIC_WORKSPACE_BYTES, nullptr,
+                         stream);
+}

@@ -21,8 +21,11 @@ EXPORTS = (
     "wanvae_status_string", "wanvae_version", "wanvae_rmsnorm_silu", "wanvae_causal_conv3d",
     "wanvae_resblock_workspace_size", "wanvae_resblock_forward",
     "wanvae_resblock_forward_profiled", "wanvae_sync_status", "wanvae_set_wait_limit_ns",
-    "wanvae_launch_count",
+    "wanvae_launch_count", "wanvae_resblock_forward_static",
 )
+
+# Size of the library's own workspace used by resblock_forward_static.
+STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 class WanvaeError(RuntimeError):
@@ -85,6 +88,9 @@ def load(path=LIB_PATH):
     L.wanvae_set_wait_limit_ns.restype = None
     L.wanvae_launch_count.argtypes = []
     L.wanvae_launch_count.restype = ctypes.c_uint64
+    L.wanvae_resblock_forward_static.argtypes = [ctypes.POINTER(ResblockParams), vp, vp, Dims,
+                                                 ctypes.POINTER(ResblockCache), vp]
+    L.wanvae_resblock_forward_static.restype = st
     _lib = L
     return L
 
@@ -204,5 +210,22 @@ def resblock_forward(x, params, y=None, cache=None, workspace=None, stream=None,
                                                 _dims(x.shape), cs, _ptr(workspace),
                                                 workspace.numel(), ev, _stream(stream))
     _check(st, "wanvae_resblock_forward")
+    del keep_alive
+    return y
+
+
+def resblock_forward_static(x, params, y, cache=None, stream=None):
+    """resblock_forward with the library's own device workspace instead of a
+    caller buffer, for callers that cannot allocate device memory where they
+    run the block.  y must be given (nothing is allocated here either)."""
+    keep_alive = params
+    if isinstance(params, dict):
+        params = make_params(params)
+    cs = None
+    if cache is not None:
+        cs = ctypes.byref(ResblockCache(cache[0].data_ptr(), cache[1].data_ptr()))
+    st = load().wanvae_resblock_forward_static(ctypes.byref(params), _ptr(x), _ptr(y),
+                                               _dims(x.shape), cs, _stream(stream))
+    _check(st, "wanvae_resblock_forward_static")
     del keep_alive
     return y
