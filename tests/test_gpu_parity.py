@@ -14,6 +14,16 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+@pytest.fixture(params=["pair", "single"])
+def variant(request, monkeypatch):
+    """Run a conv test on the CTA-pair kernel (default) and the single-CTA one."""
+    if request.param == "single":
+        monkeypatch.setenv("WANVAE_CONV_PAIR", "1")
+    else:
+        monkeypatch.delenv("WANVAE_CONV_PAIR", raising=False)
+    return request.param
+
+
 def dev(d):
     return {k: v.to(DEV) for k, v in d.items()}
 
@@ -60,7 +70,8 @@ CONV_CASES = [
     (1, 2, 16, 16, 384, 384),
     (1, 3, 11, 13, 64, 192),
     (1, 2, 10, 10, 16, 16),
-    (1, 1, 3, 200, 128, 96),
+    (1, 1, 3, 200, 128, 96),    # 5 tiles: a CTA pair's second slot is empty
+    (1, 4, 5, 7, 64, 32),       # 1 tile per frame: pairs straddle frames t=0|1, 2|3
 ]
 
 
@@ -73,7 +84,7 @@ def conv_inputs(B, T, H, W, ci, co, k, seed):
 
 
 @pytest.mark.parametrize("case", CONV_CASES)
-def test_conv3d_k3_full_clip(cuda_lib, case):
+def test_conv3d_k3_full_clip(cuda_lib, case, variant):
     B, T, H, W, ci, co = case
     x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=sum(case))
     y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
@@ -83,7 +94,7 @@ def test_conv3d_k3_full_clip(cuda_lib, case):
 
 @pytest.mark.parametrize("case", [(1, 3, 12, 20, 64, 64), (2, 2, 9, 15, 32, 48),
                                   (1, 2, 7, 9, 384, 192)])
-def test_conv3d_k1(cuda_lib, case):
+def test_conv3d_k1(cuda_lib, case, variant):
     B, T, H, W, ci, co = case
     x, w, b = conv_inputs(B, T, H, W, ci, co, 1, seed=5 + sum(case))
     y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
@@ -92,7 +103,7 @@ def test_conv3d_k1(cuda_lib, case):
 
 
 @pytest.mark.parametrize("T", [1, 2, 3])
-def test_conv3d_with_cache_reads_and_updates_cache(cuda_lib, T):
+def test_conv3d_with_cache_reads_and_updates_cache(cuda_lib, T, variant):
     B, H, W, ci, co = 2, 9, 14, 64, 32
     x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=40 + T)
     cache = synth.make_tensor((B, 2, H, W, ci), seed=50 + T)
@@ -126,6 +137,7 @@ BLOCK_CASES = [
     (1, 2, 8, 8, 384, 192),
     (1, 4, 9, 11, 96, 96),
     (1, 1, 1, 1, 32, 32),       # one voxel: every spatial/temporal tap but one is padding
+    (1, 3, 9, 11, 64, 64),      # odd tile count, pairs straddle frames
 ]
 
 
@@ -135,7 +147,7 @@ def block_inputs(case, seed):
 
 
 @pytest.mark.parametrize("case", BLOCK_CASES)
-def test_resblock_fullT(cuda_lib, case):
+def test_resblock_fullT(cuda_lib, case, variant):
     x, p = block_inputs(case, seed=0)
     y = cuda_lib.resblock_forward(x.to(DEV), dev(p))
     cuda_lib.sync_status()
@@ -153,7 +165,7 @@ def test_resblock_with_shortcut_and_equal_channels(cuda_lib):
 @pytest.mark.parametrize("case,chunks", [((1, 6, 12, 14, 64, 64), [1] * 6),
                                          ((2, 5, 9, 10, 64, 32), [2, 2, 1]),
                                          ((1, 4, 8, 8, 384, 384), [1, 3])])
-def test_resblock_streaming_equals_fullT(cuda_lib, case, chunks):
+def test_resblock_streaming_equals_fullT(cuda_lib, case, chunks, variant):
     B, T, H, W, ci, co = case
     x, p = block_inputs(case, seed=11)
     xd, pd = x.to(DEV), dev(p)

@@ -77,10 +77,13 @@ struct ConvArgs {
 
 struct TileInfo {
     int frame, pos, n, t, h0, w0, row0;
+    bool dummy;  // a pair's second slot past the last tile: zero A, nothing stored
 };
 
 __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
     TileInfo ti;
+    ti.dummy = tile >= p.num_tiles;
+    if (ti.dummy) tile = 0;
     ti.frame = tile / p.tiles_per_frame;
     ti.pos = (tile - ti.frame * p.tiles_per_frame) * kBlockM;
     ti.n = ti.frame / p.T;
@@ -91,15 +94,28 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
     return ti;
 }
 
-// First temporal tap with a source frame: taps reading t+kt-2 < 0 are zero
-// (skipped) unless a feat_cache supplies those frames.
-__device__ __forceinline__ int first_kt(const TileInfo &ti, const ConvArgs &p) {
+// First temporal tap of a work unit (one tile, or the two tiles of a CTA
+// pair, which share every B stage and so run the same taps): taps reading
+// t+kt-2 < 0 are zero (skipped) unless a feat_cache supplies those frames.
+// A pair member whose own frame needs a skipped-for-it tap loads zeros.
+template <int kPair>
+__device__ __forceinline__ int unit_first_kt(int unit, const ConvArgs &p) {
     if (p.taps != 27 || p.has_cache) return 0;
-    return ti.t >= 2 ? 0 : 2 - ti.t;
+    int kt0 = 3;
+#pragma unroll
+    for (int r = 0; r < kPair; ++r) {
+        const int tile = unit * kPair + r;
+        if (tile >= p.num_tiles) continue;
+        const int t = (tile / p.tiles_per_frame) % p.T;
+        const int k = t >= 2 ? 0 : 2 - t;
+        kt0 = k < kt0 ? k : kt0;
+    }
+    return kt0;
 }
 
-__device__ __forceinline__ int tile_stages(const TileInfo &ti, const ConvArgs &p) {
-    const int main_taps = p.taps == 27 ? (3 - first_kt(ti, p)) * 9 : 1;
+template <int kPair>
+__device__ __forceinline__ int unit_stages(int unit, const ConvArgs &p) {
+    const int main_taps = p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * 9 : 1;
     return main_taps * p.kc_main + p.kc_short;
 }
 
@@ -113,21 +129,29 @@ struct Bars {
     __device__ uint32_t drain() const { return base + 8u * (2 * stages + 4); }
 };
 
+// TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
+// 128-row A tile and its half of every B piece; all loads complete on the
+// leader CTA's `full` barrier, which the leader arms for both CTAs' bytes.
+template <int kPair>
 __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                               const CUtensorMap *mapB, const CUtensorMap *mapSA,
                               const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
-                              const Bars &bars, const WaitCtl &wc) {
+                              const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
+                              int num_units, uint32_t rank) {
+    const int frames = p.num_tiles / p.tiles_per_frame;  // B*T
+    const int M = frames * p.HW;
+    const int half_n = p.piece_n / kPair;
     int stage = 0;
     uint32_t phase = 0, fills = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const TileInfo ti = tile_info(tile, p);
-        const int kt0 = first_kt(ti, p);
+    for (int u = unit0; ok && u < num_units; u += unit_stride) {
+        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
+        const int kt0 = unit_first_kt<kPair>(u, p);
         const int nseg = p.taps == 27 ? (3 - kt0) * 9 : 1;
         const int segs = nseg + (p.kc_short > 0 ? 1 : 0);
         for (int seg = 0; ok && seg < segs; ++seg) {
             const bool shortcut = seg == nseg;
-            int tap = 0, kh = 1, kw = 1, fidx = 0;
+            int tap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
             const CUtensorMap *am = mapA;
             if (!shortcut && p.taps == 27) {
                 tap = kt0 * 9 + seg;
@@ -135,40 +159,57 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                 kh = (tap / 3) % 3;
                 kw = tap % 3;
                 const int tt = ti.t + kt - 2;
-                if (tt >= 0) {
-                    fidx = ti.n * p.T + tt;
-                } else {
-                    am = mapC;
-                    fidx = ti.n * 2 + tt + 2;
+                if (!ti.dummy) {
+                    if (tt >= 0) {
+                        fidx = ti.n * p.T + tt;
+                    } else if (p.has_cache) {
+                        am = mapC;
+                        fidx = ti.n * 2 + tt + 2;
+                    }
                 }
             }
+            const int row0 = ti.dummy ? M : ti.row0;
             const int nkc = shortcut ? p.kc_short : p.kc_main;
             for (int kc = 0; kc < nkc; ++kc) {
-                if (!mbar_wait(bars.empty(stage), phase ^ 1u, wc)) {
+                if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = bars.full(stage);
-                mbar_arrive_expect_tx(fb, p.stage_tx);
+                const uint32_t fb_local = bars.full(stage);
+                if (rank == 0) mbar_arrive_expect_tx(fb_local, p.stage_tx * kPair);
+                const uint32_t fb = kPair == 2 ? mapa_shared(fb_local, 0) : fb_local;
                 const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
                 const uint32_t sb = sa + p.a_bytes;
                 for (int s = 0; s < p.nsub; ++s) {
                     const int c0 = (kc * p.nsub + s) * p.sw;
                     const uint32_t da = sa + (uint32_t)s * p.a_sub_bytes;
-                    if (shortcut)
-                        tma_load_2d(da, mapSA, fb, c0, ti.row0);
-                    else if (p.taps == 27)
-                        tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
-                                           (uint16_t)kw, (uint16_t)kh);
-                    else
-                        tma_load_2d(da, mapA, fb, c0, ti.row0);
+                    if (kPair == 2) {
+                        if (shortcut)
+                            tma_load_2d_pair(da, mapSA, fb, c0, row0);
+                        else if (p.taps == 27)
+                            tma_load_im2col_4d_pair(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
+                                                    (uint16_t)kw, (uint16_t)kh);
+                        else
+                            tma_load_2d_pair(da, mapA, fb, c0, row0);
+                    } else {
+                        if (shortcut)
+                            tma_load_2d(da, mapSA, fb, c0, row0);
+                        else if (p.taps == 27)
+                            tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
+                                               (uint16_t)kw, (uint16_t)kh);
+                        else
+                            tma_load_2d(da, mapA, fb, c0, row0);
+                    }
                     for (int j = 0; j < p.n_pieces; ++j) {
                         const uint32_t db = sb + (uint32_t)s * p.b_sub_bytes +
-                                            (uint32_t)(j * p.piece_n * p.sw * 2);
-                        if (shortcut)
-                            tma_load_2d(db, mapSB, fb, c0, j * p.piece_n);
+                                            (uint32_t)(j * half_n * p.sw * 2);
+                        const int brow = j * p.piece_n + (int)rank * half_n;
+                        const CUtensorMap *bm = shortcut ? mapSB : mapB;
+                        const int bk = shortcut ? c0 : tap * p.c_in + c0;
+                        if (kPair == 2)
+                            tma_load_2d_pair(db, bm, fb, bk, brow);
                         else
-                            tma_load_2d(db, mapB, fb, tap * p.c_in + c0, j * p.piece_n);
+                            tma_load_2d(db, bm, fb, bk, brow);
                     }
                 }
                 ++fills;
@@ -179,67 +220,115 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
             }
         }
     }
-    if (!ok) {
+    if (!ok && rank == 0) {
         // Aborted: let the newest fill of every stage land before the CTA
         // (and its shared memory) goes away.
         volatile int no_abort = 0;
         const WaitCtl dc{kDrainNs, wc.err, &no_abort};
         const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
         for (uint32_t f = fills - n; f < fills; ++f)
-            mbar_wait(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
+            mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
     }
 }
 
+// Issue the MMAs of one pipeline stage.  KK k-steps of 16 per swizzled
+// sub-tile, NSUB sub-tiles, NP N-pieces: all compile-time, so the loop is fully
+// unrolled and every descriptor is the stage's base plus a constant (the
+// issuing thread must not spend more cycles between two MMAs than one MMA
+// takes on the tensor core).  KK == 0 selects the run-time-bounded form for
+// shapes without a specialisation.
+template <int kPair, int KK, int NSUB, int NP>
+__device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, uint64_t a0,
+                                            uint64_t b0, uint32_t idesc, bool first) {
+    const uint32_t a_sub16 = p.a_sub_bytes >> 4, b_sub16 = p.b_sub_bytes >> 4;
+    const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
+    if (KK > 0) {
+#pragma unroll
+        for (int s = 0; s < NSUB; ++s) {
+#pragma unroll
+            for (int kk = 0; kk < KK; ++kk) {
+                const uint64_t ad = a0 + (uint64_t)(s * a_sub16 + 2 * kk);
+                const uint32_t accum = (first && s == 0 && kk == 0) ? 0u : 1u;
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
+                    const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
+                    if (kPair == 2)
+                        mma_bf16_ss_pair(d, ad, bd, idesc, accum);
+                    else
+                        mma_bf16_ss(d, ad, bd, idesc, accum);
+                }
+            }
+        }
+    } else {
+        for (int s = 0; s < p.nsub; ++s) {
+            for (int kk = 0; kk < p.sw / 16; ++kk) {
+                const uint64_t ad = a0 + (uint64_t)(s * a_sub16 + 2 * kk);
+                const uint32_t accum = (first && s == 0 && kk == 0) ? 0u : 1u;
+                for (int j = 0; j < p.n_pieces; ++j) {
+                    const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
+                    const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
+                    if (kPair == 2)
+                        mma_bf16_ss_pair(d, ad, bd, idesc, accum);
+                    else
+                        mma_bf16_ss(d, ad, bd, idesc, accum);
+                }
+            }
+        }
+    }
+}
+
+// MMA issuer (one thread of the leader CTA).
+template <int kPair, int KK, int NSUB, int NP>
 __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, const Bars &bars,
-                         const WaitCtl &wc) {
-    const uint32_t idesc = idesc_bf16_f32(kBlockM, p.piece_n);
+                         const WaitCtl &wc, int unit0, int unit_stride, int num_units) {
+    const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
     const uint32_t row_bytes = (uint32_t)p.sw * 2u;
     int stage = 0, it = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int u = unit0; ok && u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
-        if (!mbar_wait(bars.acce(a), aph ^ 1u, wc)) break;
+        if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_cols);
-        const int nst = tile_stages(tile_info(tile, p), p);
+        const int nst = unit_stages<kPair>(u, p);
         for (int k = 0; k < nst; ++k) {
-            if (!mbar_wait(bars.full(stage), phase, wc)) {
+            if (!mbar_wait<kPair == 2>(bars.full(stage), phase, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
-            const uint32_t sb = sa + p.a_bytes;
-            for (int s = 0; s < p.nsub; ++s) {
-                for (int kk = 0; kk < p.sw / 16; ++kk) {
-                    const uint64_t ad =
-                        sdesc_kmajor(sa + (uint32_t)s * p.a_sub_bytes + 32u * kk, row_bytes, p.layout);
-                    const uint32_t accum = (k > 0 || s > 0 || kk > 0) ? 1u : 0u;
-                    for (int j = 0; j < p.n_pieces; ++j) {
-                        const uint64_t bd = sdesc_kmajor(
-                            sb + (uint32_t)s * p.b_sub_bytes + (uint32_t)j * p.piece_n * row_bytes +
-                                32u * kk,
-                            row_bytes, p.layout);
-                        mma_bf16_ss(dacc + (uint32_t)(j * p.piece_n), ad, bd, idesc, accum);
-                    }
-                }
-            }
-            mma_commit(bars.empty(stage));  // frees the smem stage when these MMAs finish
+            issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(sa, row_bytes, p.layout),
+                                             sdesc_kmajor(sa + p.a_bytes, row_bytes, p.layout),
+                                             idesc, k == 0);
+            // Frees the smem stage (in both CTAs of a pair) when these MMAs finish.
+            if (kPair == 2)
+                mma_commit_pair_mc(bars.empty(stage), (uint16_t)0x3);
+            else
+                mma_commit(bars.empty(stage));
             if (++stage == p.stages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok) break;
-        mma_commit(bars.accf(a));  // accumulator ready for the epilogue
+        // Accumulator ready for the epilogue (of both CTAs of a pair).
+        if (kPair == 2)
+            mma_commit_pair_mc(bars.accf(a), (uint16_t)0x3);
+        else
+            mma_commit(bars.accf(a));
     }
     // Every MMA issued above completes before TMEM is released.
     volatile int no_abort = 0;
     const WaitCtl dc{kDrainNs, wc.err, &no_abort};
-    mma_commit(bars.drain());
-    mbar_wait(bars.drain(), 0u, dc);
+    if (kPair == 2)
+        mma_commit_pair(bars.drain());
+    else
+        mma_commit(bars.drain());
+    mbar_wait<kPair == 2>(bars.drain(), 0u, dc);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -247,19 +336,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+template <int kPair>
 __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
-                              const float *s_gamma, const Bars &bars, const WaitCtl &wc) {
+                              const float *s_gamma, const Bars &bars, const WaitCtl &wc,
+                              int unit0, int unit_stride, int num_units, uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int row = q * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+    for (int u = unit0; u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
-        if (!mbar_wait_warp(bars.accf(a), aph, wc)) break;
+        if (!mbar_wait_warp<kPair == 2>(bars.accf(a), aph, wc)) break;
         tc_fence_after();
-        const TileInfo ti = tile_info(tile, p);
-        const bool valid = ti.pos + row < p.HW;
+        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
+        const bool valid = !ti.dummy && ti.pos + row < p.HW;
         const int64_t g = (int64_t)ti.row0 + row;
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols);
         uint4 *out = reinterpret_cast<uint4 *>(p.out + g * p.c_out);
@@ -325,10 +416,17 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.acce(a));
+        if (lane == 0) {
+            // Accumulator drained: tell the MMA issuer (in the leader CTA).
+            if (kPair == 2)
+                mbar_arrive_cluster(mapa_shared(bars.acce(a), 0));
+            else
+                mbar_arrive(bars.acce(a));
+        }
     }
 }
 
+template <int kPair, int KK, int NSUB, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
 conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapC,
@@ -346,6 +444,12 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
 
+    // Work units: single tiles, or pairs of consecutive tiles per cluster.
+    const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
+    const int unit0 = kPair == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int unit_stride = kPair == 2 ? (int)cluster_count_x() : (int)gridDim.x;
+    const int num_units = (p.num_tiles + kPair - 1) / kPair;
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(bars.full(s), 1);
@@ -353,7 +457,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bars.accf(a), 1);
-            mbar_init(bars.acce(a), 4);
+            mbar_init(bars.acce(a), 4 * kPair);
         }
         mbar_init(bars.drain(), 1);
         *abort_flag = 0;
@@ -369,8 +473,13 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
-        tmem_relinquish();
+        if (kPair == 2) {
+            tmem_alloc_pair(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+            tmem_relinquish();
+        }
     }
     for (int i = threadIdx.x; i < p.c_out; i += kThreads) {
         float b = p.bias ? p.bias[i] : 0.f;
@@ -379,23 +488,39 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         s_gamma[i] = p.gamma ? p.gamma[i] : 1.f;
     }
     tc_fence_before();
-    __syncthreads();
+    if (kPair == 2)
+        cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA use
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{p.wait_ns, p.err, abort_flag};
 
     if (warp == 0) {
-        if (lane == 0) conv_producer(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc);
+        if (lane == 0)
+            conv_producer<kPair>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc, unit0,
+                                 unit_stride, num_units, rank);
     } else if (warp == 1) {
-        if (lane == 0) conv_mma(p, sbase, tmem_base, bars, wc);
+        if (lane == 0 && rank == 0)
+            conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
+                                          num_units);
     } else {
-        conv_epilogue(p, tmem_base, s_bias, s_gamma, bars, wc);
+        conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, bars, wc, unit0, unit_stride,
+                             num_units, rank);
     }
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if (kPair == 2)
+        cluster_sync_all();  // no CTA leaves while its peer may still touch it
+    else
+        __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    if (warp == 1) {
+        if (kPair == 2)
+            tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+        else
+            tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+    }
 }
 
 // ------------------------------------------------------------------ host
@@ -467,23 +592,34 @@ bool encode_im2col(CUtensorMap *m, const void *base, int C, int W, int H, int fr
 int pick_sw(int c) { return c % 64 == 0 ? 64 : (c % 32 == 0 ? 32 : 16); }
 
 struct Plan {
+    int pair;  // 1: one CTA per 128-row tile; 2: CTA pair per 256 rows (cta_group::2)
     int sw, nsub, kc_main, kc_short, n_pieces, piece_n, stages;
     uint32_t a_sub, b_sub, a_bytes, stage_bytes;
     uint32_t off_bars, off_misc, off_vec, smem_bytes;
     int acc_cols, nacc, tmem_cols;
 };
 
-bool make_plan(const ConvSpec &s, Plan &pl) {
+// CTA pairs halve each CTA's share of the B (weight) operand -- half the
+// shared-memory bytes per stage, so a deeper pipeline, and half the L2->SM
+// traffic for B.  WANVAE_CONV_PAIR=1 selects the single-CTA kernel instead.
+int pair_choice() {
+    const char *e = getenv("WANVAE_CONV_PAIR");
+    return (e && e[0] == '1' && e[1] == 0) ? 1 : 2;
+}
+
+bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
+    pl.pair = pair;
     int sw = pick_sw(s.c_in);
     if (s.sc_in) {
         const int sw2 = pick_sw(s.c_sc);
         if (sw2 < sw) sw = sw2;
     }
     pl.sw = sw;
-    // N split into equal pieces of at most 256 columns, each a multiple of 16.
+    // N split into equal pieces of at most 256 columns, each a multiple of
+    // 16 * pair (a pair splits every piece's rows between its two CTAs).
     pl.n_pieces = 0;
     for (int np = 1; np <= s.c_out / 16; ++np) {
-        if (s.c_out % np == 0 && (s.c_out / np) % 16 == 0 && s.c_out / np <= 256) {
+        if (s.c_out % np == 0 && (s.c_out / np) % (16 * pair) == 0 && s.c_out / np <= 256) {
             pl.n_pieces = np;
             break;
         }
@@ -498,12 +634,14 @@ bool make_plan(const ConvSpec &s, Plan &pl) {
     if (pl.tmem_cols > 512) return false;
 
     const uint32_t reserve = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out;
+    const uint32_t b_rows = (uint32_t)(s.c_out / pair);
     const int g_main = s.c_in / sw, g_sc = s.sc_in ? s.c_sc / sw : g_main;
+    const int min_stages = pair == 2 ? 4 : 3;
     pl.nsub = 1;
     for (int d = 4; d >= 1; --d) {
         if (d * sw > 128 || g_main % d || g_sc % d) continue;
-        const uint32_t sb = (uint32_t)d * (kBlockM + s.c_out) * sw * 2;
-        if (3 * sb + reserve <= (uint32_t)kSmemBudget) {
+        const uint32_t sb = (uint32_t)d * (kBlockM + b_rows) * sw * 2;
+        if (min_stages * sb + reserve <= (uint32_t)kSmemBudget) {
             pl.nsub = d;
             break;
         }
@@ -511,7 +649,7 @@ bool make_plan(const ConvSpec &s, Plan &pl) {
     pl.kc_main = g_main / pl.nsub;
     pl.kc_short = s.sc_in ? g_sc / pl.nsub : 0;
     pl.a_sub = (uint32_t)kBlockM * sw * 2;
-    pl.b_sub = (uint32_t)s.c_out * sw * 2;
+    pl.b_sub = b_rows * sw * 2;
     pl.a_bytes = pl.a_sub * pl.nsub;
     pl.stage_bytes = (pl.a_bytes + pl.b_sub * pl.nsub + 1023u) & ~1023u;
     pl.stages = (int)((kSmemBudget - reserve) / pl.stage_bytes);
@@ -526,22 +664,75 @@ bool make_plan(const ConvSpec &s, Plan &pl) {
     return pl.smem_bytes <= (uint32_t)kSmemBudget;
 }
 
-// The dynamic shared-memory opt-in is per device; remember which devices
-// already have it.
-std::mutex g_attr_mu;
-uint64_t g_attr_done = 0;
+typedef void (*ConvKernelFn)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                             const CUtensorMap, const CUtensorMap, const ConvArgs);
 
-cudaError_t ensure_smem_attr() {
+// The specialisation for a plan: unrolled MMA issue for every (k-steps per
+// sub-tile, sub-tiles per stage, N-pieces) the planner produces, run-time
+// loops otherwise.
+template <int kPair>
+ConvKernelFn pick_kernel(int kk, int nsub, int np) {
+#define WANVAE_CONV_SPEC(KK_, NS_)                                                     \
+    if (kk == KK_ && nsub == NS_ && np == 1) return conv3d_tcgen05_kernel<kPair, KK_, NS_, 1>; \
+    if (kk == KK_ && nsub == NS_ && np == 2) return conv3d_tcgen05_kernel<kPair, KK_, NS_, 2>;
+    WANVAE_CONV_SPEC(4, 1)
+    WANVAE_CONV_SPEC(4, 2)
+    WANVAE_CONV_SPEC(2, 1)
+    WANVAE_CONV_SPEC(2, 2)
+    WANVAE_CONV_SPEC(2, 3)
+    WANVAE_CONV_SPEC(2, 4)
+    WANVAE_CONV_SPEC(1, 1)
+    WANVAE_CONV_SPEC(1, 2)
+    WANVAE_CONV_SPEC(1, 3)
+    WANVAE_CONV_SPEC(1, 4)
+#undef WANVAE_CONV_SPEC
+    return conv3d_tcgen05_kernel<kPair, 0, 0, 0>;
+}
+
+// Per-device, per-kernel launch facts: the dynamic shared-memory opt-in and
+// how many CTA-pair clusters can be resident at once.
+struct KernelFacts {
+    int dev;
+    ConvKernelFn fn;
+    int max_pairs;
+};
+std::mutex g_facts_mu;
+KernelFacts g_facts[256];
+int g_nfacts = 0;
+
+cudaError_t kernel_facts(ConvKernelFn fn, bool pair, int &max_pairs) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (bit && (g_attr_done & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(conv3d_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBudget);
-    if (e == cudaSuccess) g_attr_done |= bit;
-    return e;
+    std::lock_guard<std::mutex> lk(g_facts_mu);
+    for (int i = 0; i < g_nfacts; ++i)
+        if (g_facts[i].dev == dev && g_facts[i].fn == fn) {
+            max_pairs = g_facts[i].max_pairs;
+            return cudaSuccess;
+        }
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    if (pair) {
+        // Every launch uses >= 120 KB of shared memory, so one CTA per SM:
+        // the resident-cluster count does not depend on the exact size.
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)kSmemBudget;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+        if (e != cudaSuccess) return e;
+    }
+    if (g_nfacts < 256) g_facts[g_nfacts++] = KernelFacts{dev, fn, n};
+    max_pairs = n;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -552,15 +743,24 @@ int conv3d_supported(const ConvSpec &s) {
     if (s.c_in > 4096) return -1;
     if (s.sc_in && (s.c_sc < 16 || s.c_sc % 16 || s.c_sc > 4096)) return -1;
     Plan pl;
-    return make_plan(s, pl) ? 0 : -1;
+    return (make_plan(s, pl, 2) || make_plan(s, pl, 1)) ? 0 : -1;
 }
 
 cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     Plan pl;
-    if (!make_plan(s, pl)) return cudaErrorInvalidValue;
+    if (!make_plan(s, pl, pair_choice()) && !make_plan(s, pl, 1)) return cudaErrorInvalidValue;
     if (!load_encoders()) return cudaErrorInvalidValue;
-    const cudaError_t ae = ensure_smem_attr();
-    if (ae != cudaSuccess) return ae;
+    ConvKernelFn fn = pl.pair == 2 ? pick_kernel<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
+                                   : pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
+    int max_pairs = 0;
+    cudaError_t fe = kernel_facts(fn, pl.pair == 2, max_pairs);
+    if (fe != cudaSuccess) return fe;
+    if (pl.pair == 2 && max_pairs < 1) {
+        if (!make_plan(s, pl, 1)) return cudaErrorInvalidValue;
+        fn = pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
+        fe = kernel_facts(fn, false, max_pairs);
+        if (fe != cudaSuccess) return fe;
+    }
 
     const int HW = s.H * s.W;
     const int frames = s.B * s.T;
@@ -569,6 +769,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     memset(&mC, 0, sizeof(mC));
     memset(&mSA, 0, sizeof(mSA));
     memset(&mSB, 0, sizeof(mSB));
+    const uint32_t b_box = (uint32_t)(pl.piece_n / pl.pair);
     bool ok = true;
     if (s.k == 3) {
         ok = ok && encode_im2col(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw);
@@ -577,10 +778,10 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
         ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
     }
     ok = ok && encode_2d(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, (uint64_t)s.c_out, pl.sw,
-                         pl.piece_n, pl.sw);
+                         b_box, pl.sw);
     if (s.sc_in) {
         ok = ok && encode_2d(&mSA, s.sc_in, (uint64_t)s.c_sc, (uint64_t)M, pl.sw, kBlockM, pl.sw);
-        ok = ok && encode_2d(&mSB, s.sc_w, (uint64_t)s.c_sc, (uint64_t)s.c_out, pl.sw, pl.piece_n,
+        ok = ok && encode_2d(&mSB, s.sc_w, (uint64_t)s.c_sc, (uint64_t)s.c_out, pl.sw, b_box,
                              pl.sw);
     }
     if (!ok) return cudaErrorInvalidValue;
@@ -627,9 +828,27 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.err = ctx.err;
     a.wait_ns = ctx.wait_ns;
 
-    const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
-    conv3d_tcgen05_kernel<<<grid, kThreads, pl.smem_bytes, ctx.stream>>>(mA, mC, mB, mSA, mSB, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    if (pl.pair == 1) {
+        const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.numAttrs = 0;
+    } else {
+        const int units = (a.num_tiles + 1) / 2;
+        const int pairs = units < max_pairs ? units : max_pairs;
+        cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = ctx.stream;
+    return cudaLaunchKernelEx(&cfg, fn, mA, mC, mB, mSA, mSB, a);
 }
 
 }  // namespace wanvae
