@@ -46,7 +46,8 @@ namespace wanvae {
 namespace {
 
 constexpr int kBlockM = 128;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two warps per TMEM lane quarter, each half the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // cleanup waits after an abort
 
@@ -336,18 +337,78 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Named-barrier OR-reduction: true in every participating thread if `pred`
+// was true in any of them.
+__device__ __forceinline__ bool bar_any(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// Two x16 TMEM loads under one wait (32 columns), or one (16 columns).
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int ncols, uint32_t (&r)[32]) {
+    if (ncols >= 32) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+              "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+              "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+              "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr), "r"(taddr + 16u));
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                       "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                       "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
+                       "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                       "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+                       "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                     :
+                     : "memory");
+    } else {
+        uint32_t (&h)[16] = *reinterpret_cast<uint32_t (*)[16]>(&r[0]);
+        tmem_ld16(taddr, h);
+    }
+}
+
+// Epilogue warps: warp w reads TMEM lane quarter (w % 4) -- the hardware's
+// rule -- and owns half of the columns (half (w - 2) / 4), so two warps share
+// every row.  The fused RMS_norm combines their two partial sums of squares
+// through shared memory.
 template <int kPair>
 __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
-                              const float *s_gamma, const Bars &bars, const WaitCtl &wc,
-                              int unit0, int unit_stride, int num_units, uint32_t rank) {
+                              const float *s_gamma, float *s_part, const Bars &bars,
+                              const WaitCtl &wc, int unit0, int unit_stride, int num_units,
+                              uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int q = warp & 3;           // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2; // 0 or 1: which column half
     const int row = q * 32 + lane;
+    const int c_split = ((p.c_out / 2) + 15) / 16 * 16;
+    const int c_begin = half ? c_split : 0, c_end = half ? p.c_out : c_split;
     int it = 0;
     for (int u = unit0; u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
-        if (!mbar_wait_warp<kPair == 2>(bars.accf(a), aph, wc)) break;
+        const bool got = mbar_wait_warp<kPair == 2>(bars.accf(a), aph, wc);
+        if (p.epi == kEpiNormSilu) {
+            // The norm's halves meet at a named barrier below, so all epilogue
+            // warps take the same decision: stop if any of them gave up.
+            if (bar_any(1, 32 * kEpiWarps, !got)) break;
+        } else if (!got) {
+            break;
+        }
         tc_fence_after();
         const TileInfo ti = tile_info(u * kPair + (int)rank, p);
         const bool valid = !ti.dummy && ti.pos + row < p.HW;
@@ -357,60 +418,85 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         if (p.epi == kEpiNormSilu) {
             // RMS_norm over all c_out channels of this voxel, then SiLU.
             float ss = 0.f;
-            for (int c = 0; c < p.c_out; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(tb + (uint32_t)c, r);
+            for (int c = c_begin; c < c_end; c += 32) {
+                uint32_t r[32];
+                const int n = c_end - c >= 32 ? 32 : 16;
+                tmem_ld_cols(tb + (uint32_t)c, n, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (i < n) {
+                        const float v = __uint_as_float(r[i]) + s_bias[c + i];
+                        ss += v * v;
+                    }
+                }
+            }
+            s_part[half * kBlockM + row] = ss;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+            const float tot = s_part[row] + s_part[kBlockM + row];
+            const float scale = p.sqrt_c / fmaxf(sqrtf(tot), p.eps);
+            for (int c = c_begin; c < c_end; c += 32) {
+                uint32_t r[32];
+                const int n = c_end - c >= 32 ? 32 : 16;
+                tmem_ld_cols(tb + (uint32_t)c, n, r);
+                uint32_t o[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float v = __uint_as_float(r[i]) + s_bias[c + i];
-                    ss += v * v;
-                }
-            }
-            const float scale = p.sqrt_c / fmaxf(sqrtf(ss), p.eps);
-            for (int c = 0; c < p.c_out; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(tb + (uint32_t)c, r);
-                uint32_t o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float z0 = (__uint_as_float(r[2 * i]) + s_bias[c + 2 * i]) * scale *
-                               s_gamma[c + 2 * i];
-                    float z1 = (__uint_as_float(r[2 * i + 1]) + s_bias[c + 2 * i + 1]) * scale *
-                               s_gamma[c + 2 * i + 1];
-                    z0 = z0 / (1.0f + __expf(-z0));
-                    z1 = z1 / (1.0f + __expf(-z1));
-                    o[i] = pack_bf16x2(z0, z1);
+                    if (2 * i < n) {
+                        float z0 = (__uint_as_float(r[2 * i]) + s_bias[c + 2 * i]) * scale *
+                                   s_gamma[c + 2 * i];
+                        float z1 = (__uint_as_float(r[2 * i + 1]) + s_bias[c + 2 * i + 1]) *
+                                   scale * s_gamma[c + 2 * i + 1];
+                        z0 = __fdividef(z0, 1.0f + __expf(-z0));
+                        z1 = __fdividef(z1, 1.0f + __expf(-z1));
+                        o[i] = pack_bf16x2(z0, z1);
+                    }
                 }
                 if (valid) {
-                    out[c / 8] = make_uint4(o[0], o[1], o[2], o[3]);
-                    out[c / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        if (8 * v < n) out[c / 8 + v] = make_uint4(o[4 * v], o[4 * v + 1],
+                                                                   o[4 * v + 2], o[4 * v + 3]);
                 }
             }
+            // s_part is rewritten only after the next tile's bar_any, which
+            // every warp reaches after its last read above.
         } else {
             const uint4 *res = p.epi == kEpiResidual
                                    ? reinterpret_cast<const uint4 *>(p.resid + g * p.c_out)
                                    : nullptr;
-            for (int c = 0; c < p.c_out; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(tb + (uint32_t)c, r);
-                float v[16];
+            for (int c = c_begin; c < c_end; c += 32) {
+                uint32_t r[32];
+                const int n = c_end - c >= 32 ? 32 : 16;
+                tmem_ld_cols(tb + (uint32_t)c, n, r);
+                float v[32];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + s_bias[c + i];
+                for (int i = 0; i < 32; ++i)
+                    if (i < n) v[i] = __uint_as_float(r[i]) + s_bias[c + i];
                 if (res && valid) {
-                    const uint4 x0 = res[c / 8], x1 = res[c / 8 + 1];
-                    const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        v[2 * i] += __uint_as_float(xs[i] << 16);
-                        v[2 * i + 1] += __uint_as_float(xs[i] & 0xffff0000u);
+                    for (int vv = 0; vv < 4; ++vv) {
+                        if (8 * vv < n) {
+                            const uint4 x4 = res[c / 8 + vv];
+                            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                v[8 * vv + 2 * i] += __uint_as_float(xs[i] << 16);
+                                v[8 * vv + 2 * i + 1] += __uint_as_float(xs[i] & 0xffff0000u);
+                            }
+                        }
                     }
                 }
                 if (valid) {
-                    uint32_t o[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                    out[c / 8] = make_uint4(o[0], o[1], o[2], o[3]);
-                    out[c / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    for (int vv = 0; vv < 4; ++vv) {
+                        if (8 * vv < n) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                o[i] = pack_bf16x2(v[8 * vv + 2 * i], v[8 * vv + 2 * i + 1]);
+                            out[c / 8 + vv] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
                 }
             }
         }
@@ -443,6 +529,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_misc + 4);
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
+    float *s_part = s_gamma + p.c_out;  // [2][128] partial sums of squares
 
     // Work units: single tiles, or pairs of consecutive tiles per cluster.
     const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
@@ -457,7 +544,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bars.accf(a), 1);
-            mbar_init(bars.acce(a), 4 * kPair);
+            mbar_init(bars.acce(a), kEpiWarps * kPair);
         }
         mbar_init(bars.drain(), 1);
         *abort_flag = 0;
@@ -505,8 +592,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
             conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
                                           num_units);
     } else {
-        conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, bars, wc, unit0, unit_stride,
-                             num_units, rank);
+        conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, s_part, bars, wc, unit0,
+                             unit_stride, num_units, rank);
     }
     __syncwarp();
     tc_fence_before();
@@ -633,7 +720,8 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
     while (pl.tmem_cols < cols) pl.tmem_cols *= 2;
     if (pl.tmem_cols > 512) return false;
 
-    const uint32_t reserve = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out;
+    const uint32_t reserve = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out +
+                             2u * 4u * kBlockM /*norm partial sums*/;
     const uint32_t b_rows = (uint32_t)(s.c_out / pair);
     const int g_main = s.c_in / sw, g_sc = s.sc_in ? s.c_sc / sw : g_main;
     const int min_stages = pair == 2 ? 4 : 3;
@@ -658,7 +746,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
     pl.off_bars = pl.stage_bytes * pl.stages;
     pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 5);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out;
+    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM;
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
     if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
     return pl.smem_bytes <= (uint32_t)kSmemBudget;
