@@ -48,6 +48,7 @@ namespace {
 constexpr int kBlockM = 128;
 constexpr int kEpiWarps = 8;  // two warps per TMEM lane quarter, each half the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 rows x 32 bf16 channels
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // cleanup waits after an abort
 
@@ -67,6 +68,8 @@ struct ConvArgs {
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
     uint32_t off_bars, off_misc, off_vec;
     int acc_cols, nacc, tmem_cols;
+    int staged;          // epilogue through a whole-tile smem buffer + TMA stores
+    uint32_t off_stage;  // 1024-aligned offset of that buffer
     int epi;
     float eps, sqrt_c;
     const float *bias, *bias2, *gamma;
@@ -128,6 +131,7 @@ struct Bars {
     __device__ uint32_t accf(int a) const { return base + 8u * (2 * stages + a); }
     __device__ uint32_t acce(int a) const { return base + 8u * (2 * stages + 2 + a); }
     __device__ uint32_t drain() const { return base + 8u * (2 * stages + 4); }
+    __device__ uint32_t resf() const { return base + 8u * (2 * stages + 5); }
 };
 
 // TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
@@ -382,13 +386,44 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int ncols, uint32_t
     }
 }
 
+// Write one warp's 32-row x n-channel (n = 16 or 32) bf16 chunk: each lane
+// hands its row's n/8 16-byte pieces (o) to a swizzled shared buffer, then the
+// warp writes the chunk back four lanes per row, so every store instruction
+// covers eight whole 64-byte row segments instead of 32 scattered 16-byte
+// pieces.  Rows at or past `nvalid` (the frame's end) are not written.
+__device__ __forceinline__ void store_chunk(uint8_t *stg, const uint32_t (&o)[16], int n,
+                                            __nv_bfloat16 *out_row0, int ldc, int c,
+                                            int nvalid) {
+    const int lane = threadIdx.x & 31;
+    const int np = n / 8;  // 16-byte pieces per row
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < np) {
+            const int slot = k ^ ((lane >> 1) & 3);
+            *reinterpret_cast<uint4 *>(stg + lane * 64 + slot * 16) =
+                make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = j * 8 + (lane >> 2), q = lane & 3;
+        if (q < np && r < nvalid) {
+            const int slot = q ^ ((r >> 1) & 3);
+            const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 64 + slot * 16);
+            *reinterpret_cast<uint4 *>(out_row0 + (int64_t)r * ldc + c + q * 8) = v;
+        }
+    }
+    __syncwarp();
+}
+
 // Epilogue warps: warp w reads TMEM lane quarter (w % 4) -- the hardware's
 // rule -- and owns half of the columns (half (w - 2) / 4), so two warps share
 // every row.  The fused RMS_norm combines their two partial sums of squares
 // through shared memory.
 template <int kPair>
 __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
-                              const float *s_gamma, float *s_part, const Bars &bars,
+                              const float *s_gamma, float *s_part, uint8_t *stg, const Bars &bars,
                               const WaitCtl &wc, int unit0, int unit_stride, int num_units,
                               uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -414,7 +449,11 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         const bool valid = !ti.dummy && ti.pos + row < p.HW;
         const int64_t g = (int64_t)ti.row0 + row;
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols);
-        uint4 *out = reinterpret_cast<uint4 *>(p.out + g * p.c_out);
+        // This warp's 32 rows start at row q*32 of the tile; rows of a ragged
+        // tile past the frame's end (or of an empty pair slot) are not stored.
+        int nvalid = ti.dummy ? 0 : p.HW - ti.pos - q * 32;
+        nvalid = nvalid < 0 ? 0 : (nvalid > 32 ? 32 : nvalid);
+        __nv_bfloat16 *out_w = p.out + ((int64_t)ti.row0 + q * 32) * p.c_out;
         if (p.epi == kEpiNormSilu) {
             // RMS_norm over all c_out channels of this voxel, then SiLU.
             float ss = 0.f;
@@ -451,12 +490,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                         o[i] = pack_bf16x2(z0, z1);
                     }
                 }
-                if (valid) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        if (8 * v < n) out[c / 8 + v] = make_uint4(o[4 * v], o[4 * v + 1],
-                                                                   o[4 * v + 2], o[4 * v + 3]);
-                }
+                store_chunk(stg, o, n, out_w, p.c_out, c, nvalid);
             }
             // s_part is rewritten only after the next tile's bar_any, which
             // every warp reaches after its last read above.
@@ -486,18 +520,10 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                         }
                     }
                 }
-                if (valid) {
+                uint32_t o[16];
 #pragma unroll
-                    for (int vv = 0; vv < 4; ++vv) {
-                        if (8 * vv < n) {
-                            uint32_t o[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                o[i] = pack_bf16x2(v[8 * vv + 2 * i], v[8 * vv + 2 * i + 1]);
-                            out[c / 8 + vv] = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
-                }
+                for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                store_chunk(stg, o, n, out_w, p.c_out, c, nvalid);
             }
         }
         tc_fence_before();
@@ -512,13 +538,152 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
     }
 }
 
+// Whole-tile staged epilogue (one TMEM accumulator, c_out a multiple of 64).
+// The epilogue warps turn the accumulator into the bf16 output tile inside a
+// shared buffer laid out as TMA's 128-byte swizzle expects ([c_out/64] blocks
+// of 128 rows x 64 channels), hand TMEM back to the MMA warp at once, and one
+// thread drains the buffer to global memory with asynchronous bulk tensor
+// stores while the next tile's MMAs run.  For the residual epilogue the x tile
+// is brought into the same buffer by TMA during the mainloop (rows past the
+// frame read as zeros and are never stored: the 3-D maps clip them).
+template <int kPair>
+__device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
+                                     const float *s_gamma, float *s_part, uint8_t *buf,
+                                     const CUtensorMap *mapY, const CUtensorMap *mapR,
+                                     const Bars &bars, const WaitCtl &wc, int unit0,
+                                     int unit_stride, int num_units, uint32_t rank) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const int c_split = ((p.c_out / 2) + 15) / 16 * 16;
+    const int c_begin = half ? c_split : 0, c_end = half ? p.c_out : c_split;
+    const bool issuer = warp == 2 && lane == 0;
+    const bool resid = p.epi == kEpiResidual;
+    const int nblk = p.c_out / 64;
+    const uint32_t buf_s = smem_u32(buf);
+    const uint32_t res_bytes = (uint32_t)p.c_out * kBlockM * 2u;
+    uint32_t res_phase = 0;
+    bool res_pending = false;  // issuer: a residual load is in flight
+
+    auto issue_residual = [&](int u) {
+        const TileInfo tn = tile_info(u * kPair + (int)rank, p);
+        if (tn.dummy) return;
+        mbar_arrive_expect_tx(bars.resf(), res_bytes);
+        for (int b = 0; b < nblk; ++b)
+            tma_load_3d(buf_s + (uint32_t)b * (kBlockM * 128u), mapR, bars.resf(), b * 64, tn.pos,
+                        tn.frame);
+        res_pending = true;
+    };
+    if (issuer && resid && unit0 < num_units) issue_residual(unit0);
+
+    int it = 0;
+    for (int u = unit0; u < num_units; u += unit_stride, ++it) {
+        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
+        bool got = mbar_wait_warp<kPair == 2>(bars.accf(0), (uint32_t)it & 1u, wc);
+        if (got && resid && !ti.dummy) {
+            got = mbar_wait_warp<false>(bars.resf(), res_phase, wc);
+            res_phase ^= 1u;
+            if (issuer) res_pending = false;
+        }
+        if (bar_any(1, 32 * kEpiWarps, !got)) break;  // same decision in every epilogue warp
+        tc_fence_after();
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+        uint8_t *rowp = buf + row * 128;  // row `row` of block 0
+        const int sw = row & 7;
+        float scale = 1.f;
+        if (p.epi == kEpiNormSilu) {
+            float ss = 0.f;
+            for (int c = c_begin; c < c_end; c += 32) {
+                uint32_t r[32];
+                const int n = c_end - c >= 32 ? 32 : 16;
+                tmem_ld_cols(tb + (uint32_t)c, n, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    if (i < n) {
+                        const float v = __uint_as_float(r[i]) + s_bias[c + i];
+                        ss += v * v;
+                    }
+                }
+            }
+            s_part[half * kBlockM + row] = ss;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+            scale = p.sqrt_c / fmaxf(sqrtf(s_part[row] + s_part[kBlockM + row]), p.eps);
+        }
+        for (int c = c_begin; c < c_end; c += 32) {
+            uint32_t r[32];
+            const int n = c_end - c >= 32 ? 32 : 16;
+            tmem_ld_cols(tb + (uint32_t)c, n, r);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (8 * k < n) {
+                    const int ch = c + 8 * k;  // first channel of this 16-byte piece
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        rowp + (ch >> 6) * (kBlockM * 128) + ((((ch & 63) >> 3) ^ sw) << 4));
+                    float v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * k + i]) + s_bias[ch + i];
+                    if (p.epi == kEpiNormSilu) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float z = v[i] * scale * s_gamma[ch + i];
+                            v[i] = __fdividef(z, 1.0f + __expf(-z));
+                        }
+                    } else if (resid) {
+                        const uint4 x4 = *dst;
+                        const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            v[2 * i] += __uint_as_float(xs[i] << 16);
+                            v[2 * i + 1] += __uint_as_float(xs[i] & 0xffff0000u);
+                        }
+                    }
+                    *dst = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                }
+            }
+        }
+        fence_proxy_async_smem();  // the tile in `buf` is visible to the TMA stores below
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+        if (lane == 0) {
+            // TMEM read out: the MMA warp may start the next tile now.
+            if (kPair == 2)
+                mbar_arrive_cluster(mapa_shared(bars.acce(0), 0));
+            else
+                mbar_arrive(bars.acce(0));
+        }
+        if (issuer) {
+            if (!ti.dummy) {
+                for (int b = 0; b < nblk; ++b)
+                    tma_store_3d(mapY, buf_s + (uint32_t)b * (kBlockM * 128u), b * 64, ti.pos,
+                                 ti.frame);
+                bulk_commit();
+            }
+            // The buffer is reused only after the stores have read it.
+            bulk_wait_read_all();
+            if (resid && u + unit_stride < num_units) issue_residual(u + unit_stride);
+        }
+    }
+    if (issuer) {
+        bulk_wait_all();
+        if (res_pending) {  // aborted with a residual load in flight: let it land
+            volatile int no_abort = 0;
+            const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+            mbar_wait(bars.resf(), res_phase, dc);
+        }
+    }
+}
+
 template <int kPair, int KK, int NSUB, int NP>
 __global__ void __launch_bounds__(kThreads, 1)
 conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapC,
                       const __grid_constant__ CUtensorMap mapB,
                       const __grid_constant__ CUtensorMap mapSA,
-                      const __grid_constant__ CUtensorMap mapSB, const ConvArgs p) {
+                      const __grid_constant__ CUtensorMap mapSB,
+                      const __grid_constant__ CUtensorMap mapY,
+                      const __grid_constant__ CUtensorMap mapR, const ConvArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -530,6 +695,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
     float *s_part = s_gamma + p.c_out;  // [2][128] partial sums of squares
+    uint8_t *s_stage = reinterpret_cast<uint8_t *>(s_part + 2 * kBlockM);  // output staging
 
     // Work units: single tiles, or pairs of consecutive tiles per cluster.
     const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
@@ -547,6 +713,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
             mbar_init(bars.acce(a), kEpiWarps * kPair);
         }
         mbar_init(bars.drain(), 1);
+        mbar_init(bars.resf(), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -557,6 +724,10 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         if (p.kc_short) {
             tma_prefetch_desc(&mapSA);
             tma_prefetch_desc(&mapSB);
+        }
+        if (p.staged) {
+            tma_prefetch_desc(&mapY);
+            if (p.epi == kEpiResidual) tma_prefetch_desc(&mapR);
         }
     }
     if (warp == 1) {
@@ -592,8 +763,14 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
             conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
                                           num_units);
     } else {
-        conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, s_part, bars, wc, unit0,
-                             unit_stride, num_units, rank);
+        if (p.staged)
+            conv_epilogue_staged<kPair>(p, tmem_base, s_bias, s_gamma, s_part,
+                                        smem + p.off_stage, &mapY, &mapR, bars, wc, unit0,
+                                        unit_stride, num_units, rank);
+        else
+            conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, s_part,
+                                 s_stage + (threadIdx.x / 32 - 2) * kStageBytesPerWarp, bars, wc,
+                                 unit0, unit_stride, num_units, rank);
     }
     __syncwarp();
     tc_fence_before();
@@ -676,6 +853,20 @@ bool encode_im2col(CUtensorMap *m, const void *base, int C, int W, int H, int fr
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [frames][HW][C] bf16 view with a (64 channels x 128 rows x 1 frame) box,
+// 128-byte swizzle: rows of a tile past the frame's end are out of bounds
+// (stores skip them, loads read zeros).
+bool encode_frames(CUtensorMap *m, const void *base, int C, int HW, int frames) {
+    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)HW, (cuuint64_t)frames};
+    cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)HW * C * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kBlockM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int pick_sw(int c) { return c % 64 == 0 ? 64 : (c % 32 == 0 ? 32 : 16); }
 
 struct Plan {
@@ -684,6 +875,8 @@ struct Plan {
     uint32_t a_sub, b_sub, a_bytes, stage_bytes;
     uint32_t off_bars, off_misc, off_vec, smem_bytes;
     int acc_cols, nacc, tmem_cols;
+    int staged;
+    uint32_t off_stage;
 };
 
 // CTA pairs halve each CTA's share of the B (weight) operand -- half the
@@ -720,16 +913,29 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
     while (pl.tmem_cols < cols) pl.tmem_cols *= 2;
     if (pl.tmem_cols > 512) return false;
 
-    const uint32_t reserve = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out +
-                             2u * 4u * kBlockM /*norm partial sums*/;
     const uint32_t b_rows = (uint32_t)(s.c_out / pair);
     const int g_main = s.c_in / sw, g_sc = s.sc_in ? s.c_sc / sw : g_main;
     const int min_stages = pair == 2 ? 4 : 3;
+    // Whole-tile staged epilogue when a single TMEM accumulator leaves the
+    // tensor core idle during the epilogue (c_out > 256) and the bf16 tile
+    // fits next to a 3-deep pipeline.
+    const uint32_t stage_tile = (uint32_t)kBlockM * s.c_out * 2u;
+    const uint32_t fixed = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out +
+                           2u * 4u * kBlockM /*norm partial sums*/;
+    pl.staged = 0;
+    if (pl.nacc == 1 && s.c_out % 64 == 0) {
+        const uint32_t sb1 = (kBlockM + b_rows) * (uint32_t)sw * 2u;
+        if (3u * ((sb1 + 1023u) & ~1023u) + fixed + stage_tile <= (uint32_t)kSmemBudget)
+            pl.staged = 1;
+    }
+    const uint32_t reserve =
+        fixed + (pl.staged ? stage_tile : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
+    const int need_stages = pl.staged ? 3 : min_stages;
     pl.nsub = 1;
     for (int d = 4; d >= 1; --d) {
         if (d * sw > 128 || g_main % d || g_sc % d) continue;
         const uint32_t sb = (uint32_t)d * (kBlockM + b_rows) * sw * 2;
-        if (min_stages * sb + reserve <= (uint32_t)kSmemBudget) {
+        if (need_stages * ((sb + 1023u) & ~1023u) + reserve <= (uint32_t)kSmemBudget) {
             pl.nsub = d;
             break;
         }
@@ -743,17 +949,22 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
     pl.stages = (int)((kSmemBudget - reserve) / pl.stage_bytes);
     if (pl.stages > 8) pl.stages = 8;
     if (pl.stages < 2) return false;
-    pl.off_bars = pl.stage_bytes * pl.stages;
-    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 5);
+    uint32_t off = pl.stage_bytes * pl.stages;
+    pl.off_stage = off;
+    if (pl.staged) off += stage_tile;
+    pl.off_bars = off;
+    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 6);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM;
+    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
+                    (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
     if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
     return pl.smem_bytes <= (uint32_t)kSmemBudget;
 }
 
 typedef void (*ConvKernelFn)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                             const CUtensorMap, const CUtensorMap, const ConvArgs);
+                             const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                             const CUtensorMap, const ConvArgs);
 
 // The specialisation for a plan: unrolled MMA issue for every (k-steps per
 // sub-tile, sub-tiles per stage, N-pieces) the planner produces, run-time
@@ -853,7 +1064,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     const int HW = s.H * s.W;
     const int frames = s.B * s.T;
     const int64_t M = (int64_t)frames * HW;
-    CUtensorMap mA, mC, mB, mSA, mSB;
+    CUtensorMap mA, mC, mB, mSA, mSB, mY, mR;
+    memset(&mY, 0, sizeof(mY));
+    memset(&mR, 0, sizeof(mR));
     memset(&mC, 0, sizeof(mC));
     memset(&mSA, 0, sizeof(mSA));
     memset(&mSB, 0, sizeof(mSB));
@@ -871,6 +1084,10 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
         ok = ok && encode_2d(&mSA, s.sc_in, (uint64_t)s.c_sc, (uint64_t)M, pl.sw, kBlockM, pl.sw);
         ok = ok && encode_2d(&mSB, s.sc_w, (uint64_t)s.c_sc, (uint64_t)s.c_out, pl.sw, b_box,
                              pl.sw);
+    }
+    if (pl.staged) {
+        ok = ok && encode_frames(&mY, s.out, s.c_out, HW, frames);
+        if (s.epi == kEpiResidual) ok = ok && encode_frames(&mR, s.resid, s.c_out, HW, frames);
     }
     if (!ok) return cudaErrorInvalidValue;
 
@@ -902,6 +1119,8 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.off_bars = pl.off_bars;
     a.off_misc = pl.off_misc;
     a.off_vec = pl.off_vec;
+    a.staged = pl.staged;
+    a.off_stage = pl.off_stage;
     a.acc_cols = pl.acc_cols;
     a.nacc = pl.nacc;
     a.tmem_cols = pl.tmem_cols;
@@ -936,7 +1155,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = ctx.stream;
-    return cudaLaunchKernelEx(&cfg, fn, mA, mC, mB, mSA, mSB, a);
+    return cudaLaunchKernelEx(&cfg, fn, mA, mC, mB, mSA, mSB, mY, mR, a);
 }
 
 }  // namespace wanvae
