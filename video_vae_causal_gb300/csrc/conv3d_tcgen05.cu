@@ -591,25 +591,10 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
         uint8_t *rowp = buf + row * 128;  // row `row` of block 0
         const int sw = row & 7;
-        float scale = 1.f;
-        if (p.epi == kEpiNormSilu) {
-            float ss = 0.f;
-            for (int c = c_begin; c < c_end; c += 32) {
-                uint32_t r[32];
-                const int n = c_end - c >= 32 ? 32 : 16;
-                tmem_ld_cols(tb + (uint32_t)c, n, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (i < n) {
-                        const float v = __uint_as_float(r[i]) + s_bias[c + i];
-                        ss += v * v;
-                    }
-                }
-            }
-            s_part[half * kBlockM + row] = ss;
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-            scale = p.sqrt_c / fmaxf(sqrtf(s_part[row] + s_part[kBlockM + row]), p.eps);
-        }
+        const bool norm = p.epi == kEpiNormSilu;
+        // Pass 1: TMEM -> acc + bias (+ residual) -> bf16 tile in `buf`.  For
+        // the fused norm this stores h = acc + bias and sums h^2 in fp32.
+        float ss = 0.f;
         for (int c = c_begin; c < c_end; c += 32) {
             uint32_t r[32];
             const int n = c_end - c >= 32 ? 32 : 16;
@@ -623,12 +608,9 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
                     float v[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[8 * k + i]) + s_bias[ch + i];
-                    if (p.epi == kEpiNormSilu) {
+                    if (norm) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float z = v[i] * scale * s_gamma[ch + i];
-                            v[i] = __fdividef(z, 1.0f + __expf(-z));
-                        }
+                        for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
                     } else if (resid) {
                         const uint4 x4 = *dst;
                         const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
@@ -643,7 +625,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
                 }
             }
         }
-        fence_proxy_async_smem();  // the tile in `buf` is visible to the TMA stores below
+        if (norm) s_part[half * kBlockM + row] = ss;
         tc_fence_before();
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
         if (lane == 0) {
@@ -653,6 +635,30 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
             else
                 mbar_arrive(bars.acce(0));
         }
+        if (norm) {
+            // Pass 2, overlapping the next tile's MMAs: a2 = SiLU(h / max(|h|, eps)
+            // * sqrt(C) * gamma), in place in `buf`.
+            const float scale =
+                p.sqrt_c / fmaxf(sqrtf(s_part[row] + s_part[kBlockM + row]), p.eps);
+            for (int ch = c_begin; ch < c_end; ch += 8) {
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    rowp + (ch >> 6) * (kBlockM * 128) + ((((ch & 63) >> 3) ^ sw) << 4));
+                const uint4 h4 = *dst;
+                const uint32_t hs[4] = {h4.x, h4.y, h4.z, h4.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float z0 = __uint_as_float(hs[i] << 16) * scale * s_gamma[ch + 2 * i];
+                    float z1 = __uint_as_float(hs[i] & 0xffff0000u) * scale * s_gamma[ch + 2 * i + 1];
+                    z0 = __fdividef(z0, 1.0f + __expf(-z0));
+                    z1 = __fdividef(z1, 1.0f + __expf(-z1));
+                    o[i] = pack_bf16x2(z0, z1);
+                }
+                *dst = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        fence_proxy_async_smem();  // the tile in `buf` is visible to the TMA stores below
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
         if (issuer) {
             if (!ti.dummy) {
                 for (int b = 0; b < nblk; ++b)
