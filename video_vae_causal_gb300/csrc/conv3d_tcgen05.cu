@@ -145,7 +145,6 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                               int num_units, uint32_t rank) {
     const int frames = p.num_tiles / p.tiles_per_frame;  // B*T
     const int M = frames * p.HW;
-    const int half_n = p.piece_n / kPair;
     int stage = 0;
     uint32_t phase = 0, fills = 0;
     bool ok = true;
@@ -205,17 +204,15 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                         else
                             tma_load_2d(da, mapA, fb, c0, row0);
                     }
-                    for (int j = 0; j < p.n_pieces; ++j) {
-                        const uint32_t db = sb + (uint32_t)s * p.b_sub_bytes +
-                                            (uint32_t)(j * half_n * p.sw * 2);
-                        const int brow = j * p.piece_n + (int)rank * half_n;
-                        const CUtensorMap *bm = shortcut ? mapSB : mapB;
-                        const int bk = shortcut ? c0 : tap * p.c_in + c0;
-                        if (kPair == 2)
-                            tma_load_2d_pair(db, bm, fb, bk, brow);
-                        else
-                            tma_load_2d(db, bm, fb, bk, brow);
-                    }
+                    // This CTA's rows of every N-piece in one box: the weight
+                    // map is viewed as [piece][pair rank][half_n rows][K].
+                    const uint32_t db = sb + (uint32_t)s * p.b_sub_bytes;
+                    const CUtensorMap *bm = shortcut ? mapSB : mapB;
+                    const int bk = shortcut ? c0 : tap * p.c_in + c0;
+                    if (kPair == 2)
+                        tma_load_4d_pair(db, bm, fb, bk, 0, (int)rank, 0);
+                    else
+                        tma_load_4d(db, bm, fb, bk, 0, 0, 0);
                 }
                 ++fills;
                 if (++stage == p.stages) {
@@ -873,6 +870,22 @@ bool encode_frames(CUtensorMap *m, const void *base, int C, int HW, int frames) 
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weights [c_out][K] (K contiguous) viewed as [n_pieces][pair][half_n][K] with
+// a box of (sw, half_n, 1, n_pieces): one load brings a CTA's rows of every
+// N-piece, landing as [piece][half_n rows][sw] -- the B layout the MMAs read.
+bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int pair,
+                    int n_pieces, int sw) {
+    const int piece_n = c_out / n_pieces, half_n = piece_n / pair;
+    cuuint64_t dims[4] = {K, (cuuint64_t)half_n, (cuuint64_t)pair, (cuuint64_t)n_pieces};
+    cuuint64_t strides[3] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)piece_n * K * 2};
+    cuuint32_t box[4] = {(cuuint32_t)sw, (cuuint32_t)half_n, 1, (cuuint32_t)n_pieces};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int pick_sw(int c) { return c % 64 == 0 ? 64 : (c % 32 == 0 ? 32 : 16); }
 
 struct Plan {
@@ -1076,7 +1089,6 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     memset(&mC, 0, sizeof(mC));
     memset(&mSA, 0, sizeof(mSA));
     memset(&mSB, 0, sizeof(mSB));
-    const uint32_t b_box = (uint32_t)(pl.piece_n / pl.pair);
     bool ok = true;
     if (s.k == 3) {
         ok = ok && encode_im2col(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw);
@@ -1084,12 +1096,12 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     } else {
         ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
     }
-    ok = ok && encode_2d(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, (uint64_t)s.c_out, pl.sw,
-                         b_box, pl.sw);
+    ok = ok && encode_weights(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, s.c_out, pl.pair,
+                              pl.n_pieces, pl.sw);
     if (s.sc_in) {
         ok = ok && encode_2d(&mSA, s.sc_in, (uint64_t)s.c_sc, (uint64_t)M, pl.sw, kBlockM, pl.sw);
-        ok = ok && encode_2d(&mSB, s.sc_w, (uint64_t)s.c_sc, (uint64_t)s.c_out, pl.sw, b_box,
-                             pl.sw);
+        ok = ok && encode_weights(&mSB, s.sc_w, (uint64_t)s.c_sc, s.c_out, pl.pair, pl.n_pieces,
+                                  pl.sw);
     }
     if (pl.staged) {
         ok = ok && encode_frames(&mY, s.out, s.c_out, HW, frames);
