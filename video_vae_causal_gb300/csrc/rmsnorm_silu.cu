@@ -26,8 +26,11 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z));
 // One group of L lanes owns one voxel; each lane holds VPT 16-byte vectors
 // of it (vector j of the voxel lives in lane j % L, slot j / L), so every
 // warp-wide load covers 32 consecutive 16-byte vectors of (32 / L) voxels.
-// The channel sum of squares is reduced with xor-shuffles inside the group.
-template <bool F32, int VPT>
+// A warp works on U such voxel groups per iteration and issues all their
+// loads before the first reduction, so U * VPT loads per lane are in flight
+// (the pass is bound by DRAM latency x bytes in flight).  The channel sum of
+// squares is reduced with xor-shuffles inside the group.
+template <bool F32, int VPT, int U>
 __global__ void __launch_bounds__(256)
 rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                     const float *__restrict__ gamma, int64_t n, int C, int L, float eps,
@@ -41,55 +44,71 @@ rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
     const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
 
-    for (int64_t v0 = warp_id * gpw; v0 < n; v0 += nwarps * gpw) {
-        const int64_t v = v0 + grp;
-        const bool active = v < n;
-        uint4 buf[VPT];
-        float ss = 0.f;
+    for (int64_t v0 = warp_id * gpw * U; v0 < n; v0 += nwarps * gpw * U) {
+        uint4 buf[U][VPT];
+        float ss[U];
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            if (active) {
-                buf[i] = __ldg(x + v * V + sub + i * L);
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * gpw + grp;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i)
+                if (v < n) buf[u][i] = __ldg(x + v * V + sub + i * L);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * gpw + grp;
+            ss[u] = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                if (v >= n) continue;
                 if (F32) {
-                    float a = __uint_as_float(buf[i].x), b = __uint_as_float(buf[i].y);
-                    float c = __uint_as_float(buf[i].z), d = __uint_as_float(buf[i].w);
-                    ss += a * a + b * b + c * c + d * d;
+                    float a = __uint_as_float(buf[u][i].x), b = __uint_as_float(buf[u][i].y);
+                    float c = __uint_as_float(buf[u][i].z), d = __uint_as_float(buf[u][i].w);
+                    ss[u] += a * a + b * b + c * c + d * d;
                 } else {
-                    const uint32_t w4[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                    const uint32_t w4[4] = {buf[u][i].x, buf[u][i].y, buf[u][i].z, buf[u][i].w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         float a = bf16lo(w4[k]), b = bf16hi(w4[k]);
-                        ss += a * a + b * b;
+                        ss[u] += a * a + b * b;
                     }
                 }
             }
         }
-        for (int off = L >> 1; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        const float scale = sqrt_c / fmaxf(sqrtf(ss), eps);
-        if (!active) continue;
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            const int j = sub + i * L;
-            const float4 *g4 = reinterpret_cast<const float4 *>(gamma + j * E);
-            uint4 o;
-            if (F32) {
-                const float4 g = __ldg(g4);
-                o.x = __float_as_uint(silu(__uint_as_float(buf[i].x) * scale * g.x));
-                o.y = __float_as_uint(silu(__uint_as_float(buf[i].y) * scale * g.y));
-                o.z = __float_as_uint(silu(__uint_as_float(buf[i].z) * scale * g.z));
-                o.w = __float_as_uint(silu(__uint_as_float(buf[i].w) * scale * g.w));
-            } else {
-                const float4 ga = __ldg(g4), gb = __ldg(g4 + 1);
-                o.x = pack_bf16x2(silu(bf16lo(buf[i].x) * scale * ga.x),
-                                  silu(bf16hi(buf[i].x) * scale * ga.y));
-                o.y = pack_bf16x2(silu(bf16lo(buf[i].y) * scale * ga.z),
-                                  silu(bf16hi(buf[i].y) * scale * ga.w));
-                o.z = pack_bf16x2(silu(bf16lo(buf[i].z) * scale * gb.x),
-                                  silu(bf16hi(buf[i].z) * scale * gb.y));
-                o.w = pack_bf16x2(silu(bf16lo(buf[i].w) * scale * gb.z),
-                                  silu(bf16hi(buf[i].w) * scale * gb.w));
+        for (int u = 0; u < U; ++u)
+            for (int off = L >> 1; off > 0; off >>= 1)
+                ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * gpw + grp;
+            if (v >= n) continue;
+            const float scale = sqrt_c / fmaxf(sqrtf(ss[u]), eps);
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int j = sub + i * L;
+                const float4 *g4 = reinterpret_cast<const float4 *>(gamma + j * E);
+                const uint4 b = buf[u][i];
+                uint4 o;
+                if (F32) {
+                    const float4 g = __ldg(g4);
+                    o.x = __float_as_uint(silu(__uint_as_float(b.x) * scale * g.x));
+                    o.y = __float_as_uint(silu(__uint_as_float(b.y) * scale * g.y));
+                    o.z = __float_as_uint(silu(__uint_as_float(b.z) * scale * g.z));
+                    o.w = __float_as_uint(silu(__uint_as_float(b.w) * scale * g.w));
+                } else {
+                    const float4 ga = __ldg(g4), gb = __ldg(g4 + 1);
+                    o.x = pack_bf16x2(silu(bf16lo(b.x) * scale * ga.x),
+                                      silu(bf16hi(b.x) * scale * ga.y));
+                    o.y = pack_bf16x2(silu(bf16lo(b.y) * scale * ga.z),
+                                      silu(bf16hi(b.y) * scale * ga.w));
+                    o.z = pack_bf16x2(silu(bf16lo(b.z) * scale * gb.x),
+                                      silu(bf16hi(b.z) * scale * gb.y));
+                    o.w = pack_bf16x2(silu(bf16lo(b.w) * scale * gb.z),
+                                      silu(bf16hi(b.w) * scale * gb.w));
+                }
+                y[v * V + j] = o;
             }
-            y[v * V + j] = o;
         }
     }
 }
@@ -103,17 +122,18 @@ cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n,
     while (L < 32 && V % (2 * L) == 0) L *= 2;  // largest power of two dividing V
     const int vpt = V / L;
     const int threads = 256;
-    const int64_t voxels_per_block = (threads / 32) * (32 / L);
+    const int64_t voxels_per_block = (threads / 32) * (32 / L) * (vpt <= 4 ? 2 : 1);
     int64_t blocks = (n + voxels_per_block - 1) / voxels_per_block;
-    const int64_t cap = (int64_t)ctx.num_sms * 8;
+    const int64_t cap = (int64_t)ctx.num_sms * 3;  // one resident wave (72 registers/thread)
     if (blocks > cap) blocks = cap;
     const float sqrt_c = sqrtf((float)C);
     auto *xi = static_cast<const uint4 *>(x);
     auto *yo = static_cast<uint4 *>(y);
 #define WANVAE_NORM_CASE(K)                                                              \
     case K:                                                                              \
-        rmsnorm_silu_kernel<F32, K><<<(unsigned)blocks, threads, 0, ctx.stream>>>(       \
-            xi, yo, gamma, n, C, L, eps, sqrt_c);                                        \
+        rmsnorm_silu_kernel<F32, K, (K <= 4 ? 2 : 1)>                                    \
+            <<<(unsigned)blocks, threads, 0, ctx.stream>>>(xi, yo, gamma, n, C, L, eps,  \
+                                                           sqrt_c);                      \
         break;
     switch (vpt) {
         WANVAE_NORM_CASE(1)
