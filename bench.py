@@ -36,11 +36,17 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: per workload, ~0.5-1.5 s of GPU time)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["tiny", "latent_fullT", "stream_720p", "reduce_384_192",
+                             "fullres_96"],
+                    help="latent_fullT (default) is the headline; the others are the remaining "
+                         "workloads of the design notes")
     return ap.parse_args()
 
 
@@ -155,9 +161,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def workload_config(B, T, H, W, ci, co, ws):
-    return {"workload": "latent_fullT: ResidualBlock full-T over x bf16 [1,21,60,104,384], "
-                        "C_in=C_out=384, identity shortcut",
+WORKLOAD_TEXT = {
+    "tiny": "tiny: ResidualBlock full-T over x bf16 [1,3,16,16,32], identity shortcut",
+    "latent_fullT": "latent_fullT: ResidualBlock full-T over x bf16 [1,21,60,104,384], "
+                    "C_in=C_out=384, identity shortcut",
+    "stream_720p": "stream_720p: ResidualBlock frame by frame, 21 calls of x bf16 "
+                   "[1,1,90,160,384] with a 2-frame feat_cache per conv, C=384",
+    "reduce_384_192": "reduce_384_192: ResidualBlock full-T over x bf16 [1,41,240,416,384], "
+                      "C_in=384 -> C_out=192, 1x1x1 conv shortcut",
+    "fullres_96": "fullres_96: ResidualBlock full-T over x bf16 [1,81,480,832,96], C=96, "
+                  "identity shortcut",
+}
+
+
+def workload_config(name, B, T, H, W, ci, co, ws):
+    return {"workload": WORKLOAD_TEXT[name],
             "B": B, "T": T, "H": H, "W": W, "c_in": ci, "c_out": co,
             "l2": "flushed between steps (256 MiB write outside the timed events)",
             "parallelism": f"replicas x{ws}"}
@@ -173,7 +191,7 @@ def cpu_baseline(x, params, H, W, budget_s=12.0):
     rng = np.random.default_rng(0)
 
     def run(rows):
-        xs = x[:, 2:3, :rows].contiguous()
+        xs = x[:, 2:3, :rows].contiguous().cpu()
         cA = rng.standard_normal((1, 2, rows, W, C_in))
         cB = rng.standard_normal((1, 2, rows, W, C_out))
         t0 = time.perf_counter()
@@ -193,33 +211,40 @@ def bench_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    import torch
     import oracle
     from video_vae_causal_gb300 import synth
-    dims, ci, co, _ = synth.WORKLOADS[WORKLOAD]
+    name = args.workload
+    dims, ci, co, _ = synth.WORKLOADS[name]
     B, T, H, W = dims
-    x, p = synth.make_resblock_inputs(dims, ci, co, seed=0)
+    # The oracle only needs the few rows it runs on: draw the clip's first
+    # frames with the same recipe (small workloads: the whole clip).
+    x, p = synth.make_resblock_inputs((B, min(T, 3), H, W), ci, co, seed=0)
     params = oracle.Params.from_dict(p)
-    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    steps = args.steps if args.steps else 10
+    budget = max(1.0, 60.0 / max(1, steps + args.warmup))
     for _ in range(args.warmup):
         cpu_baseline(x, params, H, W, budget_s=budget)
     vals, samples = [], []
-    for _ in range(args.steps):
+    for _ in range(steps):
         r = cpu_baseline(x, params, H, W, budget_s=budget)
         vals.append(r["value"])
         samples.append(r["sample"])
     v = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": v,
-        "unit": "voxels/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "unit": "voxels/s", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
         "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": workload_config(B, T, H, W, ci, co, 1),
+        "config": workload_config(name, B, T, H, W, ci, co, 1),
         "cpu_baseline": {"value": v, "unit": "voxels/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": samples[-1]},
         "e2e": {"value": v, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+DEFAULT_STEPS = {"tiny": 300, "latent_fullT": 300, "stream_720p": 20, "reduce_384_192": 20,
+                 "fullres_96": 12}
 
 
 def bench_ours(args):
@@ -237,31 +262,55 @@ def bench_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     wanvae.load()
 
-    dims, ci, co, _ = synth.WORKLOADS[WORKLOAD]
+    name = args.workload
+    dims, ci, co, calls = synth.WORKLOADS[name]
     B, T, H, W = dims
     M = B * T * H * W
-    x_cpu, p_cpu = synth.make_resblock_inputs(dims, ci, co, seed=0)
-    x = x_cpu.to(dev)
-    p = {k: v.to(dev) for k, v in p_cpu.items()}
+    streaming = calls > 0
+    # Small workloads are drawn on the CPU generator, the multi-GB ones on the
+    # device generator (same recipe, different stream of numbers).
+    on_dev = M * max(ci, co) > (1 << 30)
+    x, p = synth.make_resblock_inputs(dims, ci, co, seed=0, device=dev if on_dev else "cpu")
+    x_cpu = None if on_dev else x
+    p_cpu = {k: v.cpu() for k, v in p.items()}
+    x = x.to(dev)
+    p = {k: v.to(dev) for k, v in p.items()}
     params = wanvae.make_params(p)
     y = torch.empty((B, T, H, W, co), dtype=torch.bfloat16, device=dev)
-    wsp = wanvae.make_workspace(dims, ci, co, device=dev)
+    call_dims = (B, 1, H, W) if streaming else dims
+    wsp = wanvae.make_workspace(call_dims, ci, co, device=dev)
+    caches = None
+    if streaming:
+        caches = (torch.zeros((B, 2, H, W, ci), dtype=torch.bfloat16, device=dev),
+                  torch.zeros((B, 2, H, W, co), dtype=torch.bfloat16, device=dev))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ncalls = T if streaming else 1
 
-    def step(events=None):
-        wanvae.resblock_forward(x, params, y=y, workspace=wsp, events=events)
+    def forward(xin, events=None):
+        """One step: the whole clip, full-T or frame by frame with feat_cache."""
+        if not streaming:
+            wanvae.resblock_forward(xin, params, y=y, workspace=wsp,
+                                    events=events[0] if events else None)
+            return
+        for c in caches:
+            c.zero_()  # a new clip starts with empty caches (before the first event)
+        for t in range(T):
+            wanvae.resblock_forward(xin[:, t:t + 1], params, y=y[:, t:t + 1], cache=caches,
+                                    workspace=wsp, events=events[t] if events else None)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        step()
+        forward(x)
     wanvae.sync_status()
 
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for e4 in evs:
-        for e in e4:
-            e.record(stream)
+    K = args.steps if args.steps else DEFAULT_STEPS[name]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ncalls)]
+           for _ in range(K)]
+    for step_ev in evs:
+        for e4 in step_ev:
+            for e in e4:
+                e.record(stream)
     torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
@@ -271,7 +320,7 @@ def bench_ours(args):
         t_wall = time.perf_counter()
         for k in range(K):
             flush.zero_()
-            step(evs[k])
+            forward(x, evs[k])
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
     if ws > 1:
@@ -280,43 +329,48 @@ def bench_ours(args):
     launches = wanvae.launch_count() - n0
     wanvae.sync_status()
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    norm_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    convA_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    convB_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0][0].elapsed_time(e[-1][3]) for e in evs]
+    norm_ms = [sum(c[0].elapsed_time(c[1]) for c in e) for e in evs]
+    convA_ms = [sum(c[1].elapsed_time(c[2]) for c in e) for e in evs]
+    convB_ms = [sum(c[2].elapsed_time(c[3]) for c in e) for e in evs]
     total_ms = max_over_ranks(sum(step_ms), ws, dev)
     ms_per_step = total_ms / K
     value = replica_throughput(M, ws, K, total_ms)
 
     # ---- end to end through the public API with host buffers
+    if x_cpu is None:
+        x_cpu = x.cpu()
     x_host = x_cpu.pin_memory()
     y_host = torch.empty((B, T, H, W, co), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
     E = max(1, min(args.e2e_steps, K))
     for _ in range(2):
         x_dev.copy_(x_host, non_blocking=True)
-        wanvae.resblock_forward(x_dev, params, y=y, workspace=wsp)
+        forward(x_dev)
         y_host.copy_(y, non_blocking=True)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
         x_dev.copy_(x_host, non_blocking=True)
-        wanvae.resblock_forward(x_dev, params, y=y, workspace=wsp)
+        forward(x_dev)
         y_host.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     e2e_value = replica_throughput(M, ws, E, e2e_ms)
 
-    # ---- roofline of the dominant kernel (the conv)
+    # ---- roofline of the dominant kernel (the conv: two launches per call)
     peaks = load_peaks()
-    flop_conv = 2.0 * 27 * ci * co * M  # conv A; conv B is 2*27*co*co*M (equal here)
-    conv_ms = (sum(convA_ms) + sum(convB_ms)) / (2 * K)
+    flop_A = 2.0 * 27 * ci * co * M
+    flop_B = 2.0 * 27 * co * co * M + (2.0 * ci * co * M if ci != co else 0.0)
+    n_conv_launches = 2 * ncalls
+    flop_conv = (flop_A + flop_B) / n_conv_launches          # per launch, averaged
+    conv_ms = (sum(convA_ms) + sum(convB_ms)) / (K * n_conv_launches)
     achieved = flop_conv / (conv_ms / 1e3) / 1e12
     norm_gbs = (2.0 * ci * 2 * M) / (statistics.mean(norm_ms) / 1e3) / 1e9
-    traffic = profiled_traffic()
-    block_flop = 2.0 * 27 * M * (ci * co + co * co) + (2.0 * ci * co * M if ci != co else 0.0)
+    traffic = profiled_traffic() if name == WORKLOAD else None
+    block_flop = flop_A + flop_B
 
     if rank != 0:
         if ws > 1:
@@ -327,7 +381,7 @@ def bench_ours(args):
         "value": value, "unit": "voxels/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(B, T, H, W, ci, co, ws),
+        "config": workload_config(name, B, T, H, W, ci, co, ws),
         "block_tflops": block_flop / (ms_per_step / 1e3) / 1e12,
         "kernels_ms": {"rmsnorm_silu": statistics.mean(norm_ms),
                        "conv3d_A_normsilu": statistics.mean(convA_ms),
@@ -345,6 +399,10 @@ def bench_ours(args):
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
     }
+    if streaming:
+        line["per_call_ms"] = ms_per_step / ncalls
+        line["kernels_ms_note"] = ("per step of %d calls; the conv intervals include each "
+                                   "call's feat_cache update kernel" % ncalls)
     if not args.no_cpu_baseline and ws == 1:
         import oracle
         line["cpu_baseline"] = cpu_baseline(x_cpu, oracle.Params.from_dict(p_cpu), H, W)
