@@ -14,13 +14,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["pair", "single"])
+@pytest.fixture(params=["pair-im2col", "pair-halo", "single-im2col", "single-halo"])
 def variant(request, monkeypatch):
-    """Run a conv test on the CTA-pair kernel (default) and the single-CTA one."""
-    if request.param == "single":
+    """Run a conv test on every kernel variant: CTA pair or single CTA, and
+    per-tap im2col A loads or halo tiles (16 x 8 patches, one halo load per
+    temporal tap feeding the nine spatial taps)."""
+    pair, mode = request.param.split("-")
+    if pair == "single":
         monkeypatch.setenv("WANVAE_CONV_PAIR", "1")
     else:
         monkeypatch.delenv("WANVAE_CONV_PAIR", raising=False)
+    monkeypatch.setenv("WANVAE_CONV_HALO", "1" if mode == "halo" else "0")
     return request.param
 
 
@@ -72,6 +76,8 @@ CONV_CASES = [
     (1, 2, 10, 10, 16, 16),
     (1, 1, 3, 200, 128, 96),    # 5 tiles: a CTA pair's second slot is empty
     (1, 4, 5, 7, 64, 32),       # 1 tile per frame: pairs straddle frames t=0|1, 2|3
+    (1, 3, 32, 16, 96, 96),     # whole 16x8 patches (halo mode's own choice)
+    (2, 2, 16, 24, 64, 192),
 ]
 
 

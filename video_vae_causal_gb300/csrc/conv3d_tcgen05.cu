@@ -70,6 +70,9 @@ struct ConvArgs {
     int acc_cols, nacc, tmem_cols;
     int staged;          // epilogue through a whole-tile smem buffer + TMA stores
     uint32_t off_stage;  // 1024-aligned offset of that buffer
+    int halo;            // 16x8 patch tiles, one halo load per (kt, chunk) for 9 taps
+    int patches_w;       // patches per frame row (halo mode)
+    uint32_t off_a, a_stride, a_tx;  // halo ring: 2 buffers, bytes per CTA per load
     int epi;
     float eps, sqrt_c;
     const float *bias, *bias2, *gamma;
@@ -92,10 +95,37 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
     ti.pos = (tile - ti.frame * p.tiles_per_frame) * kBlockM;
     ti.n = ti.frame / p.T;
     ti.t = ti.frame - ti.n * p.T;
-    ti.h0 = ti.pos / p.W;
-    ti.w0 = ti.pos - ti.h0 * p.W;
-    ti.row0 = ti.frame * p.HW + ti.pos;
+    if (p.halo) {
+        // 16 x 8 (H x W) patch: tile row m is pixel (h0 + m / 8, w0 + m % 8).
+        const int pt = ti.pos / kBlockM;
+        const int ph = pt / p.patches_w;
+        ti.h0 = ph * 16;
+        ti.w0 = (pt - ph * p.patches_w) * 8;
+        ti.row0 = ti.frame * p.HW + ti.h0 * p.W + ti.w0;  // first pixel's voxel index
+    } else {
+        ti.h0 = ti.pos / p.W;
+        ti.w0 = ti.pos - ti.h0 * p.W;
+        ti.row0 = ti.frame * p.HW + ti.pos;
+    }
     return ti;
+}
+
+// Halo mode: every smem halo is 18 x 10 pixels (a 16 x 8 patch grown by the
+// 3x3 window), stored as planes of 8 channels: plane j holds 16 bytes for
+// each of the 180 pixels, row-major.  The MMA A operand of tap (kh, kw) is
+// the window starting at pixel (kh, kw): rows 16 bytes apart inside a
+// patch row, patch rows one halo row (10 pixels = 160 bytes) apart, K-planes
+// one plane (2880 bytes) apart -- a no-swizzle K-major operand.
+constexpr uint32_t kHaloW = 10, kHaloH = 18;
+constexpr uint32_t kPlaneBytes = kHaloW * kHaloH * 16;
+
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;  // swizzle mode 0: none
 }
 
 // First temporal tap of a work unit (one tile, or the two tiles of a CTA
@@ -132,6 +162,8 @@ struct Bars {
     __device__ uint32_t acce(int a) const { return base + 8u * (2 * stages + 2 + a); }
     __device__ uint32_t drain() const { return base + 8u * (2 * stages + 4); }
     __device__ uint32_t resf() const { return base + 8u * (2 * stages + 5); }
+    __device__ uint32_t fulla(int i) const { return base + 8u * (2 * stages + 6 + i); }
+    __device__ uint32_t emptya(int i) const { return base + 8u * (2 * stages + 8 + i); }
 };
 
 // TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
@@ -233,6 +265,179 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
     }
 }
 
+// 5-D tiled load (x = c0 innermost).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(c4)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *m,
+                                                 uint32_t cluster_bar, int c0, int c1, int c2,
+                                                 int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "r"(c4)
+        : "memory");
+}
+
+template <int kPair>
+__device__ __forceinline__ void load5(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
+                                      int c1, int c2, int c3, int c4) {
+    if (kPair == 2)
+        tma_load_5d_pair(dst, m, bar, c0, c1, c2, c3, c4);
+    else
+        tma_load_5d(dst, m, bar, c0, c1, c2, c3, c4);
+}
+template <int kPair>
+__device__ __forceinline__ void load4(uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0,
+                                      int c1, int c2, int c3) {
+    if (kPair == 2)
+        tma_load_4d_pair(dst, m, bar, c0, c1, c2, c3);
+    else
+        tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+}
+
+// Halo-mode producer.  Per unit: for each temporal tap kt and channel chunk
+// one halo load (A ring, 2 buffers), then nine weight loads (B ring), one per
+// spatial tap; then the shortcut segment's chunks (x patch into the A ring).
+template <int kPair>
+__device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *mapC,
+                                   const CUtensorMap *mapB, const CUtensorMap *mapSA,
+                                   const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
+                                   const Bars &bars, const WaitCtl &wc, int unit0,
+                                   int unit_stride, int num_units, uint32_t rank) {
+    const int frames = p.num_tiles / p.tiles_per_frame;
+    const int chunk = p.nsub * p.sw;  // channels per halo / per weight stage
+    int stage = 0, ia = 0;
+    uint32_t phase = 0, pha = 0, fills = 0, fills_a = 0;
+    bool ok = true;
+    auto next_b = [&](uint32_t &dst, uint32_t &fb) -> bool {
+        if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) return false;
+        const uint32_t fl = bars.full(stage);
+        if (rank == 0) mbar_arrive_expect_tx(fl, p.stage_tx * kPair);
+        fb = kPair == 2 ? mapa_shared(fl, 0) : fl;
+        dst = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
+        ++fills;
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        return true;
+    };
+    auto next_a = [&](uint32_t &dst, uint32_t &fb, uint32_t tx) -> bool {
+        if (!mbar_wait<kPair == 2>(bars.emptya(ia), pha ^ 1u, wc)) return false;
+        const uint32_t fl = bars.fulla(ia);
+        if (rank == 0) mbar_arrive_expect_tx(fl, tx * kPair);
+        fb = kPair == 2 ? mapa_shared(fl, 0) : fl;
+        dst = sbase + p.off_a + (uint32_t)ia * p.a_stride;
+        ++fills_a;
+        if (++ia == 2) {
+            ia = 0;
+            pha ^= 1u;
+        }
+        return true;
+    };
+    for (int u = unit0; ok && u < num_units; u += unit_stride) {
+        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
+        const int kt0 = unit_first_kt<kPair>(u, p);
+        for (int kt = kt0; ok && kt < 3; ++kt) {
+            const int tt = ti.t + kt - 2;
+            const CUtensorMap *am = mapA;
+            int fidx = frames;  // out of range: zeros
+            if (!ti.dummy) {
+                if (tt >= 0) {
+                    fidx = ti.n * p.T + tt;
+                } else if (p.has_cache) {
+                    am = mapC;
+                    fidx = ti.n * 2 + tt + 2;
+                }
+            }
+            for (int cc = 0; ok && cc < p.kc_main; ++cc) {
+                uint32_t da, fa;
+                if (!next_a(da, fa, p.a_tx)) {
+                    ok = false;
+                    break;
+                }
+                load5<kPair>(da, am, fa, 0, ti.w0 - 1, ti.h0 - 1, cc * (chunk / 8), fidx);
+                for (int t9 = 0; t9 < 9; ++t9) {
+                    uint32_t db, fb;
+                    if (!next_b(db, fb)) {
+                        ok = false;
+                        break;
+                    }
+                    const int tap = kt * 9 + t9;
+                    load5<kPair>(db, mapB, fb, tap * p.c_in + cc * chunk, 0, (int)rank, 0, 0);
+                }
+            }
+        }
+        // shortcut segment: the patch's own pixels of x (no shift)
+        for (int cc = 0; ok && cc < p.kc_short; ++cc) {
+            uint32_t da, fa, db, fb;
+            if (!next_a(da, fa, (uint32_t)p.nsub * kBlockM * p.sw * 2u)) {
+                ok = false;
+                break;
+            }
+            for (int s = 0; s < p.nsub; ++s)
+                load4<kPair>(da + (uint32_t)s * kBlockM * p.sw * 2u, mapSA, fa,
+                             (cc * p.nsub + s) * p.sw, ti.w0, ti.h0, ti.dummy ? frames : ti.frame);
+            if (!next_b(db, fb)) {
+                ok = false;
+                break;
+            }
+            load5<kPair>(db, mapSB, fb, cc * chunk, 0, (int)rank, 0, 0);
+        }
+    }
+    if (!ok && rank == 0) {
+        volatile int no_abort = 0;
+        const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+        uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
+        for (uint32_t f = fills - n; f < fills; ++f)
+            mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
+        n = fills_a < 2u ? fills_a : 2u;
+        for (uint32_t f = fills_a - n; f < fills_a; ++f)
+            mbar_wait<kPair == 2>(bars.fulla((int)(f % 2)), (f / 2) & 1u, dc);
+    }
+}
+
+// Halo-mode MMAs of one spatial tap: k-step ks uses A planes 2ks, 2ks+1 of
+// the halo window and B sub-tile ks / KK at k-offset ks % KK.
+template <int kPair, int KK, int NSUB, int NP>
+__device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc, uint64_t a0,
+                                               uint64_t b0, uint32_t idesc, bool first) {
+    const uint32_t b_sub16 = p.b_sub_bytes >> 4;
+    const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
+    constexpr uint32_t kPlane2 = (2 * kPlaneBytes) >> 4;
+    const int kk_n = KK > 0 ? KK : p.sw / 16, ns_n = KK > 0 ? NSUB : p.nsub;
+    const int np_n = KK > 0 ? NP : p.n_pieces;
+#pragma unroll
+    for (int s = 0; s < (KK > 0 ? NSUB : 8); ++s) {
+        if (KK == 0 && s >= ns_n) break;
+#pragma unroll
+        for (int kk = 0; kk < (KK > 0 ? KK : 4); ++kk) {
+            if (KK == 0 && kk >= kk_n) break;
+            const int ks = s * kk_n + kk;
+            const uint64_t ad = a0 + (uint64_t)(ks * kPlane2);
+            const uint32_t accum = (first && ks == 0) ? 0u : 1u;
+#pragma unroll
+            for (int j = 0; j < (KK > 0 ? NP : 32); ++j) {
+                if (KK == 0 && j >= np_n) break;
+                const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
+                const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
+                if (kPair == 2)
+                    mma_bf16_ss_pair(d, ad, bd, idesc, accum);
+                else
+                    mma_bf16_ss(d, ad, bd, idesc, accum);
+            }
+        }
+    }
+}
+
 // Issue the MMAs of one pipeline stage.  KK k-steps of 16 per swizzled
 // sub-tile, NSUB sub-tiles, NP N-pieces: all compile-time, so the loop is fully
 // unrolled and every descriptor is the stage's base plus a constant (the
@@ -278,6 +483,101 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
             }
         }
     }
+}
+
+template <int kPair, int KK, int NSUB, int NP>
+__device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base,
+                              const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
+                              int num_units) {
+    const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
+    const uint32_t row_bytes = (uint32_t)p.sw * 2u;
+    int stage = 0, ia = 0, it = 0;
+    uint32_t phase = 0, pha = 0;
+    bool ok = true;
+    auto commit = [&](uint32_t bar) {
+        if (kPair == 2)
+            mma_commit_pair_mc(bar, (uint16_t)0x3);
+        else
+            mma_commit(bar);
+    };
+    for (int u = unit0; ok && u < num_units; u += unit_stride, ++it) {
+        const int a = it % p.nacc;
+        const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
+        if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_cols);
+        const int kt0 = unit_first_kt<kPair>(u, p);
+        bool first = true;
+        for (int kt = kt0; ok && kt < 3; ++kt) {
+            for (int cc = 0; ok && cc < p.kc_main; ++cc) {
+                if (!mbar_wait<kPair == 2>(bars.fulla(ia), pha, wc)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t abuf = sbase + p.off_a + (uint32_t)ia * p.a_stride;
+                for (int t9 = 0; t9 < 9; ++t9) {
+                    if (!mbar_wait<kPair == 2>(bars.full(stage), phase, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int kh = t9 / 3, kw = t9 - 3 * (t9 / 3);
+                    const uint64_t a0 = sdesc_plain(abuf + (uint32_t)(kh * kHaloW + kw) * 16u,
+                                                    kPlaneBytes, kHaloW * 16u);
+                    const uint32_t sb = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
+                    issue_tap_halo<kPair, KK, NSUB, NP>(p, dacc, a0,
+                                                        sdesc_kmajor(sb, row_bytes, p.layout),
+                                                        idesc, first);
+                    first = false;
+                    commit(bars.empty(stage));
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                commit(bars.emptya(ia));
+                if (++ia == 2) {
+                    ia = 0;
+                    pha ^= 1u;
+                }
+            }
+        }
+        for (int cc = 0; ok && cc < p.kc_short; ++cc) {
+            if (!mbar_wait<kPair == 2>(bars.fulla(ia), pha, wc) ||
+                !mbar_wait<kPair == 2>(bars.full(stage), phase, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // x patch in the A buffer, swizzled like the weights: the stage
+            // issue routine of the im2col path applies unchanged.
+            const uint32_t abuf = sbase + p.off_a + (uint32_t)ia * p.a_stride;
+            const uint32_t sb = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
+            issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(abuf, row_bytes, p.layout),
+                                             sdesc_kmajor(sb, row_bytes, p.layout), idesc, first);
+            first = false;
+            commit(bars.empty(stage));
+            commit(bars.emptya(ia));
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++ia == 2) {
+                ia = 0;
+                pha ^= 1u;
+            }
+        }
+        if (!ok) break;
+        commit(bars.accf(a));
+    }
+    volatile int no_abort = 0;
+    const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+    if (kPair == 2)
+        mma_commit_pair(bars.drain());
+    else
+        mma_commit(bars.drain());
+    mbar_wait<kPair == 2>(bars.drain(), 0u, dc);
 }
 
 // MMA issuer (one thread of the leader CTA).
@@ -383,6 +683,40 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int ncols, uint32_t
     }
 }
 
+// Where the 32 rows of one epilogue warp live in the output: consecutive
+// voxels (im2col tiles; rows past the frame's end are invalid), or four patch
+// rows of 8 pixels one frame row (W voxels) apart (halo tiles; rows and
+// columns past the frame are invalid).
+struct RowMap {
+    int seg_rows;    // rows per contiguous segment (32 or 8)
+    int64_t pitch;   // voxels between segments
+    int nseg, ncol;  // valid segments, valid rows per segment
+    __device__ __forceinline__ bool valid(int r) const {
+        return r / seg_rows < nseg && r % seg_rows < ncol;
+    }
+    __device__ __forceinline__ int64_t offset(int r) const {
+        return (int64_t)(r / seg_rows) * pitch + r % seg_rows;
+    }
+};
+
+__device__ __forceinline__ RowMap warp_rows(const ConvArgs &p, const TileInfo &ti, int q) {
+    RowMap rm;
+    if (p.halo) {
+        rm.seg_rows = 8;
+        rm.pitch = p.W;
+        const int ns = p.H - ti.h0 - 4 * q, nc = p.W - ti.w0;
+        rm.nseg = ti.dummy ? 0 : (ns < 0 ? 0 : (ns > 4 ? 4 : ns));
+        rm.ncol = nc < 0 ? 0 : (nc > 8 ? 8 : nc);
+    } else {
+        rm.seg_rows = 32;
+        rm.pitch = 0;
+        const int nv = ti.dummy ? 0 : p.HW - ti.pos - q * 32;
+        rm.nseg = 1;
+        rm.ncol = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
+    }
+    return rm;
+}
+
 // Write one warp's 32-row x n-channel (n = 16 or 32) bf16 chunk: each lane
 // hands its row's n/8 16-byte pieces (o) to a swizzled shared buffer, then the
 // warp writes the chunk back four lanes per row, so every store instruction
@@ -390,7 +724,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int ncols, uint32_t
 // pieces.  Rows at or past `nvalid` (the frame's end) are not written.
 __device__ __forceinline__ void store_chunk(uint8_t *stg, const uint32_t (&o)[16], int n,
                                             __nv_bfloat16 *out_row0, int ldc, int c,
-                                            int nvalid) {
+                                            const RowMap &rm) {
     const int lane = threadIdx.x & 31;
     const int np = n / 8;  // 16-byte pieces per row
 #pragma unroll
@@ -405,10 +739,10 @@ __device__ __forceinline__ void store_chunk(uint8_t *stg, const uint32_t (&o)[16
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int r = j * 8 + (lane >> 2), q = lane & 3;
-        if (q < np && r < nvalid) {
+        if (q < np && rm.valid(r)) {
             const int slot = q ^ ((r >> 1) & 3);
             const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 64 + slot * 16);
-            *reinterpret_cast<uint4 *>(out_row0 + (int64_t)r * ldc + c + q * 8) = v;
+            *reinterpret_cast<uint4 *>(out_row0 + rm.offset(r) * ldc + c + q * 8) = v;
         }
     }
     __syncwarp();
@@ -443,14 +777,15 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         }
         tc_fence_after();
         const TileInfo ti = tile_info(u * kPair + (int)rank, p);
-        const bool valid = !ti.dummy && ti.pos + row < p.HW;
-        const int64_t g = (int64_t)ti.row0 + row;
+        // This warp's 32 rows; rows outside the frame (or of an empty pair
+        // slot) are not stored.
+        const RowMap rm = warp_rows(p, ti, q);
+        const bool valid = rm.valid(lane);
+        const int64_t wbase = p.halo ? (int64_t)ti.row0 + (int64_t)(4 * q) * p.W
+                                     : (int64_t)ti.row0 + q * 32;
+        const int64_t g = wbase + rm.offset(lane);
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols);
-        // This warp's 32 rows start at row q*32 of the tile; rows of a ragged
-        // tile past the frame's end (or of an empty pair slot) are not stored.
-        int nvalid = ti.dummy ? 0 : p.HW - ti.pos - q * 32;
-        nvalid = nvalid < 0 ? 0 : (nvalid > 32 ? 32 : nvalid);
-        __nv_bfloat16 *out_w = p.out + ((int64_t)ti.row0 + q * 32) * p.c_out;
+        __nv_bfloat16 *out_w = p.out + wbase * p.c_out;
         if (p.epi == kEpiNormSilu) {
             // RMS_norm over all c_out channels of this voxel, then SiLU.
             float ss = 0.f;
@@ -487,7 +822,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                         o[i] = pack_bf16x2(z0, z1);
                     }
                 }
-                store_chunk(stg, o, n, out_w, p.c_out, c, nvalid);
+                store_chunk(stg, o, n, out_w, p.c_out, c, rm);
             }
             // s_part is rewritten only after the next tile's bar_any, which
             // every warp reaches after its last read above.
@@ -520,7 +855,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 uint32_t o[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                store_chunk(stg, o, n, out_w, p.c_out, c, nvalid);
+                store_chunk(stg, o, n, out_w, p.c_out, c, rm);
             }
         }
         tc_fence_before();
@@ -567,9 +902,14 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         const TileInfo tn = tile_info(u * kPair + (int)rank, p);
         if (tn.dummy) return;
         mbar_arrive_expect_tx(bars.resf(), res_bytes);
-        for (int b = 0; b < nblk; ++b)
-            tma_load_3d(buf_s + (uint32_t)b * (kBlockM * 128u), mapR, bars.resf(), b * 64, tn.pos,
-                        tn.frame);
+        for (int b = 0; b < nblk; ++b) {
+            if (p.halo)
+                tma_load_4d(buf_s + (uint32_t)b * (kBlockM * 128u), mapR, bars.resf(), b * 64,
+                            tn.w0, tn.h0, tn.frame);
+            else
+                tma_load_3d(buf_s + (uint32_t)b * (kBlockM * 128u), mapR, bars.resf(), b * 64,
+                            tn.pos, tn.frame);
+        }
         res_pending = true;
     };
     if (issuer && resid && unit0 < num_units) issue_residual(unit0);
@@ -658,9 +998,14 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
         if (issuer) {
             if (!ti.dummy) {
-                for (int b = 0; b < nblk; ++b)
-                    tma_store_3d(mapY, buf_s + (uint32_t)b * (kBlockM * 128u), b * 64, ti.pos,
-                                 ti.frame);
+                for (int b = 0; b < nblk; ++b) {
+                    if (p.halo)
+                        tma_store_4d(mapY, buf_s + (uint32_t)b * (kBlockM * 128u), b * 64, ti.w0,
+                                     ti.h0, ti.frame);
+                    else
+                        tma_store_3d(mapY, buf_s + (uint32_t)b * (kBlockM * 128u), b * 64,
+                                     ti.pos, ti.frame);
+                }
                 bulk_commit();
             }
             // The buffer is reused only after the stores have read it.
@@ -717,6 +1062,10 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         mbar_init(bars.drain(), 1);
         mbar_init(bars.resf(), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.fulla(i), 1);
+            mbar_init(bars.emptya(i), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -758,13 +1107,23 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     const WaitCtl wc{p.wait_ns, p.err, abort_flag};
 
     if (warp == 0) {
-        if (lane == 0)
-            conv_producer<kPair>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc, unit0,
-                                 unit_stride, num_units, rank);
+        if (lane == 0) {
+            if (p.halo)
+                conv_producer_halo<kPair>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
+                                          unit0, unit_stride, num_units, rank);
+            else
+                conv_producer<kPair>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
+                                     unit0, unit_stride, num_units, rank);
+        }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0)
-            conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
-                                          num_units);
+        if (lane == 0 && rank == 0) {
+            if (p.halo)
+                conv_mma_halo<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0,
+                                                   unit_stride, num_units);
+            else
+                conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
+                                              num_units);
+        }
     } else {
         if (p.staged)
             conv_epilogue_staged<kPair>(p, tmem_base, s_bias, s_gamma, s_part,
@@ -873,12 +1232,50 @@ bool encode_frames(CUtensorMap *m, const void *base, int C, int HW, int frames) 
 // Weights [c_out][K] (K contiguous) viewed as [n_pieces][pair][half_n][K] with
 // a box of (sw, half_n, 1, n_pieces): one load brings a CTA's rows of every
 // N-piece, landing as [piece][half_n rows][sw] -- the B layout the MMAs read.
+// With nsub > 0 a fifth dimension of nsub sub-tiles (sw channels apart in K)
+// lands as [sub-tile][piece][half_n rows][sw]: one load for a whole chunk.
 bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int pair,
-                    int n_pieces, int sw) {
+                    int n_pieces, int sw, int nsub) {
     const int piece_n = c_out / n_pieces, half_n = piece_n / pair;
-    cuuint64_t dims[4] = {K, (cuuint64_t)half_n, (cuuint64_t)pair, (cuuint64_t)n_pieces};
-    cuuint64_t strides[3] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)piece_n * K * 2};
-    cuuint32_t box[4] = {(cuuint32_t)sw, (cuuint32_t)half_n, 1, (cuuint32_t)n_pieces};
+    cuuint64_t dims[5] = {K, (cuuint64_t)half_n, (cuuint64_t)pair, (cuuint64_t)n_pieces,
+                          (cuuint64_t)(nsub > 0 ? nsub : 1)};
+    cuuint64_t strides[4] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)piece_n * K * 2,
+                             (cuuint64_t)sw * 2};
+    cuuint32_t box[5] = {(cuuint32_t)sw, (cuuint32_t)half_n, 1, (cuuint32_t)n_pieces,
+                         (cuuint32_t)(nsub > 0 ? nsub : 1)};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, nsub > 0 ? 5 : 4,
+                          const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// NHWC input viewed as (8 channels, W, H, C/8 chunks, frames): the chunk
+// dimension (16 bytes apart) is outside the spatial ones, so one 18 x 10
+// pixel box of `chunk` channels lands as planes [chunk/8][18][10][8 ch], the
+// no-swizzle layout the halo-mode MMAs read.  Pixels outside the frame read
+// as zeros (the conv's spatial pad).
+bool encode_halo(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int chunk) {
+    cuuint64_t dims[5] = {8, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)(C / 8),
+                          (cuuint64_t)frames};
+    cuuint64_t strides[4] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, 16,
+                             (cuuint64_t)H * W * C * 2};
+    cuuint32_t box[5] = {8, kHaloW, kHaloH, (cuuint32_t)(chunk / 8), 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// NHWC tensor as (C, W, H, frames) with a (box_c, 8, 16, 1) box: one 16 x 8
+// patch, swizzled by box_c (its smem rows are the patch's pixels in order).
+bool encode_patch(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int box_c,
+                  int sw) {
+    cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)frames};
+    cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
+    cuuint32_t box[4] = {(cuuint32_t)box_c, 8, 16, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
@@ -896,7 +1293,20 @@ struct Plan {
     int acc_cols, nacc, tmem_cols;
     int staged;
     uint32_t off_stage;
+    int halo;
+    uint32_t off_a, a_stride, a_tx;
 };
+
+// Halo tiles (16 x 8 patches, one halo load per temporal tap and channel
+// chunk feeding all nine spatial taps) move ~6x fewer A bytes and 9x fewer A
+// loads than per-tap im2col, but cover H x W in whole patches: chosen when
+// the patches tile the frame exactly.  WANVAE_CONV_HALO=0/1 forces either.
+int halo_choice(const ConvSpec &s) {
+    if (s.k != 3) return 0;
+    const char *e = getenv("WANVAE_CONV_HALO");
+    if (e && e[0] && e[1] == 0 && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+    return s.H % 16 == 0 && s.W % 8 == 0;
+}
 
 // CTA pairs halve each CTA's share of the B (weight) operand -- half the
 // shared-memory bytes per stage, so a deeper pipeline, and half the L2->SM
@@ -906,8 +1316,9 @@ int pair_choice() {
     return (e && e[0] == '1' && e[1] == 0) ? 1 : 2;
 }
 
-bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
+bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     pl.pair = pair;
+    pl.halo = halo;
     int sw = pick_sw(s.c_in);
     if (s.sc_in) {
         const int sw2 = pick_sw(s.c_sc);
@@ -950,6 +1361,48 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
     const uint32_t reserve =
         fixed + (pl.staged ? stage_tile : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
     const int need_stages = pl.staged ? 3 : min_stages;
+    if (halo) {
+        // Halo ring (2 buffers of 18 x 10 pixels x chunk channels) + a ring of
+        // per-tap weight stages; the largest chunk that leaves >= need_stages
+        // weight stages.
+        pl.nsub = 0;
+        for (int d = 4; d >= 1; --d) {
+            if (d * sw > 128 || g_main % d || g_sc % d) continue;
+            const uint32_t ha = ((uint32_t)(kHaloW * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
+            const uint32_t bs = ((uint32_t)d * b_rows * sw * 2u + 1023u) & ~1023u;
+            if (2u * ha + (uint32_t)need_stages * bs + reserve <= (uint32_t)kSmemBudget) {
+                pl.nsub = d;
+                break;
+            }
+        }
+        if (!pl.nsub) return false;
+        const int d = pl.nsub;
+        pl.kc_main = g_main / d;
+        pl.kc_short = s.sc_in ? g_sc / d : 0;
+        pl.a_sub = (uint32_t)kBlockM * sw * 2;  // one x-patch sub-tile (shortcut)
+        pl.b_sub = b_rows * sw * 2;
+        pl.a_tx = (uint32_t)(kHaloW * kHaloH) * d * sw * 2u;
+        pl.a_stride = (pl.a_tx + 1023u) & ~1023u;
+        pl.off_a = 0;
+        pl.a_bytes = 2u * pl.a_stride;  // the weight ring starts here
+        pl.stage_bytes = (pl.b_sub * d + 1023u) & ~1023u;
+        pl.stages = (int)((kSmemBudget - reserve - pl.a_bytes) / pl.stage_bytes);
+        if (pl.stages > 8) pl.stages = 8;
+        if (pl.stages < 2) return false;
+        uint32_t off = pl.a_bytes + pl.stage_bytes * pl.stages;
+        pl.off_stage = off;
+        if (pl.staged) off += stage_tile;
+        pl.off_bars = off;
+        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
+        pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
+        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
+                        (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
+        if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
+        return pl.smem_bytes <= (uint32_t)kSmemBudget;
+    }
+    pl.off_a = 0;
+    pl.a_stride = 0;
+    pl.a_tx = 0;
     pl.nsub = 1;
     for (int d = 4; d >= 1; --d) {
         if (d * sw > 128 || g_main % d || g_sc % d) continue;
@@ -972,7 +1425,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair) {
     pl.off_stage = off;
     if (pl.staged) off += stage_tile;
     pl.off_bars = off;
-    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 6);
+    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
     pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
                     (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
@@ -1061,12 +1514,18 @@ int conv3d_supported(const ConvSpec &s) {
     if (s.c_in > 4096) return -1;
     if (s.sc_in && (s.c_sc < 16 || s.c_sc % 16 || s.c_sc > 4096)) return -1;
     Plan pl;
-    return (make_plan(s, pl, 2) || make_plan(s, pl, 1)) ? 0 : -1;
+    return (make_plan(s, pl, 2, halo_choice(s)) || make_plan(s, pl, 1, halo_choice(s)) ||
+            make_plan(s, pl, 1, 0))
+               ? 0
+               : -1;
 }
 
 cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     Plan pl;
-    if (!make_plan(s, pl, pair_choice()) && !make_plan(s, pl, 1)) return cudaErrorInvalidValue;
+    const int hc = halo_choice(s);
+    if (!make_plan(s, pl, pair_choice(), hc) && !make_plan(s, pl, 1, hc) &&
+        !make_plan(s, pl, 1, 0))
+        return cudaErrorInvalidValue;
     if (!load_encoders()) return cudaErrorInvalidValue;
     ConvKernelFn fn = pl.pair == 2 ? pick_kernel<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
                                    : pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
@@ -1074,7 +1533,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     cudaError_t fe = kernel_facts(fn, pl.pair == 2, max_pairs);
     if (fe != cudaSuccess) return fe;
     if (pl.pair == 2 && max_pairs < 1) {
-        if (!make_plan(s, pl, 1)) return cudaErrorInvalidValue;
+        if (!make_plan(s, pl, 1, pl.halo) && !make_plan(s, pl, 1, 0)) return cudaErrorInvalidValue;
         fn = pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
         fe = kernel_facts(fn, false, max_pairs);
         if (fe != cudaSuccess) return fe;
@@ -1090,22 +1549,36 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     memset(&mSA, 0, sizeof(mSA));
     memset(&mSB, 0, sizeof(mSB));
     bool ok = true;
-    if (s.k == 3) {
+    if (pl.halo) {
+        const int chunk = pl.nsub * pl.sw;
+        ok = ok && encode_halo(&mA, s.in, s.c_in, s.W, s.H, frames, chunk);
+        if (s.cache) ok = ok && encode_halo(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, chunk);
+    } else if (s.k == 3) {
         ok = ok && encode_im2col(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw);
         if (s.cache) ok = ok && encode_im2col(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, pl.sw);
     } else {
         ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
     }
     ok = ok && encode_weights(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, s.c_out, pl.pair,
-                              pl.n_pieces, pl.sw);
+                              pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0);
     if (s.sc_in) {
-        ok = ok && encode_2d(&mSA, s.sc_in, (uint64_t)s.c_sc, (uint64_t)M, pl.sw, kBlockM, pl.sw);
+        if (pl.halo)
+            ok = ok && encode_patch(&mSA, s.sc_in, s.c_sc, s.W, s.H, frames, pl.sw, pl.sw);
+        else
+            ok = ok && encode_2d(&mSA, s.sc_in, (uint64_t)s.c_sc, (uint64_t)M, pl.sw, kBlockM,
+                                 pl.sw);
         ok = ok && encode_weights(&mSB, s.sc_w, (uint64_t)s.c_sc, s.c_out, pl.pair, pl.n_pieces,
-                                  pl.sw);
+                                  pl.sw, pl.halo ? pl.nsub : 0);
     }
     if (pl.staged) {
-        ok = ok && encode_frames(&mY, s.out, s.c_out, HW, frames);
-        if (s.epi == kEpiResidual) ok = ok && encode_frames(&mR, s.resid, s.c_out, HW, frames);
+        if (pl.halo) {
+            ok = ok && encode_patch(&mY, s.out, s.c_out, s.W, s.H, frames, 64, 64);
+            if (s.epi == kEpiResidual)
+                ok = ok && encode_patch(&mR, s.resid, s.c_out, s.W, s.H, frames, 64, 64);
+        } else {
+            ok = ok && encode_frames(&mY, s.out, s.c_out, HW, frames);
+            if (s.epi == kEpiResidual) ok = ok && encode_frames(&mR, s.resid, s.c_out, HW, frames);
+        }
     }
     if (!ok) return cudaErrorInvalidValue;
 
@@ -1126,14 +1599,19 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.n_pieces = pl.n_pieces;
     a.piece_n = pl.piece_n;
     a.layout = pl.sw == 64 ? kLayoutSw128 : (pl.sw == 32 ? kLayoutSw64 : kLayoutSw32);
-    a.tiles_per_frame = (HW + kBlockM - 1) / kBlockM;
+    a.halo = pl.halo;
+    a.patches_w = (s.W + 7) / 8;
+    a.off_a = pl.off_a;
+    a.a_stride = pl.a_stride;
+    a.a_tx = pl.a_tx;
+    a.tiles_per_frame = pl.halo ? ((s.H + 15) / 16) * a.patches_w : (HW + kBlockM - 1) / kBlockM;
     a.num_tiles = a.tiles_per_frame * frames;
     a.stages = pl.stages;
     a.a_sub_bytes = pl.a_sub;
     a.b_sub_bytes = pl.b_sub;
     a.a_bytes = pl.a_bytes;
     a.stage_bytes = pl.stage_bytes;
-    a.stage_tx = (pl.a_sub + pl.b_sub) * pl.nsub;
+    a.stage_tx = pl.halo ? pl.b_sub * pl.nsub : (pl.a_sub + pl.b_sub) * pl.nsub;
     a.off_bars = pl.off_bars;
     a.off_misc = pl.off_misc;
     a.off_vec = pl.off_vec;
