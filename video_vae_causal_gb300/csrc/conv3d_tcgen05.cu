@@ -72,6 +72,7 @@ struct ConvArgs {
     uint32_t off_stage;  // 1024-aligned offset of that buffer
     int halo;            // 16x8 patch tiles, one halo load per (kt, chunk) for 9 taps
     int patches_w;       // patches per frame row (halo mode)
+    int tb;              // spatial taps per weight stage (halo mode: 1, 3)
     uint32_t off_a, a_stride, a_tx;  // halo ring: 2 buffers, bytes per CTA per load
     int epi;
     float eps, sqrt_c;
@@ -162,8 +163,41 @@ struct Bars {
     __device__ uint32_t acce(int a) const { return base + 8u * (2 * stages + 2 + a); }
     __device__ uint32_t drain() const { return base + 8u * (2 * stages + 4); }
     __device__ uint32_t resf() const { return base + 8u * (2 * stages + 5); }
-    __device__ uint32_t fulla(int i) const { return base + 8u * (2 * stages + 6 + i); }
-    __device__ uint32_t emptya(int i) const { return base + 8u * (2 * stages + 8 + i); }
+    __device__ uint32_t emptya(int i) const { return base + 8u * (2 * stages + 6 + i); }
+};
+
+// The MMA issuer's view of the `full` ring.  A barrier access by the issuing
+// thread is slow while the tensor core streams its operands out of shared
+// memory (the access queues behind them), and the MMAs already queued run dry
+// meanwhile.  So each stage costs one access: the next stage's barrier is
+// tested, without blocking, before the current stage's MMAs are issued, and a
+// stage found complete that way is used without waiting again.
+template <bool kCluster>
+struct FullRing {
+    int stage = 0;
+    uint32_t phase = 0;
+    bool next_ready = false;
+    // Bounded wait for the current stage (free if the look-ahead saw it complete).
+    __device__ __forceinline__ bool acquire(const Bars &bars, const WaitCtl &wc) {
+        if (next_ready) return true;
+        return mbar_wait<kCluster>(bars.full(stage), phase, wc);
+    }
+    // Look ahead at the stage after the current one.
+    __device__ __forceinline__ void test_next(const Bars &bars) {
+        int ns = stage + 1;
+        uint32_t np = phase;
+        if (ns == bars.stages) {
+            ns = 0;
+            np ^= 1u;
+        }
+        next_ready = mbar_test_t<kCluster>(bars.full(ns), np);
+    }
+    __device__ __forceinline__ void advance(const Bars &bars) {
+        if (++stage == bars.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
 };
 
 // TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
@@ -303,9 +337,11 @@ __device__ __forceinline__ void load4(uint32_t dst, const CUtensorMap *m, uint32
         tma_load_4d(dst, m, bar, c0, c1, c2, c3);
 }
 
-// Halo-mode producer.  Per unit: for each temporal tap kt and channel chunk
-// one halo load (A ring, 2 buffers), then nine weight loads (B ring), one per
-// spatial tap; then the shortcut segment's chunks (x patch into the A ring).
+// Halo-mode producer.  Per unit, for each temporal tap kt and channel chunk:
+// one halo load into the A ring (2 buffers) and 9 / tb weight stages of tb
+// spatial taps each (B ring); the halo completes on the barrier of the first
+// of those stages, so the MMA issuer waits once per stage.  Then the shortcut
+// segment's chunks (x patch into the A ring + its weights, one stage each).
 template <int kPair>
 __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *mapC,
                                    const CUtensorMap *mapB, const CUtensorMap *mapSA,
@@ -313,14 +349,17 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                                    const Bars &bars, const WaitCtl &wc, int unit0,
                                    int unit_stride, int num_units, uint32_t rank) {
     const int frames = p.num_tiles / p.tiles_per_frame;
-    const int chunk = p.nsub * p.sw;  // channels per halo / per weight stage
+    const int chunk = p.nsub * p.sw;  // channels per halo / per weight sub-stage
+    const int groups = 9 / p.tb;
     int stage = 0, ia = 0;
-    uint32_t phase = 0, pha = 0, fills = 0, fills_a = 0;
+    uint32_t phase = 0, pha = 0, fills = 0;
     bool ok = true;
-    auto next_b = [&](uint32_t &dst, uint32_t &fb) -> bool {
+    // Next B stage, armed for `tx` bytes per CTA (both CTAs' loads complete
+    // on the leader's barrier).
+    auto next_stage = [&](uint32_t tx, uint32_t &dst, uint32_t &fb) -> bool {
         if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) return false;
         const uint32_t fl = bars.full(stage);
-        if (rank == 0) mbar_arrive_expect_tx(fl, p.stage_tx * kPair);
+        if (rank == 0) mbar_arrive_expect_tx(fl, tx * kPair);
         fb = kPair == 2 ? mapa_shared(fl, 0) : fl;
         dst = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
         ++fills;
@@ -330,13 +369,9 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         }
         return true;
     };
-    auto next_a = [&](uint32_t &dst, uint32_t &fb, uint32_t tx) -> bool {
+    auto next_abuf = [&](uint32_t &dst) -> bool {
         if (!mbar_wait<kPair == 2>(bars.emptya(ia), pha ^ 1u, wc)) return false;
-        const uint32_t fl = bars.fulla(ia);
-        if (rank == 0) mbar_arrive_expect_tx(fl, tx * kPair);
-        fb = kPair == 2 ? mapa_shared(fl, 0) : fl;
         dst = sbase + p.off_a + (uint32_t)ia * p.a_stride;
-        ++fills_a;
         if (++ia == 2) {
             ia = 0;
             pha ^= 1u;
@@ -359,49 +394,47 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                 }
             }
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
-                uint32_t da, fa;
-                if (!next_a(da, fa, p.a_tx)) {
+                uint32_t da;
+                if (!next_abuf(da)) {
                     ok = false;
                     break;
                 }
-                load5<kPair>(da, am, fa, 0, ti.w0 - 1, ti.h0 - 1, cc * (chunk / 8), fidx);
-                for (int t9 = 0; t9 < 9; ++t9) {
+                for (int g = 0; g < groups; ++g) {
                     uint32_t db, fb;
-                    if (!next_b(db, fb)) {
+                    if (!next_stage(p.stage_tx + (g == 0 ? p.a_tx : 0u), db, fb)) {
                         ok = false;
                         break;
                     }
-                    const int tap = kt * 9 + t9;
+                    if (g == 0)
+                        load5<kPair>(da, am, fb, 0, ti.w0 - 1, ti.h0 - 1, cc * (chunk / 8), fidx);
+                    // tb consecutive spatial taps of this chunk in one box
+                    const int tap = kt * 9 + g * p.tb;
                     load5<kPair>(db, mapB, fb, tap * p.c_in + cc * chunk, 0, (int)rank, 0, 0);
                 }
             }
         }
         // shortcut segment: the patch's own pixels of x (no shift)
+        const uint32_t sub_a = (uint32_t)kBlockM * p.sw * 2u;
         for (int cc = 0; ok && cc < p.kc_short; ++cc) {
-            uint32_t da, fa, db, fb;
-            if (!next_a(da, fa, (uint32_t)p.nsub * kBlockM * p.sw * 2u)) {
+            uint32_t da, db, fb;
+            if (!next_abuf(da) || !next_stage(p.nsub * (sub_a + p.b_sub_bytes), db, fb)) {
                 ok = false;
                 break;
             }
             for (int s = 0; s < p.nsub; ++s)
-                load4<kPair>(da + (uint32_t)s * kBlockM * p.sw * 2u, mapSA, fa,
-                             (cc * p.nsub + s) * p.sw, ti.w0, ti.h0, ti.dummy ? frames : ti.frame);
-            if (!next_b(db, fb)) {
-                ok = false;
-                break;
-            }
+                load4<kPair>(da + (uint32_t)s * sub_a, mapSA, fb, (cc * p.nsub + s) * p.sw, ti.w0,
+                             ti.h0, ti.dummy ? frames : ti.frame);
             load5<kPair>(db, mapSB, fb, cc * chunk, 0, (int)rank, 0, 0);
         }
     }
     if (!ok && rank == 0) {
+        // Aborted: let the newest fill of every stage (halo loads included)
+        // land before the CTA and its shared memory go away.
         volatile int no_abort = 0;
         const WaitCtl dc{kDrainNs, wc.err, &no_abort};
-        uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
+        const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
         for (uint32_t f = fills - n; f < fills; ++f)
             mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
-        n = fills_a < 2u ? fills_a : 2u;
-        for (uint32_t f = fills_a - n; f < fills_a; ++f)
-            mbar_wait<kPair == 2>(bars.fulla((int)(f % 2)), (f / 2) & 1u, dc);
     }
 }
 
@@ -485,14 +518,19 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
     }
 }
 
+// Halo-mode MMA issuer: per (kt, chunk), 9 / tb weight stages of tb spatial
+// taps, each tap reading the halo through a window shifted by (kh, kw); the
+// halo buffer is released after the ninth tap.
 template <int kPair, int KK, int NSUB, int NP>
 __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base,
                               const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
                               int num_units) {
     const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
     const uint32_t row_bytes = (uint32_t)p.sw * 2u;
-    int stage = 0, ia = 0, it = 0;
-    uint32_t phase = 0, pha = 0;
+    const uint32_t tap_b16 = (uint32_t)p.nsub * (p.b_sub_bytes >> 4);  // one tap's weights
+    const bool tb3 = p.tb == 3;
+    FullRing<kPair == 2> ring;
+    int ia = 0, it = 0;
     bool ok = true;
     auto commit = [&](uint32_t bar) {
         if (kPair == 2)
@@ -510,63 +548,60 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
-                if (!mbar_wait<kPair == 2>(bars.fulla(ia), pha, wc)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t abuf = sbase + p.off_a + (uint32_t)ia * p.a_stride;
+                // The nine taps are unrolled so that every A descriptor is the
+                // halo's base plus a constant and nothing but the stage
+                // bookkeeping sits between two taps' MMAs.
+                const uint64_t abase =
+                    sdesc_plain(sbase + p.off_a + (uint32_t)ia * p.a_stride, kPlaneBytes,
+                                kHaloW * 16u);
+                uint64_t b0 = 0;
+#pragma unroll
                 for (int t9 = 0; t9 < 9; ++t9) {
-                    if (!mbar_wait<kPair == 2>(bars.full(stage), phase, wc)) {
-                        ok = false;
-                        break;
+                    const int j = tb3 ? t9 % 3 : 0;  // tap within its weight stage
+                    if (j == 0) {
+                        // the first stage of (kt, cc) also carries the halo
+                        if (!ring.acquire(bars, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        ring.test_next(bars);
+                        b0 = sdesc_kmajor(sbase + p.a_bytes + (uint32_t)ring.stage * p.stage_bytes,
+                                          row_bytes, p.layout);
                     }
-                    tc_fence_after();
-                    const int kh = t9 / 3, kw = t9 - 3 * (t9 / 3);
-                    const uint64_t a0 = sdesc_plain(abuf + (uint32_t)(kh * kHaloW + kw) * 16u,
-                                                    kPlaneBytes, kHaloW * 16u);
-                    const uint32_t sb = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
-                    issue_tap_halo<kPair, KK, NSUB, NP>(p, dacc, a0,
-                                                        sdesc_kmajor(sb, row_bytes, p.layout),
-                                                        idesc, first);
+                    const uint32_t shift16 = (uint32_t)((t9 / 3) * kHaloW + t9 % 3);
+                    issue_tap_halo<kPair, KK, NSUB, NP>(p, dacc, abase + shift16,
+                                                        b0 + (uint64_t)(j * tap_b16), idesc,
+                                                        first);
                     first = false;
-                    commit(bars.empty(stage));
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (!tb3 || j == 2) {
+                        commit(bars.empty(ring.stage));
+                        ring.advance(bars);
                     }
                 }
                 if (!ok) break;
                 commit(bars.emptya(ia));
-                if (++ia == 2) {
-                    ia = 0;
-                    pha ^= 1u;
-                }
+                if (++ia == 2) ia = 0;
             }
         }
         for (int cc = 0; ok && cc < p.kc_short; ++cc) {
-            if (!mbar_wait<kPair == 2>(bars.fulla(ia), pha, wc) ||
-                !mbar_wait<kPair == 2>(bars.full(stage), phase, wc)) {
+            if (!ring.acquire(bars, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            ring.test_next(bars);
             // x patch in the A buffer, swizzled like the weights: the stage
             // issue routine of the im2col path applies unchanged.
             const uint32_t abuf = sbase + p.off_a + (uint32_t)ia * p.a_stride;
-            const uint32_t sb = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
+            const uint32_t sb = sbase + p.a_bytes + (uint32_t)ring.stage * p.stage_bytes;
             issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(abuf, row_bytes, p.layout),
                                              sdesc_kmajor(sb, row_bytes, p.layout), idesc, first);
             first = false;
-            commit(bars.empty(stage));
+            commit(bars.empty(ring.stage));
             commit(bars.emptya(ia));
-            if (++stage == p.stages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (++ia == 2) {
-                ia = 0;
-                pha ^= 1u;
-            }
+            ring.advance(bars);
+            if (++ia == 2) ia = 0;
         }
         if (!ok) break;
         commit(bars.accf(a));
@@ -586,8 +621,8 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
                          const WaitCtl &wc, int unit0, int unit_stride, int num_units) {
     const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
     const uint32_t row_bytes = (uint32_t)p.sw * 2u;
-    int stage = 0, it = 0;
-    uint32_t phase = 0;
+    FullRing<kPair == 2> ring;
+    int it = 0;
     bool ok = true;
     for (int u = unit0; ok && u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
@@ -597,24 +632,22 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
         const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_cols);
         const int nst = unit_stages<kPair>(u, p);
         for (int k = 0; k < nst; ++k) {
-            if (!mbar_wait<kPair == 2>(bars.full(stage), phase, wc)) {
+            if (!ring.acquire(bars, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
+            ring.test_next(bars);
+            const uint32_t sa = sbase + (uint32_t)ring.stage * p.stage_bytes;
             issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(sa, row_bytes, p.layout),
                                              sdesc_kmajor(sa + p.a_bytes, row_bytes, p.layout),
                                              idesc, k == 0);
             // Frees the smem stage (in both CTAs of a pair) when these MMAs finish.
             if (kPair == 2)
-                mma_commit_pair_mc(bars.empty(stage), (uint16_t)0x3);
+                mma_commit_pair_mc(bars.empty(ring.stage), (uint16_t)0x3);
             else
-                mma_commit(bars.empty(stage));
-            if (++stage == p.stages) {
-                stage = 0;
-                phase ^= 1u;
-            }
+                mma_commit(bars.empty(ring.stage));
+            ring.advance(bars);
         }
         if (!ok) break;
         // Accumulator ready for the epilogue (of both CTAs of a pair).
@@ -1062,10 +1095,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         mbar_init(bars.drain(), 1);
         mbar_init(bars.resf(), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bars.fulla(i), 1);
-            mbar_init(bars.emptya(i), 1);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(bars.emptya(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1251,6 +1281,26 @@ bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weights [c_out][27 * c_in] of one N piece (n_pieces == 1) viewed as
+// (K, half_n rows, pair rank, nsub sub-tiles sw apart, tb taps c_in apart): one
+// box holds this CTA's rows of tb consecutive taps of one channel chunk, laid
+// out [tap][sub-tile][row][sw], the order the halo-mode MMAs step through.
+bool encode_weight_taps(CUtensorMap *m, const void *base, uint64_t K, int c_in, int c_out,
+                        int pair, int sw, int nsub, int tb) {
+    const int half_n = c_out / pair;
+    cuuint64_t dims[5] = {K, (cuuint64_t)half_n, (cuuint64_t)pair, (cuuint64_t)nsub,
+                          (cuuint64_t)tb};
+    cuuint64_t strides[4] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)sw * 2,
+                             (cuuint64_t)c_in * 2};
+    cuuint32_t box[5] = {(cuuint32_t)sw, (cuuint32_t)half_n, 1, (cuuint32_t)nsub,
+                         (cuuint32_t)tb};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // NHWC input viewed as (8 channels, W, H, C/8 chunks, frames): the chunk
 // dimension (16 bytes apart) is outside the spatial ones, so one 18 x 10
 // pixel box of `chunk` channels lands as planes [chunk/8][18][10][8 ch], the
@@ -1294,6 +1344,7 @@ struct Plan {
     int staged;
     uint32_t off_stage;
     int halo;
+    int tb;  // spatial taps per weight stage (halo mode)
     uint32_t off_a, a_stride, a_tx;
 };
 
@@ -1363,16 +1414,31 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     const int need_stages = pl.staged ? 3 : min_stages;
     if (halo) {
         // Halo ring (2 buffers of 18 x 10 pixels x chunk channels) + a ring of
-        // per-tap weight stages; the largest chunk that leaves >= need_stages
-        // weight stages.
+        // weight stages of tb spatial taps each.  Every stage costs the MMA
+        // issuer one barrier access, so take the (chunk, tb) with the fewest
+        // stages per tile among those that leave a deep enough ring (>= 3
+        // stages of 3 taps, >= need_stages of one tap); 3-tap stages need the
+        // weights of one CTA in one piece (n_pieces == 1).
         pl.nsub = 0;
+        pl.tb = 1;
+        int best_waits = 0, best_stages = 0;
         for (int d = 4; d >= 1; --d) {
             if (d * sw > 128 || g_main % d || g_sc % d) continue;
             const uint32_t ha = ((uint32_t)(kHaloW * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
-            const uint32_t bs = ((uint32_t)d * b_rows * sw * 2u + 1023u) & ~1023u;
-            if (2u * ha + (uint32_t)need_stages * bs + reserve <= (uint32_t)kSmemBudget) {
-                pl.nsub = d;
-                break;
+            for (int tb = 3; tb >= 1; tb -= 2) {
+                if (tb > 1 && pl.n_pieces != 1) continue;
+                const uint32_t bs = ((uint32_t)(tb * d) * b_rows * sw * 2u + 1023u) & ~1023u;
+                if (2u * ha + reserve >= (uint32_t)kSmemBudget) continue;
+                int st = (int)(((uint32_t)kSmemBudget - reserve - 2u * ha) / bs);
+                if (st > 8) st = 8;
+                if (st < (tb > 1 ? 3 : need_stages)) continue;
+                const int waits = 27 * (g_main / d) / tb + (s.sc_in ? g_sc / d : 0);
+                if (!pl.nsub || waits < best_waits || (waits == best_waits && st > best_stages)) {
+                    pl.nsub = d;
+                    pl.tb = tb;
+                    best_waits = waits;
+                    best_stages = st;
+                }
             }
         }
         if (!pl.nsub) return false;
@@ -1385,7 +1451,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
         pl.a_stride = (pl.a_tx + 1023u) & ~1023u;
         pl.off_a = 0;
         pl.a_bytes = 2u * pl.a_stride;  // the weight ring starts here
-        pl.stage_bytes = (pl.b_sub * d + 1023u) & ~1023u;
+        pl.stage_bytes = (pl.b_sub * d * (uint32_t)pl.tb + 1023u) & ~1023u;
         pl.stages = (int)((kSmemBudget - reserve - pl.a_bytes) / pl.stage_bytes);
         if (pl.stages > 8) pl.stages = 8;
         if (pl.stages < 2) return false;
@@ -1393,7 +1459,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
         pl.off_stage = off;
         if (pl.staged) off += stage_tile;
         pl.off_bars = off;
-        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
+        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 8);
         pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
         pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
                         (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
@@ -1403,6 +1469,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     pl.off_a = 0;
     pl.a_stride = 0;
     pl.a_tx = 0;
+    pl.tb = 1;
     pl.nsub = 1;
     for (int d = 4; d >= 1; --d) {
         if (d * sw > 128 || g_main % d || g_sc % d) continue;
@@ -1425,7 +1492,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     pl.off_stage = off;
     if (pl.staged) off += stage_tile;
     pl.off_bars = off;
-    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
+    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 8);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
     pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
                     (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
@@ -1559,8 +1626,12 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     } else {
         ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
     }
-    ok = ok && encode_weights(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, s.c_out, pl.pair,
-                              pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0);
+    if (pl.halo && pl.tb > 1)
+        ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)27 * s.c_in, s.c_in, s.c_out, pl.pair,
+                                      pl.sw, pl.nsub, pl.tb);
+    else
+        ok = ok && encode_weights(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, s.c_out, pl.pair,
+                                  pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0);
     if (s.sc_in) {
         if (pl.halo)
             ok = ok && encode_patch(&mSA, s.sc_in, s.c_sc, s.W, s.H, frames, pl.sw, pl.sw);
@@ -1601,6 +1672,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.layout = pl.sw == 64 ? kLayoutSw128 : (pl.sw == 32 ? kLayoutSw64 : kLayoutSw32);
     a.halo = pl.halo;
     a.patches_w = (s.W + 7) / 8;
+    a.tb = pl.tb;
     a.off_a = pl.off_a;
     a.a_stride = pl.a_stride;
     a.a_tx = pl.a_tx;
@@ -1611,7 +1683,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.b_sub_bytes = pl.b_sub;
     a.a_bytes = pl.a_bytes;
     a.stage_bytes = pl.stage_bytes;
-    a.stage_tx = pl.halo ? pl.b_sub * pl.nsub : (pl.a_sub + pl.b_sub) * pl.nsub;
+    a.stage_tx = pl.halo ? pl.b_sub * pl.nsub * (uint32_t)pl.tb : (pl.a_sub + pl.b_sub) * pl.nsub;
     a.off_bars = pl.off_bars;
     a.off_misc = pl.off_misc;
     a.off_vec = pl.off_vec;
