@@ -166,31 +166,17 @@ struct Bars {
     __device__ uint32_t emptya(int i) const { return base + 8u * (2 * stages + 6 + i); }
 };
 
-// The MMA issuer's view of the `full` ring.  A barrier access by the issuing
-// thread is slow while the tensor core streams its operands out of shared
-// memory (the access queues behind them), and the MMAs already queued run dry
-// meanwhile.  So each stage costs one access: the next stage's barrier is
-// tested, without blocking, before the current stage's MMAs are issued, and a
-// stage found complete that way is used without waiting again.
+// The MMA issuer's view of the `full` ring.  Every barrier access by the
+// issuing thread is slow while the tensor core streams its operands out of
+// shared memory (the access queues behind them) and the few MMAs already
+// queued run dry meanwhile, so the issuers wait once per stage and make the
+// stages as large as shared memory allows.
 template <bool kCluster>
 struct FullRing {
     int stage = 0;
     uint32_t phase = 0;
-    bool next_ready = false;
-    // Bounded wait for the current stage (free if the look-ahead saw it complete).
     __device__ __forceinline__ bool acquire(const Bars &bars, const WaitCtl &wc) {
-        if (next_ready) return true;
         return mbar_wait<kCluster>(bars.full(stage), phase, wc);
-    }
-    // Look ahead at the stage after the current one.
-    __device__ __forceinline__ void test_next(const Bars &bars) {
-        int ns = stage + 1;
-        uint32_t np = phase;
-        if (ns == bars.stages) {
-            ns = 0;
-            np ^= 1u;
-        }
-        next_ready = mbar_test_t<kCluster>(bars.full(ns), np);
     }
     __device__ __forceinline__ void advance(const Bars &bars) {
         if (++stage == bars.stages) {
@@ -439,35 +425,36 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
 }
 
 // Halo-mode MMAs of one spatial tap: k-step ks uses A planes 2ks, 2ks+1 of
-// the halo window and B sub-tile ks / KK at k-offset ks % KK.
+// the halo window and B sub-tile ks / KK at k-offset ks % KK (sub-tiles
+// b_sub16 descriptor units apart).
 template <int kPair, int KK, int NSUB, int NP>
 __device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc, uint64_t a0,
-                                               uint64_t b0, uint32_t idesc, bool first) {
-    const uint32_t b_sub16 = p.b_sub_bytes >> 4;
+                                               uint64_t b0, uint32_t b_sub16, uint32_t idesc,
+                                               bool first) {
     const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
     constexpr uint32_t kPlane2 = (2 * kPlaneBytes) >> 4;
-    const int kk_n = KK > 0 ? KK : p.sw / 16, ns_n = KK > 0 ? NSUB : p.nsub;
-    const int np_n = KK > 0 ? NP : p.n_pieces;
+    auto mma = [&](int s, int kk, int ks, int j) {
+        const uint64_t ad = a0 + (uint64_t)(ks * kPlane2);
+        const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
+        const uint32_t accum = (first && ks == 0) ? 0u : 1u;
+        const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
+        if (kPair == 2)
+            mma_bf16_ss_pair(d, ad, bd, idesc, accum);
+        else
+            mma_bf16_ss(d, ad, bd, idesc, accum);
+    };
+    if (KK > 0) {
 #pragma unroll
-    for (int s = 0; s < (KK > 0 ? NSUB : 8); ++s) {
-        if (KK == 0 && s >= ns_n) break;
+        for (int s = 0; s < NSUB; ++s)
 #pragma unroll
-        for (int kk = 0; kk < (KK > 0 ? KK : 4); ++kk) {
-            if (KK == 0 && kk >= kk_n) break;
-            const int ks = s * kk_n + kk;
-            const uint64_t ad = a0 + (uint64_t)(ks * kPlane2);
-            const uint32_t accum = (first && ks == 0) ? 0u : 1u;
+            for (int kk = 0; kk < KK; ++kk)
 #pragma unroll
-            for (int j = 0; j < (KK > 0 ? NP : 32); ++j) {
-                if (KK == 0 && j >= np_n) break;
-                const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
-                const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
-                if (kPair == 2)
-                    mma_bf16_ss_pair(d, ad, bd, idesc, accum);
-                else
-                    mma_bf16_ss(d, ad, bd, idesc, accum);
-            }
-        }
+                for (int j = 0; j < NP; ++j) mma(s, kk, s * KK + kk, j);
+    } else {
+        const int kk_n = p.sw / 16;
+        for (int s = 0; s < p.nsub; ++s)
+            for (int kk = 0; kk < kk_n; ++kk)
+                for (int j = 0; j < p.n_pieces; ++j) mma(s, kk, s * kk_n + kk, j);
     }
 }
 
@@ -520,14 +507,20 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
 
 // Halo-mode MMA issuer: per (kt, chunk), 9 / tb weight stages of tb spatial
 // taps, each tap reading the halo through a window shifted by (kh, kw); the
-// halo buffer is released after the ninth tap.
+// halo buffer is released after the ninth tap.  Descriptors are the ring
+// bases plus offsets, so nothing but the stage bookkeeping sits between two
+// stages' MMAs.
 template <int kPair, int KK, int NSUB, int NP>
 __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base,
                               const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
                               int num_units) {
     const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
     const uint32_t row_bytes = (uint32_t)p.sw * 2u;
-    const uint32_t tap_b16 = (uint32_t)p.nsub * (p.b_sub_bytes >> 4);  // one tap's weights
+    const uint32_t b_sub16 = p.b_sub_bytes >> 4;
+    const uint32_t tap_b16 = (uint32_t)p.nsub * b_sub16;  // one tap's weights
+    const uint32_t stage16 = p.stage_bytes >> 4, astride16 = p.a_stride >> 4;
+    const uint64_t bdesc0 = sdesc_kmajor(sbase + p.a_bytes, row_bytes, p.layout);
+    const uint64_t adesc0 = sdesc_plain(sbase + p.off_a, kPlaneBytes, kHaloW * 16u);
     const bool tb3 = p.tb == 3;
     FullRing<kPair == 2> ring;
     int ia = 0, it = 0;
@@ -548,40 +541,45 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
-                // The nine taps are unrolled so that every A descriptor is the
-                // halo's base plus a constant and nothing but the stage
-                // bookkeeping sits between two taps' MMAs.
-                const uint64_t abase =
-                    sdesc_plain(sbase + p.off_a + (uint32_t)ia * p.a_stride, kPlaneBytes,
-                                kHaloW * 16u);
-                uint64_t b0 = 0;
-#pragma unroll
-                for (int t9 = 0; t9 < 9; ++t9) {
-                    const int j = tb3 ? t9 % 3 : 0;  // tap within its weight stage
-                    if (j == 0) {
-                        // the first stage of (kt, cc) also carries the halo
+                const uint64_t abase = adesc0 + (uint64_t)(ia * astride16);
+                if (tb3) {
+                    // the first stage of (kt, cc) also carries the halo
+                    for (int kh = 0; kh < 3; ++kh) {
                         if (!ring.acquire(bars, wc)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        ring.test_next(bars);
-                        b0 = sdesc_kmajor(sbase + p.a_bytes + (uint32_t)ring.stage * p.stage_bytes,
-                                          row_bytes, p.layout);
+                        const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16);
+                        const uint64_t ah = abase + (uint64_t)(kh * kHaloW);
+#pragma unroll
+                        for (int kw = 0; kw < 3; ++kw)
+                            issue_tap_halo<kPair, KK, NSUB, NP>(p, dacc, ah + kw,
+                                                                b0 + (uint64_t)(kw * tap_b16),
+                                                                b_sub16, idesc, first && kw == 0);
+                        first = false;
+                        commit(bars.empty(ring.stage));
+                        ring.advance(bars);
                     }
-                    const uint32_t shift16 = (uint32_t)((t9 / 3) * kHaloW + t9 % 3);
-                    issue_tap_halo<kPair, KK, NSUB, NP>(p, dacc, abase + shift16,
-                                                        b0 + (uint64_t)(j * tap_b16), idesc,
-                                                        first);
-                    first = false;
-                    if (!tb3 || j == 2) {
+                } else {
+                    for (int t9 = 0; t9 < 9; ++t9) {
+                        if (!ring.acquire(bars, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int kh = t9 / 3, kw = t9 - 3 * kh;
+                        issue_tap_halo<kPair, KK, NSUB, NP>(
+                            p, dacc, abase + (uint64_t)(kh * kHaloW + kw),
+                            bdesc0 + (uint64_t)(ring.stage * stage16), b_sub16, idesc, first);
+                        first = false;
                         commit(bars.empty(ring.stage));
                         ring.advance(bars);
                     }
                 }
                 if (!ok) break;
                 commit(bars.emptya(ia));
-                if (++ia == 2) ia = 0;
+                ia ^= 1;
             }
         }
         for (int cc = 0; ok && cc < p.kc_short; ++cc) {
@@ -590,7 +588,6 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
                 break;
             }
             tc_fence_after();
-            ring.test_next(bars);
             // x patch in the A buffer, swizzled like the weights: the stage
             // issue routine of the im2col path applies unchanged.
             const uint32_t abuf = sbase + p.off_a + (uint32_t)ia * p.a_stride;
@@ -601,7 +598,7 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
             commit(bars.empty(ring.stage));
             commit(bars.emptya(ia));
             ring.advance(bars);
-            if (++ia == 2) ia = 0;
+            ia ^= 1;
         }
         if (!ok) break;
         commit(bars.accf(a));
@@ -637,7 +634,6 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
                 break;
             }
             tc_fence_after();
-            ring.test_next(bars);
             const uint32_t sa = sbase + (uint32_t)ring.stage * p.stage_bytes;
             issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(sa, row_bytes, p.layout),
                                              sdesc_kmajor(sa + p.a_bytes, row_bytes, p.layout),

@@ -108,31 +108,6 @@ __device__ __forceinline__ bool mbar_try_wait_t(uint32_t bar, uint32_t parity) {
     return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
 }
 
-// Non-blocking test of the phase of `parity` (acquire at CTA or cluster
-// scope).  Unlike try_wait it never suspends the thread, so it can look ahead
-// at a barrier that may not have completed yet.
-template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_test_t(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    if (kCluster)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.b32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.b32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    return ok != 0;
-}
-
 // Single-thread bounded wait for the phase of `parity` to complete.  Gives up
 // when another thread of the CTA raised the abort flag, or after limit_ns;
 // in the latter case it raises the abort flag and the device error bit.
