@@ -14,17 +14,21 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["pair-im2col", "pair-halo", "single-im2col", "single-halo"])
+@pytest.fixture(params=["pair-im2col", "pair-halo", "pair-wide", "single-im2col", "single-halo",
+                        "single-wide"])
 def variant(request, monkeypatch):
     """Run a conv test on every kernel variant: CTA pair or single CTA, and
-    per-tap im2col A loads or halo tiles (16 x 8 patches, one halo load per
-    temporal tap feeding the nine spatial taps)."""
+    per-tap im2col A loads, halo tiles (16 x 8 patches, one halo load per
+    temporal tap feeding the nine spatial taps) or wide halo tiles (16 x 16
+    patches, two accumulators per CTA; layers with c_out <= 128 and no
+    shortcut, others fall back to 16 x 8)."""
     pair, mode = request.param.split("-")
     if pair == "single":
         monkeypatch.setenv("WANVAE_CONV_PAIR", "1")
     else:
         monkeypatch.delenv("WANVAE_CONV_PAIR", raising=False)
-    monkeypatch.setenv("WANVAE_CONV_HALO", "1" if mode == "halo" else "0")
+    monkeypatch.setenv("WANVAE_CONV_HALO", "0" if mode == "im2col" else "1")
+    monkeypatch.setenv("WANVAE_CONV_WIDE", "1" if mode == "wide" else "0")
     return request.param
 
 
@@ -76,8 +80,10 @@ CONV_CASES = [
     (1, 2, 10, 10, 16, 16),
     (1, 1, 3, 200, 128, 96),    # 5 tiles: a CTA pair's second slot is empty
     (1, 4, 5, 7, 64, 32),       # 1 tile per frame: pairs straddle frames t=0|1, 2|3
-    (1, 3, 32, 16, 96, 96),     # whole 16x8 patches (halo mode's own choice)
+    (1, 3, 32, 16, 96, 96),     # whole 16x8 and 16x16 patches (the halo modes' own choice)
     (2, 2, 16, 24, 64, 192),
+    (1, 2, 32, 40, 64, 64),     # 16x16 patches with a ragged last patch column
+    (2, 3, 17, 33, 96, 96),     # ragged in H and W, several patches, two clips
 ]
 
 

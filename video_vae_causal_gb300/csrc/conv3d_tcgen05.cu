@@ -38,6 +38,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -67,11 +68,16 @@ struct ConvArgs {
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
     uint32_t off_bars, off_misc, off_vec;
-    int acc_cols, nacc, tmem_cols;
+    int acc_cols;        // TMEM columns of one 128-row accumulator
+    int acc_stride;      // columns of one accumulator buffer (nq accumulators)
+    int nacc, tmem_cols;
     int staged;          // epilogue through a whole-tile smem buffer + TMA stores
     uint32_t off_stage;  // 1024-aligned offset of that buffer
     int halo;            // 16x8 patch tiles, one halo load per (kt, chunk) for 9 taps
     int patches_w;       // patches per frame row (halo mode)
+    int nq;              // 128-row sub-tiles per CTA tile (halo mode: 1, or 2 for 16x16 patches)
+    int halo_w;          // halo width in pixels: 8 * nq + 2
+    uint32_t plane_bytes;  // one 8-channel plane of the halo: 18 * halo_w * 16
     int tb;              // spatial taps per weight stage (halo mode: 1, 3)
     uint32_t off_a, a_stride, a_tx;  // halo ring: 2 buffers, bytes per CTA per load
     int epi;
@@ -97,11 +103,12 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
     ti.n = ti.frame / p.T;
     ti.t = ti.frame - ti.n * p.T;
     if (p.halo) {
-        // 16 x 8 (H x W) patch: tile row m is pixel (h0 + m / 8, w0 + m % 8).
+        // 16 x 8nq (H x W) patch of nq sub-tiles: row m of sub-tile s is
+        // pixel (h0 + m / 8, w0 + 8 s + m % 8).
         const int pt = ti.pos / kBlockM;
         const int ph = pt / p.patches_w;
         ti.h0 = ph * 16;
-        ti.w0 = (pt - ph * p.patches_w) * 8;
+        ti.w0 = (pt - ph * p.patches_w) * 8 * p.nq;
         ti.row0 = ti.frame * p.HW + ti.h0 * p.W + ti.w0;  // first pixel's voxel index
     } else {
         ti.h0 = ti.pos / p.W;
@@ -111,14 +118,13 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
     return ti;
 }
 
-// Halo mode: every smem halo is 18 x 10 pixels (a 16 x 8 patch grown by the
-// 3x3 window), stored as planes of 8 channels: plane j holds 16 bytes for
-// each of the 180 pixels, row-major.  The MMA A operand of tap (kh, kw) is
-// the window starting at pixel (kh, kw): rows 16 bytes apart inside a
-// patch row, patch rows one halo row (10 pixels = 160 bytes) apart, K-planes
-// one plane (2880 bytes) apart -- a no-swizzle K-major operand.
-constexpr uint32_t kHaloW = 10, kHaloH = 18;
-constexpr uint32_t kPlaneBytes = kHaloW * kHaloH * 16;
+// Halo mode: every smem halo is 18 x halo_w pixels (a 16 x 8nq patch grown
+// by the 3x3 window; halo_w = 10 or 18), stored as planes of 8 channels:
+// plane j holds 16 bytes for each pixel, row-major.  The MMA A operand of
+// tap (kh, kw) for sub-tile s is the window starting at pixel (kh, kw + 8s):
+// rows 16 bytes apart inside a patch row, patch rows one halo row (halo_w *
+// 16 bytes) apart, K-planes one plane apart -- a no-swizzle K-major operand.
+constexpr uint32_t kHaloH = 18;
 
 __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
@@ -424,17 +430,16 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
     }
 }
 
-// Halo-mode MMAs of one spatial tap: k-step ks uses A planes 2ks, 2ks+1 of
-// the halo window and B sub-tile ks / KK at k-offset ks % KK (sub-tiles
-// b_sub16 descriptor units apart).
+// Halo-mode MMAs of one spatial tap and one 128-row sub-tile: k-step ks uses
+// A planes 2ks, 2ks+1 of the halo window (plane2 descriptor units per k-step)
+// and B sub-tile ks / KK at k-offset ks % KK (sub-tiles b_sub16 units apart).
 template <int kPair, int KK, int NSUB, int NP>
 __device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc, uint64_t a0,
-                                               uint64_t b0, uint32_t b_sub16, uint32_t idesc,
-                                               bool first) {
+                                               uint64_t b0, uint32_t b_sub16, uint32_t plane2,
+                                               uint32_t idesc, bool first) {
     const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
-    constexpr uint32_t kPlane2 = (2 * kPlaneBytes) >> 4;
     auto mma = [&](int s, int kk, int ks, int j) {
-        const uint64_t ad = a0 + (uint64_t)(ks * kPlane2);
+        const uint64_t ad = a0 + (uint64_t)(ks * plane2);
         const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
         const uint32_t accum = (first && ks == 0) ? 0u : 1u;
         const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
@@ -506,10 +511,11 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
 }
 
 // Halo-mode MMA issuer: per (kt, chunk), 9 / tb weight stages of tb spatial
-// taps, each tap reading the halo through a window shifted by (kh, kw); the
-// halo buffer is released after the ninth tap.  Descriptors are the ring
-// bases plus offsets, so nothing but the stage bookkeeping sits between two
-// stages' MMAs.
+// taps, each tap reading the halo through a window shifted by (kh, kw) for
+// each of the nq sub-tiles (one TMEM accumulator each); the halo buffer is
+// released after the ninth tap.  Descriptors are the ring bases plus
+// offsets, so nothing but the stage bookkeeping sits between two stages'
+// MMAs.
 template <int kPair, int KK, int NSUB, int NP>
 __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base,
                               const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
@@ -519,8 +525,9 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
     const uint32_t b_sub16 = p.b_sub_bytes >> 4;
     const uint32_t tap_b16 = (uint32_t)p.nsub * b_sub16;  // one tap's weights
     const uint32_t stage16 = p.stage_bytes >> 4, astride16 = p.a_stride >> 4;
+    const uint32_t plane2 = (2u * p.plane_bytes) >> 4, hrow16 = (uint32_t)p.halo_w;
     const uint64_t bdesc0 = sdesc_kmajor(sbase + p.a_bytes, row_bytes, p.layout);
-    const uint64_t adesc0 = sdesc_plain(sbase + p.off_a, kPlaneBytes, kHaloW * 16u);
+    const uint64_t adesc0 = sdesc_plain(sbase + p.off_a, p.plane_bytes, (uint32_t)p.halo_w * 16u);
     const bool tb3 = p.tb == 3;
     FullRing<kPair == 2> ring;
     int ia = 0, it = 0;
@@ -531,51 +538,55 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         else
             mma_commit(bar);
     };
+    // One stage: taps kw = 0 .. NTAP-1 of row kh (or the single tap `tap0`),
+    // for every sub-tile.  NQ and NTAP are compile-time so the whole stage
+    // is one straight run of MMAs.
+    auto stage = [&](auto nq_c, auto ntap_c, uint32_t dacc, uint64_t abase, int kh, int kw0,
+                     bool first) {
+        constexpr int NQ = decltype(nq_c)::value, NTAP = decltype(ntap_c)::value;
+        const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16);
+        const uint64_t ah = abase + (uint64_t)(kh * hrow16 + kw0);
+#pragma unroll
+        for (int kw = 0; kw < NTAP; ++kw)
+#pragma unroll
+            for (int sq = 0; sq < NQ; ++sq)
+                issue_tap_halo<kPair, KK, NSUB, NP>(
+                    p, dacc + (uint32_t)(sq * p.acc_cols), ah + (uint64_t)(kw + 8 * sq),
+                    b0 + (uint64_t)(kw * tap_b16), b_sub16, plane2, idesc, first && kw == 0);
+    };
+    using I1 = std::integral_constant<int, 1>;
+    using I2 = std::integral_constant<int, 2>;
+    using I3 = std::integral_constant<int, 3>;
     for (int u = unit0; ok && u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
         if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
-        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_cols);
+        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
         const int kt0 = unit_first_kt<kPair>(u, p);
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
                 const uint64_t abase = adesc0 + (uint64_t)(ia * astride16);
-                if (tb3) {
-                    // the first stage of (kt, cc) also carries the halo
-                    for (int kh = 0; kh < 3; ++kh) {
-                        if (!ring.acquire(bars, wc)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16);
-                        const uint64_t ah = abase + (uint64_t)(kh * kHaloW);
-#pragma unroll
-                        for (int kw = 0; kw < 3; ++kw)
-                            issue_tap_halo<kPair, KK, NSUB, NP>(p, dacc, ah + kw,
-                                                                b0 + (uint64_t)(kw * tap_b16),
-                                                                b_sub16, idesc, first && kw == 0);
-                        first = false;
-                        commit(bars.empty(ring.stage));
-                        ring.advance(bars);
+                // the first stage of (kt, cc) also carries the halo
+                const int nst = tb3 ? 3 : 9;
+                for (int g = 0; g < nst; ++g) {
+                    if (!ring.acquire(bars, wc)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    for (int t9 = 0; t9 < 9; ++t9) {
-                        if (!ring.acquire(bars, wc)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const int kh = t9 / 3, kw = t9 - 3 * kh;
-                        issue_tap_halo<kPair, KK, NSUB, NP>(
-                            p, dacc, abase + (uint64_t)(kh * kHaloW + kw),
-                            bdesc0 + (uint64_t)(ring.stage * stage16), b_sub16, idesc, first);
-                        first = false;
-                        commit(bars.empty(ring.stage));
-                        ring.advance(bars);
+                    tc_fence_after();
+                    const int kh = tb3 ? g : g / 3, kw0 = tb3 ? 0 : g - 3 * (g / 3);
+                    if (p.nq == 2) {
+                        if (tb3) stage(I2{}, I3{}, dacc, abase, kh, kw0, first);
+                        else stage(I2{}, I1{}, dacc, abase, kh, kw0, first);
+                    } else {
+                        if (tb3) stage(I1{}, I3{}, dacc, abase, kh, kw0, first);
+                        else stage(I1{}, I1{}, dacc, abase, kh, kw0, first);
                     }
+                    first = false;
+                    commit(bars.empty(ring.stage));
+                    ring.advance(bars);
                 }
                 if (!ok) break;
                 commit(bars.emptya(ia));
@@ -626,7 +637,7 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
         if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
-        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_cols);
+        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
         const int nst = unit_stages<kPair>(u, p);
         for (int k = 0; k < nst; ++k) {
             if (!ring.acquire(bars, wc)) {
@@ -728,12 +739,13 @@ struct RowMap {
     }
 };
 
-__device__ __forceinline__ RowMap warp_rows(const ConvArgs &p, const TileInfo &ti, int q) {
+__device__ __forceinline__ RowMap warp_rows(const ConvArgs &p, const TileInfo &ti, int q,
+                                            int sub = 0) {
     RowMap rm;
     if (p.halo) {
         rm.seg_rows = 8;
         rm.pitch = p.W;
-        const int ns = p.H - ti.h0 - 4 * q, nc = p.W - ti.w0;
+        const int ns = p.H - ti.h0 - 4 * q, nc = p.W - ti.w0 - 8 * sub;
         rm.nseg = ti.dummy ? 0 : (ns < 0 ? 0 : (ns > 4 ? 4 : ns));
         rm.ncol = nc < 0 ? 0 : (nc > 8 ? 8 : nc);
     } else {
@@ -806,15 +818,18 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         }
         tc_fence_after();
         const TileInfo ti = tile_info(u * kPair + (int)rank, p);
-        // This warp's 32 rows; rows outside the frame (or of an empty pair
-        // slot) are not stored.
-        const RowMap rm = warp_rows(p, ti, q);
+        for (int sub = 0; sub < p.nq; ++sub) {
+        // This warp's 32 rows of sub-tile `sub`; rows outside the frame (or
+        // of an empty pair slot) are not stored.
+        const RowMap rm = warp_rows(p, ti, q, sub);
         const bool valid = rm.valid(lane);
-        const int64_t wbase = p.halo ? (int64_t)ti.row0 + (int64_t)(4 * q) * p.W
+        const int64_t wbase = p.halo ? (int64_t)ti.row0 + (int64_t)(4 * q) * p.W + 8 * sub
                                      : (int64_t)ti.row0 + q * 32;
         const int64_t g = wbase + rm.offset(lane);
-        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * p.acc_cols);
+        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
+                            (uint32_t)(a * p.acc_stride + sub * p.acc_cols);
         __nv_bfloat16 *out_w = p.out + wbase * p.c_out;
+        float *part = s_part + sub * 2 * kBlockM;  // each sub-tile its own partial sums
         if (p.epi == kEpiNormSilu) {
             // RMS_norm over all c_out channels of this voxel, then SiLU.
             float ss = 0.f;
@@ -830,9 +845,9 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                     }
                 }
             }
-            s_part[half * kBlockM + row] = ss;
+            part[half * kBlockM + row] = ss;
             asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-            const float tot = s_part[row] + s_part[kBlockM + row];
+            const float tot = part[row] + part[kBlockM + row];
             const float scale = p.sqrt_c / fmaxf(sqrtf(tot), p.eps);
             for (int c = c_begin; c < c_end; c += 32) {
                 uint32_t r[32];
@@ -853,8 +868,8 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 }
                 store_chunk(stg, o, n, out_w, p.c_out, c, rm);
             }
-            // s_part is rewritten only after the next tile's bar_any, which
-            // every warp reaches after its last read above.
+            // A sub-tile's partial sums are rewritten only after the next
+            // tile's bar_any, which every warp reaches after its last read.
         } else {
             const uint4 *res = p.epi == kEpiResidual
                                    ? reinterpret_cast<const uint4 *>(p.resid + g * p.c_out)
@@ -887,6 +902,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 store_chunk(stg, o, n, out_w, p.c_out, c, rm);
             }
         }
+        }  // sub-tiles
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -1071,8 +1087,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_misc + 4);
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
-    float *s_part = s_gamma + p.c_out;  // [2][128] partial sums of squares
-    uint8_t *s_stage = reinterpret_cast<uint8_t *>(s_part + 2 * kBlockM);  // output staging
+    float *s_part = s_gamma + p.c_out;  // [2 sub-tiles][2][128] partial sums of squares
+    uint8_t *s_stage = reinterpret_cast<uint8_t *>(s_part + 4 * kBlockM);  // output staging
 
     // Work units: single tiles, or pairs of consecutive tiles per cluster.
     const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
@@ -1298,16 +1314,17 @@ bool encode_weight_taps(CUtensorMap *m, const void *base, uint64_t K, int c_in, 
 }
 
 // NHWC input viewed as (8 channels, W, H, C/8 chunks, frames): the chunk
-// dimension (16 bytes apart) is outside the spatial ones, so one 18 x 10
-// pixel box of `chunk` channels lands as planes [chunk/8][18][10][8 ch], the
-// no-swizzle layout the halo-mode MMAs read.  Pixels outside the frame read
-// as zeros (the conv's spatial pad).
-bool encode_halo(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int chunk) {
+// dimension (16 bytes apart) is outside the spatial ones, so one 18 x halo_w
+// pixel box of `chunk` channels lands as planes [chunk/8][18][halo_w][8 ch],
+// the no-swizzle layout the halo-mode MMAs read.  Pixels outside the frame
+// read as zeros (the conv's spatial pad).
+bool encode_halo(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int chunk,
+                 int halo_w) {
     cuuint64_t dims[5] = {8, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)(C / 8),
                           (cuuint64_t)frames};
     cuuint64_t strides[4] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, 16,
                              (cuuint64_t)H * W * C * 2};
-    cuuint32_t box[5] = {8, kHaloW, kHaloH, (cuuint32_t)(chunk / 8), 1};
+    cuuint32_t box[5] = {8, (cuuint32_t)halo_w, kHaloH, (cuuint32_t)(chunk / 8), 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1339,8 +1356,11 @@ struct Plan {
     int acc_cols, nacc, tmem_cols;
     int staged;
     uint32_t off_stage;
-    int halo;
+    int halo;  // 16 x 8 patch tiles with halo loads
     int tb;  // spatial taps per weight stage (halo mode)
+    int nq, halo_w;  // sub-tiles per CTA tile, halo width in pixels (halo mode)
+    uint32_t plane_bytes;
+    int acc_stride;
     uint32_t off_a, a_stride, a_tx;
 };
 
@@ -1363,9 +1383,26 @@ int pair_choice() {
     return (e && e[0] == '1' && e[1] == 0) ? 1 : 2;
 }
 
-bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
+// Wide halo tiles (16 x 16 patches, two accumulators per CTA) where the
+// patches tile the frame and the layer is narrow enough (make_plan checks
+// c_out and the shortcut).  WANVAE_CONV_WIDE=0/1 forces either.
+int wide_choice(const ConvSpec &s, int halo) {
+    if (!halo) return 0;
+    const char *e = getenv("WANVAE_CONV_WIDE");
+    if (e && e[0] && e[1] == 0 && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+    return s.H % 16 == 0 && s.W % 16 == 0;
+}
+
+bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.pair = pair;
     pl.halo = halo;
+    // Wide halo tiles: 16 x 16 patches, two 128-row sub-tiles per CTA, so
+    // every weight stage feeds twice the MMAs.  Two double-buffered
+    // accumulators per CTA must fit TMEM (c_out <= 128); no shortcut segment.
+    pl.nq = (halo && wide) ? 2 : 1;
+    if (pl.nq == 2 && (s.sc_in || s.c_out > 128)) return false;
+    pl.halo_w = 8 * pl.nq + 2;
+    pl.plane_bytes = (uint32_t)(kHaloH * pl.halo_w * 16);
     int sw = pick_sw(s.c_in);
     if (s.sc_in) {
         const int sw2 = pick_sw(s.c_sc);
@@ -1384,8 +1421,10 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     if (!pl.n_pieces) return false;
     pl.piece_n = s.c_out / pl.n_pieces;
     pl.acc_cols = (s.c_out + 31) / 32 * 32;
-    pl.nacc = 2 * pl.acc_cols <= 512 ? 2 : 1;
-    int cols = pl.nacc * pl.acc_cols;
+    pl.acc_stride = pl.nq * pl.acc_cols;
+    pl.nacc = 2 * pl.acc_stride <= 512 ? 2 : 1;
+    if (pl.nq == 2 && pl.nacc != 2) return false;
+    int cols = pl.nacc * pl.acc_stride;
     pl.tmem_cols = 32;
     while (pl.tmem_cols < cols) pl.tmem_cols *= 2;
     if (pl.tmem_cols > 512) return false;
@@ -1398,7 +1437,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     // fits next to a 3-deep pipeline.
     const uint32_t stage_tile = (uint32_t)kBlockM * s.c_out * 2u;
     const uint32_t fixed = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out +
-                           2u * 4u * kBlockM /*norm partial sums*/;
+                           4u * 4u * kBlockM /*norm partial sums*/;
     pl.staged = 0;
     if (pl.nacc == 1 && s.c_out % 64 == 0) {
         const uint32_t sb1 = (kBlockM + b_rows) * (uint32_t)sw * 2u;
@@ -1409,7 +1448,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
         fixed + (pl.staged ? stage_tile : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
     const int need_stages = pl.staged ? 3 : min_stages;
     if (halo) {
-        // Halo ring (2 buffers of 18 x 10 pixels x chunk channels) + a ring of
+        // Halo ring (2 buffers of 18 x halo_w pixels x chunk channels) + a ring of
         // weight stages of tb spatial taps each.  Every stage costs the MMA
         // issuer one barrier access, so take the (chunk, tb) with the fewest
         // stages per tile among those that leave a deep enough ring (>= 3
@@ -1420,7 +1459,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
         int best_waits = 0, best_stages = 0;
         for (int d = 4; d >= 1; --d) {
             if (d * sw > 128 || g_main % d || g_sc % d) continue;
-            const uint32_t ha = ((uint32_t)(kHaloW * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
+            const uint32_t ha = ((uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
             for (int tb = 3; tb >= 1; tb -= 2) {
                 if (tb > 1 && pl.n_pieces != 1) continue;
                 const uint32_t bs = ((uint32_t)(tb * d) * b_rows * sw * 2u + 1023u) & ~1023u;
@@ -1443,7 +1482,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
         pl.kc_short = s.sc_in ? g_sc / d : 0;
         pl.a_sub = (uint32_t)kBlockM * sw * 2;  // one x-patch sub-tile (shortcut)
         pl.b_sub = b_rows * sw * 2;
-        pl.a_tx = (uint32_t)(kHaloW * kHaloH) * d * sw * 2u;
+        pl.a_tx = (uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u;
         pl.a_stride = (pl.a_tx + 1023u) & ~1023u;
         pl.off_a = 0;
         pl.a_bytes = 2u * pl.a_stride;  // the weight ring starts here
@@ -1457,7 +1496,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
         pl.off_bars = off;
         pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 8);
         pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
+        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                         (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
         if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
         return pl.smem_bytes <= (uint32_t)kSmemBudget;
@@ -1490,7 +1529,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo) {
     pl.off_bars = off;
     pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 8);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 2u * 4u * kBlockM +
+    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                     (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
     if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
@@ -1569,6 +1608,15 @@ cudaError_t kernel_facts(ConvKernelFn fn, bool pair, int &max_pairs) {
     return cudaSuccess;
 }
 
+// The first plan that fits: the preferred CTA grouping with wide halo tiles,
+// then plain halo tiles, then the same on single CTAs, then im2col.
+bool pick_plan(const ConvSpec &s, Plan &pl, int pair) {
+    const int hc = halo_choice(s), wc = wide_choice(s, hc);
+    return (wc && make_plan(s, pl, pair, hc, 1)) || make_plan(s, pl, pair, hc, 0) ||
+           (wc && make_plan(s, pl, 1, hc, 1)) || make_plan(s, pl, 1, hc, 0) ||
+           make_plan(s, pl, 1, 0, 0);
+}
+
 }  // namespace
 
 int conv3d_supported(const ConvSpec &s) {
@@ -1577,18 +1625,12 @@ int conv3d_supported(const ConvSpec &s) {
     if (s.c_in > 4096) return -1;
     if (s.sc_in && (s.c_sc < 16 || s.c_sc % 16 || s.c_sc > 4096)) return -1;
     Plan pl;
-    return (make_plan(s, pl, 2, halo_choice(s)) || make_plan(s, pl, 1, halo_choice(s)) ||
-            make_plan(s, pl, 1, 0))
-               ? 0
-               : -1;
+    return pick_plan(s, pl, 2) ? 0 : -1;
 }
 
 cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     Plan pl;
-    const int hc = halo_choice(s);
-    if (!make_plan(s, pl, pair_choice(), hc) && !make_plan(s, pl, 1, hc) &&
-        !make_plan(s, pl, 1, 0))
-        return cudaErrorInvalidValue;
+    if (!pick_plan(s, pl, pair_choice())) return cudaErrorInvalidValue;
     if (!load_encoders()) return cudaErrorInvalidValue;
     ConvKernelFn fn = pl.pair == 2 ? pick_kernel<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
                                    : pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
@@ -1596,7 +1638,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     cudaError_t fe = kernel_facts(fn, pl.pair == 2, max_pairs);
     if (fe != cudaSuccess) return fe;
     if (pl.pair == 2 && max_pairs < 1) {
-        if (!make_plan(s, pl, 1, pl.halo) && !make_plan(s, pl, 1, 0)) return cudaErrorInvalidValue;
+        if (!pick_plan(s, pl, 1)) return cudaErrorInvalidValue;
         fn = pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
         fe = kernel_facts(fn, false, max_pairs);
         if (fe != cudaSuccess) return fe;
@@ -1614,8 +1656,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     bool ok = true;
     if (pl.halo) {
         const int chunk = pl.nsub * pl.sw;
-        ok = ok && encode_halo(&mA, s.in, s.c_in, s.W, s.H, frames, chunk);
-        if (s.cache) ok = ok && encode_halo(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, chunk);
+        ok = ok && encode_halo(&mA, s.in, s.c_in, s.W, s.H, frames, chunk, pl.halo_w);
+        if (s.cache)
+            ok = ok && encode_halo(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, chunk, pl.halo_w);
     } else if (s.k == 3) {
         ok = ok && encode_im2col(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw);
         if (s.cache) ok = ok && encode_im2col(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, pl.sw);
@@ -1667,7 +1710,10 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.piece_n = pl.piece_n;
     a.layout = pl.sw == 64 ? kLayoutSw128 : (pl.sw == 32 ? kLayoutSw64 : kLayoutSw32);
     a.halo = pl.halo;
-    a.patches_w = (s.W + 7) / 8;
+    a.nq = pl.halo ? pl.nq : 1;
+    a.halo_w = pl.halo_w;
+    a.plane_bytes = pl.plane_bytes;
+    a.patches_w = (s.W + 8 * a.nq - 1) / (8 * a.nq);
     a.tb = pl.tb;
     a.off_a = pl.off_a;
     a.a_stride = pl.a_stride;
@@ -1686,6 +1732,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.staged = pl.staged;
     a.off_stage = pl.off_stage;
     a.acc_cols = pl.acc_cols;
+    a.acc_stride = pl.acc_stride;
     a.nacc = pl.nacc;
     a.tmem_cols = pl.tmem_cols;
     a.epi = s.epi;
