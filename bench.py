@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--frames", type=int, default=None,
+                    help="override the workload's T (smaller cases for profiling); the "
+                         "JSON line's config records the dims actually run")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["tiny", "latent_fullT", "stream_720p", "reduce_384_192",
                              "fullres_96"],
@@ -77,10 +80,10 @@ def conv_source_sha():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per conv launch from the committed ncu summary, if it was
-    taken on the current conv source (else None)."""
-    path = os.path.join(ROOT, "profiles", "conv3d_tcgen05_latent_fullT.md")
+def profiled_traffic(name):
+    """DRAM bytes per conv launch of workload `name` from its committed ncu
+    summary, if there is one taken on the current conv source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"conv3d_tcgen05_{name}.md")
     try:
         kv = {}
         for line in open(path):
@@ -264,6 +267,8 @@ def bench_ours(args):
 
     name = args.workload
     dims, ci, co, calls = synth.WORKLOADS[name]
+    if args.frames:
+        dims = (dims[0], args.frames) + tuple(dims[2:])
     B, T, H, W = dims
     M = B * T * H * W
     streaming = calls > 0
@@ -369,7 +374,7 @@ def bench_ours(args):
     conv_ms = (sum(convA_ms) + sum(convB_ms)) / (K * n_conv_launches)
     achieved = flop_conv / (conv_ms / 1e3) / 1e12
     norm_gbs = (2.0 * ci * 2 * M) / (statistics.mean(norm_ms) / 1e3) / 1e9
-    traffic = profiled_traffic() if name == WORKLOAD else None
+    traffic = profiled_traffic(name) if not args.frames else None
     block_flop = flop_A + flop_B
 
     if rank != 0:
