@@ -65,6 +65,7 @@ struct ConvArgs {
     int n_pieces, piece_n;
     uint32_t layout;     // UMMA swizzle mode matching sw
     int tiles_per_frame, num_tiles;
+    int frames;          // B * T
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
     uint32_t off_bars, off_misc, off_vec;
@@ -94,12 +95,20 @@ struct TileInfo {
     bool dummy;  // a pair's second slot past the last tile: zero A, nothing stored
 };
 
+// Halo mode orders tiles patch-major, frame-minor: the tiles of the three
+// output frames that read one input frame (its temporal taps) run side by
+// side, so a frame is fetched from DRAM about once although it does not fit
+// L2 three times over.  im2col mode orders them frame-major.
+__device__ __forceinline__ int tile_frame(int tile, const ConvArgs &p) {
+    return p.halo ? tile % p.frames : tile / p.tiles_per_frame;
+}
+
 __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
     TileInfo ti;
     ti.dummy = tile >= p.num_tiles;
     if (ti.dummy) tile = 0;
-    ti.frame = tile / p.tiles_per_frame;
-    ti.pos = (tile - ti.frame * p.tiles_per_frame) * kBlockM;
+    ti.frame = tile_frame(tile, p);
+    ti.pos = (p.halo ? tile / p.frames : tile - ti.frame * p.tiles_per_frame) * kBlockM;
     ti.n = ti.frame / p.T;
     ti.t = ti.frame - ti.n * p.T;
     if (p.halo) {
@@ -147,7 +156,7 @@ __device__ __forceinline__ int unit_first_kt(int unit, const ConvArgs &p) {
     for (int r = 0; r < kPair; ++r) {
         const int tile = unit * kPair + r;
         if (tile >= p.num_tiles) continue;
-        const int t = (tile / p.tiles_per_frame) % p.T;
+        const int t = tile_frame(tile, p) % p.T;
         const int k = t >= 2 ? 0 : 2 - t;
         kt0 = k < kt0 ? k : kt0;
     }
@@ -1720,6 +1729,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.a_tx = pl.a_tx;
     a.tiles_per_frame = pl.halo ? ((s.H + 15) / 16) * a.patches_w : (HW + kBlockM - 1) / kBlockM;
     a.num_tiles = a.tiles_per_frame * frames;
+    a.frames = frames;
     a.stages = pl.stages;
     a.a_sub_bytes = pl.a_sub;
     a.b_sub_bytes = pl.b_sub;

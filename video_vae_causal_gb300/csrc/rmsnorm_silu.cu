@@ -21,7 +21,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + __expf(-z)); }
+// The pass is bound by issue slots, not DRAM, at 8 channels per 16-byte
+// vector, so SiLU uses the fast reciprocal-based divide (for z below about
+// -87 the denominator overflows and the result is the limit 0).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // One group of L lanes owns one voxel; each lane holds VPT 16-byte vectors
 // of it (vector j of the voxel lives in lane j % L, slot j / L), so every
@@ -123,18 +126,26 @@ cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n,
     const int vpt = V / L;
     const int threads = 256;
     const int64_t voxels_per_block = (threads / 32) * (32 / L) * (vpt <= 4 ? 2 : 1);
-    int64_t blocks = (n + voxels_per_block - 1) / voxels_per_block;
-    const int64_t cap = (int64_t)ctx.num_sms * 3;  // one resident wave (72 registers/thread)
-    if (blocks > cap) blocks = cap;
+    const int64_t blocks = (n + voxels_per_block - 1) / voxels_per_block;
     const float sqrt_c = sqrtf((float)C);
     auto *xi = static_cast<const uint4 *>(x);
     auto *yo = static_cast<uint4 *>(y);
+    // One resident wave (grid-stride beyond it): as many CTAs per SM as the
+    // instantiation's registers allow, looked up once per instantiation.
 #define WANVAE_NORM_CASE(K)                                                              \
-    case K:                                                                              \
-        rmsnorm_silu_kernel<F32, K, (K <= 4 ? 2 : 1)>                                    \
-            <<<(unsigned)blocks, threads, 0, ctx.stream>>>(xi, yo, gamma, n, C, L, eps,  \
-                                                           sqrt_c);                      \
-        break;
+    case K: {                                                                            \
+        auto *kern = rmsnorm_silu_kernel<F32, K, (K <= 4 ? 2 : 1)>;                      \
+        static int per_sm = 0;                                                           \
+        if (per_sm == 0 &&                                                               \
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) !=  \
+                cudaSuccess)                                                             \
+            per_sm = 2;                                                                  \
+        if (per_sm < 1) per_sm = 1;                                                      \
+        const int64_t cap = (int64_t)ctx.num_sms * per_sm;                               \
+        kern<<<(unsigned)(blocks < cap ? blocks : cap), threads, 0, ctx.stream>>>(        \
+            xi, yo, gamma, n, C, L, eps, sqrt_c);                                        \
+        break;                                                                           \
+    }
     switch (vpt) {
         WANVAE_NORM_CASE(1)
         WANVAE_NORM_CASE(2)
