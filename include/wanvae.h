@@ -125,8 +125,10 @@ wanvae_status wanvae_rmsnorm_silu(const void *x, void *y, const float *gamma,
  *   cache : NULL for a whole clip (zero causal pad), or bf16 [B][2][H][W][c_in]
  *           holding the two frames before x (read, then replaced in stream
  *           order by the last two frames of concat(cache, x)).
- * Errors: INVALID_ARG, UNSUPPORTED (c_in or c_out not a multiple of 16 or
- * above 512), MISALIGNED, CUDA. */
+ *   c_in  : a multiple of 16, at most 512.  c_out: 1 to 15 (a decoder's
+ *           conv_out, e.g. 96 -> 3; the kernel pads N internally) or a
+ *           multiple of 16 up to 512.
+ * Errors: INVALID_ARG, UNSUPPORTED (other channel counts), MISALIGNED, CUDA. */
 wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bias,
                                    void *y, wanvae_dims d, int64_t c_in, int64_t c_out,
                                    int k, void *cache, wanvae_stream stream);

@@ -86,6 +86,8 @@ def test_conv_argument_errors(lib):
     assert f(A, A, None, Y, _dims(1, 0, 4, 4), 32, 32, 3, None, None) == wanvae.ERR_INVALID_ARG
     assert f(A, A, None, Y, d, 40, 32, 3, None, None) == wanvae.ERR_UNSUPPORTED
     assert f(A, A, None, Y, d, 32, 1024, 3, None, None) == wanvae.ERR_UNSUPPORTED
+    assert f(A, A, None, Y, d, 32, 17, 3, None, None) == wanvae.ERR_UNSUPPORTED  # 16 < c_out, % 16
+    assert f(A, A, None, Y, d, 32, 0, 3, None, None) == wanvae.ERR_INVALID_ARG
     assert f(A, A + 4, None, Y, d, 32, 32, 3, None, None) == wanvae.ERR_MISALIGNED
     assert f(A, A, None, A + 16, d, 32, 32, 3, None, None) == wanvae.ERR_INVALID_ARG  # alias
 

@@ -84,6 +84,7 @@ CONV_CASES = [
     (2, 2, 16, 24, 64, 192),
     (1, 2, 32, 40, 64, 64),     # 16x16 patches with a ragged last patch column
     (2, 3, 17, 33, 96, 96),     # ragged in H and W, several patches, two clips
+    (1, 3, 12, 20, 16, 384),    # a decoder's conv_in (16 -> 384)
 ]
 
 
@@ -102,6 +103,39 @@ def test_conv3d_k3_full_clip(cuda_lib, case, variant):
     y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
     cuda_lib.sync_status()
     compare(to_f64(y), oracle.causal_conv3d(x, w, b), what=f"conv3 {case}")
+
+
+# Narrow outputs (c_out < 16): a decoder's conv_out to RGB and odd widths; N is
+# padded inside the kernel and the weight rows past c_out read as zeros.
+NARROW_CASES = [
+    (1, 3, 12, 20, 96, 3),      # conv_out 96 -> 3, ragged tiles
+    (2, 2, 9, 15, 32, 1),
+    (1, 3, 32, 32, 64, 13),     # whole 16x16 patches (wide halo tiles)
+    (1, 2, 16, 24, 128, 8),
+]
+
+
+@pytest.mark.parametrize("case", NARROW_CASES)
+def test_conv3d_k3_narrow_output(cuda_lib, case, variant):
+    B, T, H, W, ci, co = case
+    x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=70 + sum(case))
+    y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.causal_conv3d(x, w, b), what=f"conv3 narrow {case}")
+
+
+def test_conv3d_narrow_with_cache_and_k1(cuda_lib, variant):
+    B, T, H, W, ci, co = 1, 2, 9, 14, 64, 3
+    x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=80)
+    cache = synth.make_tensor((B, 2, H, W, ci), seed=81)
+    cache_d = cache.to(DEV)
+    y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV), cache=cache_d)
+    x1, w1, b1 = conv_inputs(1, 2, 7, 9, 16, 5, 1, seed=82)
+    y1 = cuda_lib.causal_conv3d(x1.to(DEV), w1.to(DEV), b1.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.causal_conv3d(x, w, b, cache=cache), what="conv3 narrow cache")
+    assert np.array_equal(to_f64(cache_d), oracle.cache_next(cache, x))
+    compare(to_f64(y1), oracle.causal_conv3d(x1, w1, b1), what="conv1 narrow")
 
 
 @pytest.mark.parametrize("case", [(1, 3, 12, 20, 64, 64), (2, 2, 9, 15, 32, 48),

@@ -132,7 +132,9 @@ wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bi
     if (k != 1 && k != 3) return WANVAE_ERR_INVALID_ARG;
     if (k == 1 && cache) return WANVAE_ERR_INVALID_ARG;
     if (!dims_ok(d) || c_in < 1 || c_out < 1) return WANVAE_ERR_INVALID_ARG;
-    if (c_in % 16 || c_out % 16 || c_in > 512 || c_out > 512) return WANVAE_ERR_UNSUPPORTED;
+    // c_out below 16 (a decoder's conv_out to RGB) is padded inside the kernel.
+    if (c_in % 16 || (c_out % 16 && c_out > 15) || c_in > 512 || c_out > 512)
+        return WANVAE_ERR_UNSUPPORTED;
     if (misaligned(x) || misaligned(w) || misaligned(y) || misaligned(bias) || misaligned(cache))
         return WANVAE_ERR_MISALIGNED;
     const int64_t M = voxels(d);

@@ -80,6 +80,8 @@ struct ConvArgs {
     int halo_w;          // halo width in pixels: 8 * nq + 2
     uint32_t plane_bytes;  // one 8-channel plane of the halo: 18 * halo_w * 16
     int tb;              // spatial taps per weight stage (halo mode: 1, 3)
+    int narrow;          // c_out < 16: N padded to 16 per CTA, rows past c_out read as zeros
+    int bc_row, bc_rank; // B box coordinates of this CTA's rows: (rank * bc_row, rank * bc_rank)
     uint32_t off_a, a_stride, a_tx;  // halo ring: 2 buffers, bytes per CTA per load
     int epi;
     float eps, sqrt_c;
@@ -277,7 +279,8 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                     const CUtensorMap *bm = shortcut ? mapSB : mapB;
                     const int bk = shortcut ? c0 : tap * p.c_in + c0;
                     if (kPair == 2)
-                        tma_load_4d_pair(db, bm, fb, bk, 0, (int)rank, 0);
+                        tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
+                                         (int)rank * p.bc_rank, 0);
                     else
                         tma_load_4d(db, bm, fb, bk, 0, 0, 0);
                 }
@@ -410,7 +413,8 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                         load5<kPair>(da, am, fb, 0, ti.w0 - 1, ti.h0 - 1, cc * (chunk / 8), fidx);
                     // tb consecutive spatial taps of this chunk in one box
                     const int tap = kt * 9 + g * p.tb;
-                    load5<kPair>(db, mapB, fb, tap * p.c_in + cc * chunk, 0, (int)rank, 0, 0);
+                    load5<kPair>(db, mapB, fb, tap * p.c_in + cc * chunk, (int)rank * p.bc_row,
+                                 (int)rank * p.bc_rank, 0, 0);
                 }
             }
         }
@@ -839,7 +843,19 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                             (uint32_t)(a * p.acc_stride + sub * p.acc_cols);
         __nv_bfloat16 *out_w = p.out + wbase * p.c_out;
         float *part = s_part + sub * 2 * kBlockM;  // each sub-tile its own partial sums
-        if (p.epi == kEpiNormSilu) {
+        if (p.narrow) {
+            // c_out < 16 (bias epilogue only): one 16-column TMEM load, then
+            // each row's c_out channels as scalar bf16 stores.
+            if (half == 0) {
+                uint32_t r[32];
+                tmem_ld_cols(tb, 16, r);
+                if (valid) {
+                    __nv_bfloat16 *o = p.out + g * p.c_out;
+                    for (int c = 0; c < p.c_out; ++c)
+                        o[c] = __float2bfloat16_rn(__uint_as_float(r[c]) + s_bias[c]);
+                }
+            }
+        } else if (p.epi == kEpiNormSilu) {
             // RMS_norm over all c_out channels of this voxel, then SiLU.
             float ss = 0.f;
             for (int c = c_begin; c < c_end; c += 32) {
@@ -1285,10 +1301,16 @@ bool encode_frames(CUtensorMap *m, const void *base, int C, int HW, int frames) 
 // N-piece, landing as [piece][half_n rows][sw] -- the B layout the MMAs read.
 // With nsub > 0 a fifth dimension of nsub sub-tiles (sw channels apart in K)
 // lands as [sub-tile][piece][half_n rows][sw]: one load for a whole chunk.
+//
+// Narrow layers (c_out < 16, n_pieces = 1, the piece padded to 16 rows per
+// CTA): the row dimension is the true c_out and the pair dimension has extent
+// 1; a CTA's box starts at row rank * half_n, and rows past c_out read as zeros.
 bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int pair,
-                    int n_pieces, int sw, int nsub) {
-    const int piece_n = c_out / n_pieces, half_n = piece_n / pair;
-    cuuint64_t dims[5] = {K, (cuuint64_t)half_n, (cuuint64_t)pair, (cuuint64_t)n_pieces,
+                    int n_pieces, int sw, int nsub, int npad = 0) {
+    const bool narrow = npad > c_out;
+    const int piece_n = (narrow ? npad : c_out) / n_pieces, half_n = piece_n / pair;
+    cuuint64_t dims[5] = {K, (cuuint64_t)(narrow ? c_out : half_n),
+                          (cuuint64_t)(narrow ? 1 : pair), (cuuint64_t)n_pieces,
                           (cuuint64_t)(nsub > 0 ? nsub : 1)};
     cuuint64_t strides[4] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)piece_n * K * 2,
                              (cuuint64_t)sw * 2};
@@ -1307,10 +1329,11 @@ bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int
 // box holds this CTA's rows of tb consecutive taps of one channel chunk, laid
 // out [tap][sub-tile][row][sw], the order the halo-mode MMAs step through.
 bool encode_weight_taps(CUtensorMap *m, const void *base, uint64_t K, int c_in, int c_out,
-                        int pair, int sw, int nsub, int tb) {
-    const int half_n = c_out / pair;
-    cuuint64_t dims[5] = {K, (cuuint64_t)half_n, (cuuint64_t)pair, (cuuint64_t)nsub,
-                          (cuuint64_t)tb};
+                        int pair, int sw, int nsub, int tb, int npad = 0) {
+    const bool narrow = npad > c_out;  // as in encode_weights
+    const int half_n = (narrow ? npad : c_out) / pair;
+    cuuint64_t dims[5] = {K, (cuuint64_t)(narrow ? c_out : half_n),
+                          (cuuint64_t)(narrow ? 1 : pair), (cuuint64_t)nsub, (cuuint64_t)tb};
     cuuint64_t strides[4] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)sw * 2,
                              (cuuint64_t)c_in * 2};
     cuuint32_t box[5] = {(cuuint32_t)sw, (cuuint32_t)half_n, 1, (cuuint32_t)nsub,
@@ -1368,6 +1391,7 @@ struct Plan {
     int halo;  // 16 x 8 patch tiles with halo loads
     int tb;  // spatial taps per weight stage (halo mode)
     int nq, halo_w;  // sub-tiles per CTA tile, halo width in pixels (halo mode)
+    int narrow, npad;  // c_out < 16: N padded to npad
     uint32_t plane_bytes;
     int acc_stride;
     uint32_t off_a, a_stride, a_tx;
@@ -1420,16 +1444,21 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.sw = sw;
     // N split into equal pieces of at most 256 columns, each a multiple of
     // 16 * pair (a pair splits every piece's rows between its two CTAs).
+    // Narrow layers (c_out < 16) pad N to 16 rows per CTA; their weight rows
+    // past c_out are TMA out-of-bounds zeros and only c_out columns are stored.
+    pl.narrow = s.c_out < 16;
+    if (pl.narrow && (s.sc_in || s.epi != kEpiBias)) return false;
+    pl.npad = pl.narrow ? 16 * pair : s.c_out;
     pl.n_pieces = 0;
-    for (int np = 1; np <= s.c_out / 16; ++np) {
-        if (s.c_out % np == 0 && (s.c_out / np) % (16 * pair) == 0 && s.c_out / np <= 256) {
+    for (int np = 1; np <= pl.npad / 16; ++np) {
+        if (pl.npad % np == 0 && (pl.npad / np) % (16 * pair) == 0 && pl.npad / np <= 256) {
             pl.n_pieces = np;
             break;
         }
     }
     if (!pl.n_pieces) return false;
-    pl.piece_n = s.c_out / pl.n_pieces;
-    pl.acc_cols = (s.c_out + 31) / 32 * 32;
+    pl.piece_n = pl.npad / pl.n_pieces;
+    pl.acc_cols = (pl.npad + 31) / 32 * 32;
     pl.acc_stride = pl.nq * pl.acc_cols;
     pl.nacc = 2 * pl.acc_stride <= 512 ? 2 : 1;
     if (pl.nq == 2 && pl.nacc != 2) return false;
@@ -1438,7 +1467,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     while (pl.tmem_cols < cols) pl.tmem_cols *= 2;
     if (pl.tmem_cols > 512) return false;
 
-    const uint32_t b_rows = (uint32_t)(s.c_out / pair);
+    const uint32_t b_rows = (uint32_t)(pl.npad / pair);
     const int g_main = s.c_in / sw, g_sc = s.sc_in ? s.c_sc / sw : g_main;
     const int min_stages = pair == 2 ? 4 : 3;
     // Whole-tile staged epilogue when a single TMEM accumulator leaves the
@@ -1630,7 +1659,9 @@ bool pick_plan(const ConvSpec &s, Plan &pl, int pair) {
 
 int conv3d_supported(const ConvSpec &s) {
     if (s.k != 1 && s.k != 3) return -1;
-    if (s.c_in < 16 || s.c_in % 16 || s.c_out < 16 || s.c_out % 16 || s.c_out > 512) return -1;
+    if (s.c_in < 16 || s.c_in % 16 || s.c_out < 1 || (s.c_out >= 16 && s.c_out % 16) ||
+        s.c_out > 512)
+        return -1;
     if (s.c_in > 4096) return -1;
     if (s.sc_in && (s.c_sc < 16 || s.c_sc % 16 || s.c_sc > 4096)) return -1;
     Plan pl;
@@ -1676,10 +1707,10 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     }
     if (pl.halo && pl.tb > 1)
         ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)27 * s.c_in, s.c_in, s.c_out, pl.pair,
-                                      pl.sw, pl.nsub, pl.tb);
+                                      pl.sw, pl.nsub, pl.tb, pl.npad);
     else
         ok = ok && encode_weights(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, s.c_out, pl.pair,
-                                  pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0);
+                                  pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0, pl.npad);
     if (s.sc_in) {
         if (pl.halo)
             ok = ok && encode_patch(&mSA, s.sc_in, s.c_sc, s.W, s.H, frames, pl.sw, pl.sw);
@@ -1724,6 +1755,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.plane_bytes = pl.plane_bytes;
     a.patches_w = (s.W + 8 * a.nq - 1) / (8 * a.nq);
     a.tb = pl.tb;
+    a.narrow = pl.narrow;
+    a.bc_row = pl.narrow ? pl.npad / pl.pair : 0;
+    a.bc_rank = pl.narrow ? 0 : 1;
     a.off_a = pl.off_a;
     a.a_stride = pl.a_stride;
     a.a_tx = pl.a_tx;
