@@ -47,9 +47,11 @@ def parse():
                          "JSON line's config records the dims actually run")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["tiny", "latent_fullT", "stream_720p", "reduce_384_192",
-                             "fullres_96"],
+                             "fullres_96", "conv_in_latent", "post_quant_latent",
+                             "conv_out_fullres"],
                     help="latent_fullT (default) is the headline; the others are the remaining "
-                         "workloads of the design notes")
+                         "workloads of the design notes (the conv_* / post_quant_* ones time "
+                         "one CausalConv3d call: the decoder's boundary convs)")
     return ap.parse_args()
 
 
@@ -174,6 +176,12 @@ WORKLOAD_TEXT = {
                       "C_in=384 -> C_out=192, 1x1x1 conv shortcut",
     "fullres_96": "fullres_96: ResidualBlock full-T over x bf16 [1,81,480,832,96], C=96, "
                   "identity shortcut",
+    "conv_in_latent": "conv_in_latent: CausalConv3d k=3 over x bf16 [1,21,60,104,16], "
+                      "16 -> 384 (the decoder's conv_in), full clip",
+    "post_quant_latent": "post_quant_latent: CausalConv3d k=1 over x bf16 [1,21,60,104,16], "
+                         "16 -> 16 (the decoder's post_quant_conv)",
+    "conv_out_fullres": "conv_out_fullres: CausalConv3d k=3 over x bf16 [1,81,480,832,96], "
+                        "96 -> 3 (the decoder's conv_out to RGB), full clip",
 }
 
 
@@ -217,6 +225,8 @@ def bench_reference(args):
     import oracle
     from video_vae_causal_gb300 import synth
     name = args.workload
+    if name in synth.CONV_WORKLOADS:
+        return bench_reference_conv(args)
     dims, ci, co, _ = synth.WORKLOADS[name]
     B, T, H, W = dims
     # The oracle only needs the few rows it runs on: draw the clip's first
@@ -246,8 +256,170 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def bench_reference_conv(args):
+    """The oracle's CausalConv3d, as it stands, on the host cores: each step
+    one bounded sample (the clip's first frames over a band of rows)."""
+    import oracle
+    from video_vae_causal_gb300 import synth
+    name = args.workload
+    dims, ci, co, k = synth.CONV_WORKLOADS[name]
+    B, T, H, W = dims
+    x, w, b = synth.make_conv_inputs((B, min(T, 3), H, W), ci, co, k, seed=0)
+    steps = args.steps if args.steps else 10
+    budget = max(1.0, 60.0 / max(1, steps + args.warmup))
+    t0 = time.perf_counter()
+    oracle.causal_conv3d(x[:, :, :1], w, b)
+    rows = int(max(1, min(H, budget / max(time.perf_counter() - t0, 1e-3))))
+    vals = []
+    for i in range(args.warmup + steps):
+        t0 = time.perf_counter()
+        oracle.causal_conv3d(x[:, :, :rows], w, b)
+        if i >= args.warmup:
+            vals.append(x.shape[0] * x.shape[1] * rows * W / (time.perf_counter() - t0))
+    v = statistics.median(vals)
+    sample = f"the clip's first {x.shape[1]} frames over {rows} of {H} rows x {W} columns"
+    print(json.dumps({
+        "impl": "reference", "metric": "CausalConv3d voxels/s", "value": v, "unit": "voxels/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(name, B, T, H, W, ci, co, 1),
+        "cpu_baseline": {"value": v, "unit": "voxels/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 DEFAULT_STEPS = {"tiny": 300, "latent_fullT": 300, "stream_720p": 20, "reduce_384_192": 20,
-                 "fullres_96": 12}
+                 "fullres_96": 12, "conv_in_latent": 300, "post_quant_latent": 300,
+                 "conv_out_fullres": 30}
+
+
+def bench_conv(args):
+    """One CausalConv3d call per step (the decoder's boundary convs): device
+    time by CUDA events around the call, end to end with host buffers, the
+    roofline of the conv against whichever of the tensor and HBM peaks its
+    arithmetic intensity makes binding, and the oracle on a bounded sample."""
+    import torch
+    import torch.distributed as dist
+
+    from video_vae_causal_gb300 import synth, wanvae
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    wanvae.load()
+    name = args.workload
+    dims, ci, co, k = synth.CONV_WORKLOADS[name]
+    if args.frames:
+        dims = (dims[0], args.frames) + tuple(dims[2:])
+    B, T, H, W = dims
+    M = B * T * H * W
+    on_dev = M * max(ci, co) > (1 << 30)
+    x, w, b = synth.make_conv_inputs(dims, ci, co, k, seed=0, device=dev if on_dev else "cpu")
+    x_cpu = None if on_dev else x
+    w_cpu, b_cpu = w.cpu(), b.cpu()
+    x, w, b = x.to(dev), w.to(dev), b.to(dev)
+    y = torch.empty((B, T, H, W, co), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K = args.steps if args.steps else DEFAULT_STEPS[name]
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        wanvae.causal_conv3d(x, w, b, y=y)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = wanvae.launch_count()
+    with ClockSampler(local) as clk:
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            wanvae.causal_conv3d(x, w, b, y=y)
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+    launches = wanvae.launch_count() - n0
+    wanvae.sync_status()
+    total_ms = max_over_ranks(sum(a.elapsed_time(z) for a, z in evs), ws, dev)
+    ms = total_ms / K
+    value = replica_throughput(M, ws, K, total_ms)
+
+    if x_cpu is None:
+        x_cpu = x.cpu()
+    x_host = x_cpu.pin_memory()
+    y_host = torch.empty((B, T, H, W, co), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    E = max(1, min(args.e2e_steps, K))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        wanvae.causal_conv3d(x_dev, w, b, y=y)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        x_dev.copy_(x_host, non_blocking=True)
+        wanvae.causal_conv3d(x_dev, w, b, y=y)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_value = replica_throughput(M, ws, E, max_over_ranks(e0.elapsed_time(e1), ws, dev))
+
+    peaks = load_peaks()
+    flop = 2.0 * k ** 3 * ci * co * M                    # useful work (the padded N is not counted)
+    nbytes = (ci + co) * 2.0 * M + w.numel() * 2.0 + co * 4.0  # read x once, write y once
+    tflops = flop / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+              "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"], "flop_per_launch": flop}
+    hbm = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": nbytes}
+    main, other = (tensor, hbm) if flop / nbytes >= ridge else (hbm, tensor)
+    main.update({"kernel": "conv3d_tcgen05_kernel", "traffic": None,
+                 "peak_source": peaks["source"] + (" bf16 burst" if main is tensor else " HBM copy"),
+                 "arith_intensity_flop_per_byte": flop / nbytes, "ridge_flop_per_byte": ridge})
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": "CausalConv3d voxels/s (roofline: the bound its arithmetic intensity sets)",
+        "value": value, "unit": "voxels/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(name, B, T, H, W, ci, co, ws),
+        "roofline": main, "roofline_other": other,
+        "e2e": {"value": e2e_value, "unit": "voxels/s", "h2d_bytes_per_step": x.numel() * 2,
+                "d2h_bytes_per_step": y.numel() * 2, "steps": E},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        import oracle
+        # The oracle on the first frames of the clip over as many rows as fit ~10 s.
+        xs = x_cpu[:, :min(T, 3)]
+        t0 = time.perf_counter()
+        oracle.causal_conv3d(xs[:, :, :1], w_cpu, b_cpu)
+        t1 = max(time.perf_counter() - t0, 1e-3)
+        rows = int(max(1, min(H, 10.0 / t1)))
+        t0 = time.perf_counter()
+        oracle.causal_conv3d(xs[:, :, :rows], w_cpu, b_cpu)
+        dt = time.perf_counter() - t0
+        vox = xs.shape[0] * xs.shape[1] * rows * W
+        line["cpu_baseline"] = {"value": vox / dt, "unit": "voxels/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"the clip's first {xs.shape[1]} frames over {rows} "
+                                          f"of {H} rows x {W} columns: {vox} voxels in {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
 
 
 def bench_ours(args):
@@ -420,6 +592,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         bench_reference(args)
+    elif args.workload in ("conv_in_latent", "post_quant_latent", "conv_out_fullres"):
+        bench_conv(args)
     else:
         bench_ours(args)
 

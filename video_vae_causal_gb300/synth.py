@@ -23,6 +23,16 @@ WORKLOADS = {
     "fullres_96": ((1, 81, 480, 832), 96, 96, 0),
 }
 
+# The decoder's boundary convs, as single CausalConv3d calls:
+# (name, (B, T, H, W), c_in, c_out, k).  conv_in lifts the 16-channel latent
+# to 384 channels, post_quant_conv is the pointwise 16 -> 16 before it, and
+# conv_out maps the 96-channel full-resolution features to RGB.
+CONV_WORKLOADS = {
+    "conv_in_latent": ((1, 21, 60, 104), 16, 384, 3),
+    "post_quant_latent": ((1, 21, 60, 104), 16, 16, 1),
+    "conv_out_fullres": ((1, 81, 480, 832), 96, 3, 3),
+}
+
 
 def _uniform(g, shape, lo, hi, device):
     return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
@@ -57,6 +67,20 @@ def make_resblock_inputs(dims, c_in, c_out, seed=0, device="cpu", shortcut=None)
     x = torch.randn((B, T, H, W, c_in), generator=g, device=device,
                     dtype=torch.float32).to(torch.bfloat16)
     return x, make_params(c_in, c_out, g, device=device, shortcut=shortcut)
+
+
+def make_conv_inputs(dims, c_in, c_out, k, seed=0, device="cpu"):
+    """x [B,T,H,W,c_in] bf16 ~ N(0,1), w [c_out,k,k,k,c_in] bf16 ~ U(+-1/sqrt(fan_in)),
+    bias fp32 ~ U(-0.1, 0.1), drawn in that order from one seeded generator."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, T, H, W = dims
+    x = torch.randn((B, T, H, W, c_in), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    bound = 1.0 / math.sqrt(k * k * k * c_in)
+    w = _uniform(g, (c_out, k, k, k, c_in), -bound, bound, device).to(torch.bfloat16)
+    b = _uniform(g, (c_out,), -0.1, 0.1, device)
+    return x, w, b
 
 
 def make_tensor(shape, seed=0, device="cpu", dtype=torch.bfloat16, kind="normal", lo=-1.0, hi=1.0):
