@@ -112,11 +112,21 @@ NARROW_CASES = [
     (2, 2, 9, 15, 32, 1),
     (1, 3, 32, 32, 64, 13),     # whole 16x16 patches (wide halo tiles)
     (1, 2, 16, 24, 128, 8),
+    (2, 4, 17, 33, 48, 4),      # 16-channel weight sub-tiles, ragged patches, two clips
+    (1, 2, 16, 16, 16, 2),
 ]
 
 
+@pytest.fixture(params=["stencil", "gemm"])
+def narrow_path(request, monkeypatch):
+    """Layers with c_out <= 4 and k=3 run as one GEMM over all taps plus a
+    stencil sum unless WANVAE_CONV_NARROW=0 sends them to the implicit GEMM."""
+    monkeypatch.setenv("WANVAE_CONV_NARROW", "1" if request.param == "stencil" else "0")
+    return request.param
+
+
 @pytest.mark.parametrize("case", NARROW_CASES)
-def test_conv3d_k3_narrow_output(cuda_lib, case, variant):
+def test_conv3d_k3_narrow_output(cuda_lib, case, variant, narrow_path):
     B, T, H, W, ci, co = case
     x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=70 + sum(case))
     y = cuda_lib.causal_conv3d(x.to(DEV), w.to(DEV), b.to(DEV))
@@ -124,7 +134,7 @@ def test_conv3d_k3_narrow_output(cuda_lib, case, variant):
     compare(to_f64(y), oracle.causal_conv3d(x, w, b), what=f"conv3 narrow {case}")
 
 
-def test_conv3d_narrow_with_cache_and_k1(cuda_lib, variant):
+def test_conv3d_narrow_with_cache_and_k1(cuda_lib, variant, narrow_path):
     B, T, H, W, ci, co = 1, 2, 9, 14, 64, 3
     x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=80)
     cache = synth.make_tensor((B, 2, H, W, ci), seed=81)

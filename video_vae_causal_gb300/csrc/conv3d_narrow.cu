@@ -1,0 +1,339 @@
+// conv3d_narrow.cu -- CausalConv3d k=3 for very narrow outputs (c_out <= 4:
+// the decoder's conv_out from 96 channels to RGB, "Sharding of WAN 2.2 VAE",
+// decoder tree).
+//
+// As an implicit GEMM with N = c_out, every MMA would carry 3 useful columns
+// of at least 16 and the 27 shifted taps would need 27 MMAs per k-step: the
+// issue rate, not the math, would bound it.  Instead the taps go into N:
+//
+//   Z_f[p, (o, kt, kh, kw)] = sum_c a_f[p, c] * W[o, kt, kh, kw, c]
+//
+// is one dense GEMM per input frame f over the halo pixels p of a 16 x 16
+// patch (M = 18 x 18 = 324 pixels in three 128-row tiles, N = 27 c_out padded
+// to 16, K = c_in), and the conv is the stencil sum
+//
+//   y_t[q, o] = b[o] + sum_{kt,kh,kw} Z_{t-2+kt}[q + (kh, kw), (o, kt, kh, kw)]
+//
+// over the three input frames that output frame t reads.  A CTA owns one
+// patch and marches along T: each input frame is loaded once (one TMA halo
+// box), multiplied once, and its Z adds into the three output frames it
+// feeds (running sums in registers); an output frame is stored as soon as
+// its last input frame (kt = 2) is in.  Frames before t = 0 are the causal
+// zeros (skipped) or, with a feat_cache, the cache's two frames.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace wanvae {
+namespace {
+
+constexpr int kThreadsN = 256;           // 8 warps; thread q owns output pixel q of the patch
+constexpr int kHalo = 18;                // halo width and height (16 x 16 patch + the 3x3 window)
+constexpr int kHaloPx = kHalo * kHalo;   // 324 pixels = M rows (three 128-row MMA tiles)
+constexpr uint32_t kPlaneN = kHaloPx * 16;  // one 8-channel plane of the halo, bytes
+constexpr int kZStride = 29;             // floats per pixel row of Z in smem (odd: conflict-free)
+constexpr uint64_t kDrainNsN = 200ull * 1000 * 1000;
+
+struct NarrowArgs {
+    int B, T, H, W, c_in, c_out;
+    int npad;               // MMA N: 27 c_out rounded up to 16
+    int sw;                 // channels per B sub-tile (32 -> 64-B swizzle, 16 -> 32-B)
+    int patches_w, patches_h, num_items;
+    int has_cache;
+    uint32_t off_b, off_z, off_bars;  // shared-memory layout (from the aligned base)
+    uint32_t b_tx;          // bytes of the whole B operand
+    uint32_t halo_tx;       // bytes of one halo load
+    const float *bias;
+    __nv_bfloat16 *out;
+    unsigned *err;
+    uint64_t wait_ns;
+};
+
+// Bars: halo full, MMA done, weights loaded.
+struct NBars {
+    uint32_t base;
+    __device__ uint32_t full() const { return base; }
+    __device__ uint32_t mmad() const { return base + 8; }
+    __device__ uint32_t wld() const { return base + 16; }
+};
+
+template <int CO>
+__global__ void __launch_bounds__(kThreadsN, 1)
+conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
+                     const __grid_constant__ CUtensorMap mapC,
+                     const __grid_constant__ CUtensorMap mapW, const NarrowArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const NBars bars{sbase + p.off_bars};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 32);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_bars + 36);
+    float *zs = reinterpret_cast<float *>(smem + p.off_z);
+
+    if (tid == 0) {
+        mbar_init(bars.full(), 1);
+        mbar_init(bars.mmad(), 1);
+        mbar_init(bars.wld(), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&mapX);
+        tma_prefetch_desc(&mapW);
+        if (p.has_cache) tma_prefetch_desc(&mapC);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{p.wait_ns, p.err, abort_flag};
+
+    // The whole B operand (27 c_out rows, rows up to npad read as zeros) once.
+    const uint32_t row_b = (uint32_t)p.sw * 2u;
+    const uint32_t bsub = (uint32_t)p.npad * row_b;  // one sw-channel sub-tile of B
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bars.wld(), p.b_tx);
+        for (int s = 0; s < p.c_in / p.sw; ++s)
+            tma_load_2d(sbase + p.off_b + (uint32_t)s * bsub, &mapW, bars.wld(), s * p.sw, 0);
+    }
+    bool ok = mbar_wait_warp(bars.wld(), 0u, wc);
+    ok = !bar_any(1, kThreadsN, !ok);
+
+    const uint32_t idesc = idesc_bf16_f32(128, p.npad);
+    const uint32_t layout = p.sw == 32 ? kLayoutSw64 : kLayoutSw32;
+    const uint64_t bdesc = sdesc_kmajor(sbase + p.off_b, row_b, layout);
+    const int ksteps = p.c_in / 16, kk_per_sub = p.sw / 16;
+    const int qh = tid >> 4, qw = tid & 15;       // this thread's output pixel in the patch
+    const int qd = warp & 3, jw = warp >> 2;       // TMEM lane quarter; first M tile copied
+    const int f0 = p.has_cache ? -2 : 0;
+    uint32_t ph_full = 0, ph_mma = 0;
+    int pending_full = 0;                          // halo loads issued but not waited for
+    int pending_mma = 0;                           // MMAs committed but not waited for
+
+    // halo load of frame f (f < 0: cache frame f + 2) into the halo buffer
+    auto load_halo = [&](int b, int f, int h0, int w0) {
+        mbar_arrive_expect_tx(bars.full(), p.halo_tx);
+        const CUtensorMap *m = f < 0 ? &mapC : &mapX;
+        const int frame = f < 0 ? b * 2 + f + 2 : b * p.T + f;
+        asm volatile(
+            "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(sbase),
+            "l"(reinterpret_cast<uint64_t>(m)), "r"(bars.full()), "r"(0), "r"(w0 - 1),
+            "r"(h0 - 1), "r"(0), "r"(frame)
+            : "memory");
+    };
+
+    for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+        const int per_clip = p.patches_h * p.patches_w;
+        const int b = item / per_clip, pr = item - b * per_clip;
+        const int h0 = (pr / p.patches_w) * 16, w0 = (pr % p.patches_w) * 16;
+        float cur[CO], nxt[CO], nx2[CO];  // output frames f, f+1, f+2
+#pragma unroll
+        for (int o = 0; o < CO; ++o) cur[o] = nxt[o] = nx2[o] = 0.f;
+        if (tid == 0) load_halo(b, f0, h0, w0);
+        pending_full = 1;
+        for (int f = f0; f < p.T; ++f) {
+            // halo of frame f in shared memory
+            ok = mbar_wait_warp(bars.full(), ph_full, wc);
+            if (bar_any(1, kThreadsN, !ok)) {
+                ok = false;
+                break;
+            }
+            ph_full ^= 1u;
+            pending_full = 0;
+            tc_fence_after();
+            if (tid == 0) {
+                // Z_f for the three 128-row tiles of the halo: A rows are
+                // consecutive halo pixels (16 B each within a plane), K planes
+                // one plane apart.
+                const uint64_t a0 = sdesc_plain(sbase, kPlaneN, 128u);
+                for (int j = 0; j < 3; ++j) {
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const int s = ks / kk_per_sub, kk = ks - s * kk_per_sub;
+                        const uint64_t ad =
+                            a0 + (uint64_t)((j * 128 * 16 + ks * 2 * (int)kPlaneN) >> 4);
+                        const uint64_t bd =
+                            bdesc + (uint64_t)(((uint32_t)s * bsub + (uint32_t)kk * 32u) >> 4);
+                        mma_bf16_ss(tmem + (uint32_t)(j * p.npad), ad, bd, idesc,
+                                    ks > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bars.mmad());
+            }
+            pending_mma = 1;
+            ok = mbar_wait_warp(bars.mmad(), ph_mma, wc);
+            if (bar_any(1, kThreadsN, !ok)) {
+                ok = false;
+                break;
+            }
+            ph_mma ^= 1u;
+            pending_mma = 0;
+            tc_fence_after();
+            // the halo buffer is free: fetch the next frame while Z is reduced
+            if (tid == 0 && f + 1 < p.T) load_halo(b, f + 1, h0, w0);
+            pending_full = f + 1 < p.T ? 1 : 0;
+#pragma unroll
+            for (int o = 0; o < CO; ++o) {
+                // Z columns (o, 0..26) of every halo pixel -> shared memory
+                for (int j = jw; j < 3; j += 2) {
+                    uint32_t r[32];
+                    tmem_ld_cols(tmem + ((uint32_t)(qd * 32) << 16) +
+                                     (uint32_t)(j * p.npad + o * 27),
+                                 32, r);
+                    const int px = j * 128 + qd * 32 + lane;
+                    if (px < kHaloPx) {
+#pragma unroll
+                        for (int c = 0; c < 27; ++c)
+                            zs[px * kZStride + c] = __uint_as_float(r[c]);
+                    }
+                }
+                __syncthreads();
+                // the 3x3 spatial stencil for each temporal tap
+                const float *zq = zs + (qh * kHalo + qw) * kZStride;
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+                    for (int kw = 0; kw < 3; ++kw) {
+                        const float *z = zq + (kh * kHalo + kw) * kZStride + kh * 3 + kw;
+                        s0 += z[0];   // kt = 0: output frame f + 2
+                        s1 += z[9];   // kt = 1: output frame f + 1
+                        s2 += z[18];  // kt = 2: output frame f
+                    }
+                cur[o] += s2;
+                nxt[o] += s1;
+                nx2[o] += s0;
+                __syncthreads();  // z is rewritten by the next output channel
+            }
+            tc_fence_before();
+            if (f >= 0) {
+                const int h = h0 + qh, w = w0 + qw;
+                if (h < p.H && w < p.W) {
+                    __nv_bfloat16 *y =
+                        p.out + ((((int64_t)b * p.T + f) * p.H + h) * p.W + w) * CO;
+#pragma unroll
+                    for (int o = 0; o < CO; ++o)
+                        y[o] = __float2bfloat16_rn(cur[o] + (p.bias ? p.bias[o] : 0.f));
+                }
+            }
+#pragma unroll
+            for (int o = 0; o < CO; ++o) {
+                cur[o] = nxt[o];
+                nxt[o] = nx2[o];
+                nx2[o] = 0.f;
+            }
+        }
+    }
+    // Aborted: let a halo load in flight land and committed MMAs finish before
+    // the CTA's shared memory and TMEM go away.
+    if (!ok && tid == 0) {
+        volatile int no_abort = 0;
+        const WaitCtl dc{kDrainNsN, p.err, &no_abort};
+        if (pending_full) mbar_wait(bars.full(), ph_full, dc);
+        if (pending_mma) mbar_wait(bars.mmad(), ph_mma, dc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int CO>
+cudaError_t launch_narrow(const NarrowArgs &a, const CUtensorMap &mX, const CUtensorMap &mC,
+                          const CUtensorMap &mW, uint32_t smem, const LaunchCtx &ctx) {
+    auto kern = conv3d_narrow_kernel<CO>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = a.num_items < ctx.num_sms ? a.num_items : ctx.num_sms;
+    kern<<<grid, kThreadsN, smem, ctx.stream>>>(mX, mC, mW, a);
+    return cudaGetLastError();
+}
+
+// WANVAE_CONV_NARROW=0 routes narrow layers to the implicit-GEMM kernel.
+bool narrow_enabled() {
+    const char *e = getenv("WANVAE_CONV_NARROW");
+    return !(e && e[0] == '0' && e[1] == 0);
+}
+
+}  // namespace
+
+int conv3d_narrow_supported(const ConvSpec &s) {
+    if (!narrow_enabled()) return -1;
+    if (s.k != 3 || s.c_out < 1 || s.c_out > 4 || s.sc_in || s.epi != kEpiBias) return -1;
+    if (s.c_in < 16 || s.c_in % 16 || s.c_in > 128) return -1;
+    return 0;
+}
+
+cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx) {
+    NarrowArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = s.B;
+    a.T = s.T;
+    a.H = s.H;
+    a.W = s.W;
+    a.c_in = s.c_in;
+    a.c_out = s.c_out;
+    a.npad = (27 * s.c_out + 15) / 16 * 16;
+    a.sw = s.c_in % 32 == 0 ? 32 : 16;
+    a.patches_w = (s.W + 15) / 16;
+    a.patches_h = (s.H + 15) / 16;
+    a.num_items = s.B * a.patches_w * a.patches_h;
+    a.has_cache = s.cache != nullptr;
+    // Shared memory: halo planes (+ slack: the third 128-row tile reads 60
+    // rows past the halo's 324 pixels, garbage rows whose results are never
+    // used), B, Z, barriers.
+    const uint32_t halo_bytes = (uint32_t)(s.c_in / 8) * kPlaneN;
+    const uint32_t halo_alloc = (halo_bytes + 1024u + 1023u) & ~1023u;
+    a.halo_tx = halo_bytes;
+    a.off_b = halo_alloc;
+    a.b_tx = (uint32_t)a.npad * (uint32_t)s.c_in * 2u;
+    a.off_z = (a.off_b + a.b_tx + 1023u) & ~1023u;
+    a.off_bars = (a.off_z + (uint32_t)(kHaloPx * kZStride * 4) + 15u) & ~15u;
+    uint32_t smem = 1024u + a.off_bars + 64u;
+    if (smem < 120u * 1024u) smem = 120u * 1024u;  // one CTA per SM (it holds 512 TMEM columns)
+    a.bias = s.bias;
+    a.out = static_cast<__nv_bfloat16 *>(s.out);
+    a.err = ctx.err;
+    a.wait_ns = ctx.wait_ns;
+
+    // NHWC input as (8 channels, W, H, C/8 planes, frames): an 18 x 18 box of
+    // all C channels lands as [C/8][18][18][8] (out-of-frame pixels: zeros).
+    const int frames = s.B * s.T;
+    CUtensorMap mX, mC, mW;
+    memset(&mC, 0, sizeof(mC));
+    cuuint64_t dx[5] = {8, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)(s.c_in / 8),
+                        (cuuint64_t)frames};
+    cuuint64_t sx[4] = {(cuuint64_t)s.c_in * 2, (cuuint64_t)s.W * s.c_in * 2, 16,
+                        (cuuint64_t)s.H * s.W * s.c_in * 2};
+    cuuint32_t bx[5] = {8, kHalo, kHalo, (cuuint32_t)(s.c_in / 8), 1};
+    bool ok = encode_tiled_bf16(&mX, 5, s.in, dx, sx, bx, 0);
+    if (s.cache) {
+        cuuint64_t dc[5] = {dx[0], dx[1], dx[2], dx[3], (cuuint64_t)s.B * 2};
+        ok = ok && encode_tiled_bf16(&mC, 5, s.cache, dc, sx, bx, 0);
+    }
+    // Weights [c_out][27][c_in] = a [27 c_out][c_in] K-major matrix; a box of
+    // npad rows (rows past 27 c_out read as zeros) x sw channels.
+    cuuint64_t dw[2] = {(cuuint64_t)s.c_in, (cuuint64_t)(27 * s.c_out)};
+    cuuint64_t sww[1] = {(cuuint64_t)s.c_in * 2};
+    cuuint32_t bw[2] = {(cuuint32_t)a.sw, (cuuint32_t)a.npad};
+    ok = ok && encode_tiled_bf16(&mW, 2, s.w, dw, sww, bw, a.sw * 2);
+    if (!ok) return cudaErrorInvalidValue;
+    if (!s.cache) mC = mX;
+    switch (s.c_out) {
+        case 1: return launch_narrow<1>(a, mX, mC, mW, smem, ctx);
+        case 2: return launch_narrow<2>(a, mX, mC, mW, smem, ctx);
+        case 3: return launch_narrow<3>(a, mX, mC, mW, smem, ctx);
+        case 4: return launch_narrow<4>(a, mX, mC, mW, smem, ctx);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace wanvae

@@ -137,14 +137,6 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
 // 16 bytes) apart, K-planes one plane apart -- a no-swizzle K-major operand.
 constexpr uint32_t kHaloH = 18;
 
-__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1u << 46;
-    return d;  // swizzle mode 0: none
-}
 
 // First temporal tap of a work unit (one tile, or the two tiles of a CTA
 // pair, which share every B stage and so run the same taps): taps reading
@@ -691,51 +683,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Named-barrier OR-reduction: true in every participating thread if `pred`
-// was true in any of them.
-__device__ __forceinline__ bool bar_any(int id, int nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred q, p;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
-// Two x16 TMEM loads under one wait (32 columns), or one (16 columns).
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, int ncols, uint32_t (&r)[32]) {
-    if (ncols >= 32) {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-            "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-              "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
-              "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-              "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr), "r"(taddr + 16u));
-        asm volatile("tcgen05.wait::ld.sync.aligned;"
-                     : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                       "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                       "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
-                       "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                       "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
-                       "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-                     :
-                     : "memory");
-    } else {
-        uint32_t (&h)[16] = *reinterpret_cast<uint32_t (*)[16]>(&r[0]);
-        tmem_ld16(taddr, h);
-    }
-}
-
 // Where the 32 rows of one epilogue warp live in the output: consecutive
 // voxels (im2col tiles; rows past the frame's end are invalid), or four patch
 // rows of 8 pixels one frame row (W voxels) apart (halo tiles; rows and
@@ -851,8 +798,10 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 tmem_ld_cols(tb, 16, r);
                 if (valid) {
                     __nv_bfloat16 *o = p.out + g * p.c_out;
-                    for (int c = 0; c < p.c_out; ++c)
-                        o[c] = __float2bfloat16_rn(__uint_as_float(r[c]) + s_bias[c]);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)  // constant indexes keep r in registers
+                        if (c < p.c_out)
+                            o[c] = __float2bfloat16_rn(__uint_as_float(r[c]) + s_bias[c]);
                 }
             }
         } else if (p.epi == kEpiNormSilu) {
@@ -1668,7 +1617,22 @@ int conv3d_supported(const ConvSpec &s) {
     return pick_plan(s, pl, 2) ? 0 : -1;
 }
 
+bool encode_tiled_bf16(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims,
+                       const cuuint64_t *strides, const cuuint32_t *box, int swizzle_bytes) {
+    if (!load_encoders()) return false;
+    const CUtensorMapSwizzle sz = swizzle_bytes == 128   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                          const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
+    if (conv3d_narrow_supported(s) == 0) return launch_conv3d_narrow(s, ctx);
     Plan pl;
     if (!pick_plan(s, pl, pair_choice())) return cudaErrorInvalidValue;
     if (!load_encoders()) return cudaErrorInvalidValue;

@@ -2,6 +2,7 @@
 // kernels (rmsnorm_silu.cu, conv3d_tcgen05.cu).  Not installed, not exported.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -62,5 +63,17 @@ int conv3d_supported(const ConvSpec &s);
 // Enqueue the conv; returns a cudaError_t (cudaErrorInvalidValue when a
 // tensor map cannot be encoded).
 cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx);
+
+// The k=3 conv for very narrow outputs (c_out <= 4, a decoder's conv_out to
+// RGB) as one GEMM over all 27 taps at once plus a 3x3x3 stencil sum
+// (conv3d_narrow.cu).  conv3d_narrow_supported returns 0 when it applies.
+int conv3d_narrow_supported(const ConvSpec &s);
+cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx);
+
+// cuTensorMapEncodeTiled for a bf16 tensor of `rank` dimensions (driver
+// entry point looked up once); swizzle_bytes 0, 32, 64 or 128.  False when
+// the entry point is missing or the encoding is rejected.
+bool encode_tiled_bf16(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims,
+                       const cuuint64_t *strides, const cuuint32_t *box, int swizzle_bytes);
 
 }  // namespace wanvae
