@@ -1,4 +1,4 @@
-// conv3d_narrow.cu -- CausalConv3d k=3 for very narrow outputs (c_out <= 4:
+// conv3d_narrow.cu -- CausalConv3d k=3 for very narrow outputs (c_out <= 3:
 // the decoder's conv_out from 96 channels to RGB, "Sharding of WAN 2.2 VAE",
 // decoder tree).
 //
@@ -34,7 +34,6 @@ constexpr int kThreadsN = 256;           // 8 warps; thread q owns output pixel 
 constexpr int kHalo = 18;                // halo width and height (16 x 16 patch + the 3x3 window)
 constexpr int kHaloPx = kHalo * kHalo;   // 324 pixels = M rows (three 128-row MMA tiles)
 constexpr uint32_t kPlaneN = kHaloPx * 16;  // one 8-channel plane of the halo, bytes
-constexpr int kZStride = 29;             // floats per pixel row of Z in smem (odd: conflict-free)
 constexpr uint64_t kDrainNsN = 200ull * 1000 * 1000;
 
 struct NarrowArgs {
@@ -116,6 +115,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
     uint32_t ph_full = 0, ph_mma = 0;
     int pending_full = 0;                          // halo loads issued but not waited for
     int pending_mma = 0;                           // MMAs committed but not waited for
+    int lost_full = -1;  // thread 0: phase of a halo load whose wait gave up (still in flight)
 
     // halo load of frame f (f < 0: cache frame f + 2) into the halo buffer
     auto load_halo = [&](int b, int f, int h0, int w0) {
@@ -130,6 +130,41 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
             : "memory");
     };
 
+    constexpr int kZS = (27 * CO) | 1;  // floats per halo pixel of Z in smem (odd: conflict-free)
+    // Z of one input frame, all c_out x 27 columns of every halo pixel:
+    // TMEM -> shared memory, so TMEM is free for the next frame's MMAs.
+    auto copy_z = [&]() {
+        for (int j = jw; j < 3; j += 2) {
+            const int px = j * 128 + qd * 32 + lane;
+#pragma unroll
+            for (int c0 = 0; c0 < 27 * CO; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_cols(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(j * p.npad + c0), 32,
+                             r);
+                if (px < kHaloPx) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (c0 + c < 27 * CO) zs[px * kZS + c0 + c] = __uint_as_float(r[c]);
+                }
+            }
+        }
+    };
+    auto issue_mma = [&]() {
+        // Z_f for the three 128-row tiles of the halo: A rows are consecutive
+        // halo pixels (16 B each within a plane), K planes one plane apart.
+        const uint64_t a0 = sdesc_plain(sbase, kPlaneN, 128u);
+        for (int j = 0; j < 3; ++j) {
+            for (int ks = 0; ks < ksteps; ++ks) {
+                const int s = ks / kk_per_sub, kk = ks - s * kk_per_sub;
+                const uint64_t ad = a0 + (uint64_t)((j * 128 * 16 + ks * 2 * (int)kPlaneN) >> 4);
+                const uint64_t bd =
+                    bdesc + (uint64_t)(((uint32_t)s * bsub + (uint32_t)kk * 32u) >> 4);
+                mma_bf16_ss(tmem + (uint32_t)(j * p.npad), ad, bd, idesc, ks > 0 ? 1u : 0u);
+            }
+        }
+        mma_commit(bars.mmad());
+    };
+
     for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
         const int per_clip = p.patches_h * p.patches_w;
         const int b = item / per_clip, pr = item - b * per_clip;
@@ -137,72 +172,55 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
         float cur[CO], nxt[CO], nx2[CO];  // output frames f, f+1, f+2
 #pragma unroll
         for (int o = 0; o < CO; ++o) cur[o] = nxt[o] = nx2[o] = 0.f;
+        // Prologue: Z of the first input frame into shared memory.
         if (tid == 0) load_halo(b, f0, h0, w0);
         pending_full = 1;
+        ok = mbar_wait_warp(bars.full(), ph_full, wc);
+        if (bar_any(1, kThreadsN, !ok)) {
+            ok = false;
+            break;
+        }
+        ph_full ^= 1u;
+        pending_full = 0;
+        tc_fence_after();
+        if (tid == 0) issue_mma();
+        pending_mma = 1;
+        ok = mbar_wait_warp(bars.mmad(), ph_mma, wc);
+        if (bar_any(1, kThreadsN, !ok)) {
+            ok = false;
+            break;
+        }
+        ph_mma ^= 1u;
+        pending_mma = 0;
+        tc_fence_after();
+        if (tid == 0 && f0 + 1 < p.T) load_halo(b, f0 + 1, h0, w0);
+        pending_full = f0 + 1 < p.T ? 1 : 0;
+        copy_z();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
         for (int f = f0; f < p.T; ++f) {
-            // halo of frame f in shared memory
-            ok = mbar_wait_warp(bars.full(), ph_full, wc);
-            if (bar_any(1, kThreadsN, !ok)) {
-                ok = false;
-                break;
-            }
-            ph_full ^= 1u;
-            pending_full = 0;
-            tc_fence_after();
-            if (tid == 0) {
-                // Z_f for the three 128-row tiles of the halo: A rows are
-                // consecutive halo pixels (16 B each within a plane), K planes
-                // one plane apart.
-                const uint64_t a0 = sdesc_plain(sbase, kPlaneN, 128u);
-                for (int j = 0; j < 3; ++j) {
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const int s = ks / kk_per_sub, kk = ks - s * kk_per_sub;
-                        const uint64_t ad =
-                            a0 + (uint64_t)((j * 128 * 16 + ks * 2 * (int)kPlaneN) >> 4);
-                        const uint64_t bd =
-                            bdesc + (uint64_t)(((uint32_t)s * bsub + (uint32_t)kk * 32u) >> 4);
-                        mma_bf16_ss(tmem + (uint32_t)(j * p.npad), ad, bd, idesc,
-                                    ks > 0 ? 1u : 0u);
-                    }
+            const bool next = f + 1 < p.T;
+            // Frame f+1's MMAs run on the tensor core while frame f's stencil
+            // sums run on the CUDA cores (TMEM was emptied into smem).
+            if (next && tid == 0) {
+                if (mbar_wait(bars.full(), ph_full, wc)) {
+                    tc_fence_after();
+                    issue_mma();
+                } else {
+                    lost_full = (int)ph_full;  // the abort flag is up: the wait below gives up
                 }
-                mma_commit(bars.mmad());
             }
-            pending_mma = 1;
-            ok = mbar_wait_warp(bars.mmad(), ph_mma, wc);
-            if (bar_any(1, kThreadsN, !ok)) {
-                ok = false;
-                break;
-            }
-            ph_mma ^= 1u;
-            pending_mma = 0;
-            tc_fence_after();
-            // the halo buffer is free: fetch the next frame while Z is reduced
-            if (tid == 0 && f + 1 < p.T) load_halo(b, f + 1, h0, w0);
-            pending_full = f + 1 < p.T ? 1 : 0;
+            // the 3x3 spatial stencil of Z_f for each temporal tap and channel
+            const float *zq = zs + (qh * kHalo + qw) * kZS;
 #pragma unroll
             for (int o = 0; o < CO; ++o) {
-                // Z columns (o, 0..26) of every halo pixel -> shared memory
-                for (int j = jw; j < 3; j += 2) {
-                    uint32_t r[32];
-                    tmem_ld_cols(tmem + ((uint32_t)(qd * 32) << 16) +
-                                     (uint32_t)(j * p.npad + o * 27),
-                                 32, r);
-                    const int px = j * 128 + qd * 32 + lane;
-                    if (px < kHaloPx) {
-#pragma unroll
-                        for (int c = 0; c < 27; ++c)
-                            zs[px * kZStride + c] = __uint_as_float(r[c]);
-                    }
-                }
-                __syncthreads();
-                // the 3x3 spatial stencil for each temporal tap
-                const float *zq = zs + (qh * kHalo + qw) * kZStride;
                 float s0 = 0.f, s1 = 0.f, s2 = 0.f;
 #pragma unroll
                 for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
                     for (int kw = 0; kw < 3; ++kw) {
-                        const float *z = zq + (kh * kHalo + kw) * kZStride + kh * 3 + kw;
+                        const float *z = zq + (kh * kHalo + kw) * kZS + o * 27 + kh * 3 + kw;
                         s0 += z[0];   // kt = 0: output frame f + 2
                         s1 += z[9];   // kt = 1: output frame f + 1
                         s2 += z[18];  // kt = 2: output frame f
@@ -210,9 +228,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
                 cur[o] += s2;
                 nxt[o] += s1;
                 nx2[o] += s0;
-                __syncthreads();  // z is rewritten by the next output channel
             }
-            tc_fence_before();
             if (f >= 0) {
                 const int h = h0 + qh, w = w0 + qw;
                 if (h < p.H && w < p.W) {
@@ -229,6 +245,25 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
                 nxt[o] = nx2[o];
                 nx2[o] = 0.f;
             }
+            if (!next) break;
+            ph_full ^= 1u;  // frame f+1's halo was consumed by its MMAs
+            pending_full = 0;
+            pending_mma = lost_full < 0 ? 1 : 0;
+            ok = mbar_wait_warp(bars.mmad(), ph_mma, wc);
+            // (the reduction is also the barrier that ends every read of Z_f)
+            if (bar_any(1, kThreadsN, !ok)) {
+                ok = false;
+                break;
+            }
+            ph_mma ^= 1u;
+            pending_mma = 0;
+            tc_fence_after();
+            if (tid == 0 && f + 2 < p.T) load_halo(b, f + 2, h0, w0);
+            pending_full = f + 2 < p.T ? 1 : 0;
+            copy_z();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
         }
     }
     // Aborted: let a halo load in flight land and committed MMAs finish before
@@ -237,6 +272,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
         volatile int no_abort = 0;
         const WaitCtl dc{kDrainNsN, p.err, &no_abort};
         if (pending_full) mbar_wait(bars.full(), ph_full, dc);
+        if (lost_full >= 0) mbar_wait(bars.full(), (uint32_t)lost_full, dc);
         if (pending_mma) mbar_wait(bars.mmad(), ph_mma, dc);
     }
     tc_fence_before();
@@ -267,7 +303,7 @@ bool narrow_enabled() {
 
 int conv3d_narrow_supported(const ConvSpec &s) {
     if (!narrow_enabled()) return -1;
-    if (s.k != 3 || s.c_out < 1 || s.c_out > 4 || s.sc_in || s.epi != kEpiBias) return -1;
+    if (s.k != 3 || s.c_out < 1 || s.c_out > 3 || s.sc_in || s.epi != kEpiBias) return -1;
     if (s.c_in < 16 || s.c_in % 16 || s.c_in > 128) return -1;
     return 0;
 }
@@ -296,7 +332,8 @@ cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx) {
     a.off_b = halo_alloc;
     a.b_tx = (uint32_t)a.npad * (uint32_t)s.c_in * 2u;
     a.off_z = (a.off_b + a.b_tx + 1023u) & ~1023u;
-    a.off_bars = (a.off_z + (uint32_t)(kHaloPx * kZStride * 4) + 15u) & ~15u;
+    const uint32_t zs_floats = (uint32_t)((27 * s.c_out) | 1);
+    a.off_bars = (a.off_z + (uint32_t)kHaloPx * zs_floats * 4u + 15u) & ~15u;
     uint32_t smem = 1024u + a.off_bars + 64u;
     if (smem < 120u * 1024u) smem = 120u * 1024u;  // one CTA per SM (it holds 512 TMEM columns)
     a.bias = s.bias;
@@ -331,7 +368,6 @@ cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx) {
         case 1: return launch_narrow<1>(a, mX, mC, mW, smem, ctx);
         case 2: return launch_narrow<2>(a, mX, mC, mW, smem, ctx);
         case 3: return launch_narrow<3>(a, mX, mC, mW, smem, ctx);
-        case 4: return launch_narrow<4>(a, mX, mC, mW, smem, ctx);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -64,7 +64,7 @@ int conv3d_supported(const ConvSpec &s);
 // tensor map cannot be encoded).
 cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx);
 
-// The k=3 conv for very narrow outputs (c_out <= 4, a decoder's conv_out to
+// The k=3 conv for very narrow outputs (c_out <= 3, a decoder's conv_out to
 // RGB) as one GEMM over all 27 taps at once plus a 3x3x3 stencil sum
 // (conv3d_narrow.cu).  conv3d_narrow_supported returns 0 when it applies.
 int conv3d_narrow_supported(const ConvSpec &s);
