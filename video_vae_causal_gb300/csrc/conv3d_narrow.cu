@@ -16,7 +16,8 @@
 //
 // over the three input frames that output frame t reads.  A CTA owns one
 // patch and marches along T: each input frame is loaded once (one TMA halo
-// box), multiplied once, and its Z adds into the three output frames it
+// box per 64- or 32-channel chunk, 128-/64-byte swizzled rows of one pixel
+// each), multiplied once, and its Z adds into the three output frames it
 // feeds (running sums in registers); an output frame is stored as soon as
 // its last input frame (kt = 2) is in.  Frames before t = 0 are the causal
 // zeros (skipped) or, with a feat_cache, the cache's two frames.
@@ -33,16 +34,18 @@ namespace {
 constexpr int kThreadsN = 256;           // 8 warps; thread q owns output pixel q of the patch
 constexpr int kHalo = 18;                // halo width and height (16 x 16 patch + the 3x3 window)
 constexpr int kHaloPx = kHalo * kHalo;   // 324 pixels = M rows (three 128-row MMA tiles)
-constexpr uint32_t kPlaneN = kHaloPx * 16;  // one 8-channel plane of the halo, bytes
+constexpr int kHaloRows = 328;           // halo rows in smem: the third M tile (rows 200..327)
+                                         // reads 4 slack rows past the 324 pixels
 constexpr uint64_t kDrainNsN = 200ull * 1000 * 1000;
 
 struct NarrowArgs {
     int B, T, H, W, c_in, c_out;
     int npad;               // MMA N: 27 c_out rounded up to 16
-    int sw;                 // channels per B sub-tile (32 -> 64-B swizzle, 16 -> 32-B)
+    int nch;                // channel chunks: 64 channels each, then a last one of 32
     int patches_w, patches_h, num_items;
     int has_cache;
-    uint32_t off_b, off_z, off_bars;  // shared-memory layout (from the aligned base)
+    uint32_t off_a0, off_a1, off_b0, off_b1;  // per chunk (at most two): halo rows, B rows
+    uint32_t off_z, off_bars;
     uint32_t b_tx;          // bytes of the whole B operand
     uint32_t halo_tx;       // bytes of one halo load
     const float *bias;
@@ -59,11 +62,24 @@ struct NBars {
     __device__ uint32_t wld() const { return base + 16; }
 };
 
+// First halo pixel of each 128-row M tile (the third overlaps the second so
+// that it needs only 4 slack rows).
+__device__ __forceinline__ int tile_row(int j) { return j == 0 ? 0 : (j == 1 ? 128 : 200); }
+
+// Chunk k holds channels [64 k, 64 k + width): width 64 (128-B rows, 128-B
+// swizzle) except a last chunk of 32 (64-B rows, 64-B swizzle).
+__device__ __forceinline__ int chunk_w(const NarrowArgs &p, int k) {
+    return (k == p.nch - 1 && p.c_in % 64) ? 32 : 64;
+}
+
 template <int CO>
 __global__ void __launch_bounds__(kThreadsN, 1)
-conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
-                     const __grid_constant__ CUtensorMap mapC,
-                     const __grid_constant__ CUtensorMap mapW, const NarrowArgs p) {
+conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX64,
+                     const __grid_constant__ CUtensorMap mapX32,
+                     const __grid_constant__ CUtensorMap mapC64,
+                     const __grid_constant__ CUtensorMap mapC32,
+                     const __grid_constant__ CUtensorMap mapW64,
+                     const __grid_constant__ CUtensorMap mapW32, const NarrowArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -80,9 +96,10 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
         mbar_init(bars.wld(), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&mapX);
-        tma_prefetch_desc(&mapW);
-        if (p.has_cache) tma_prefetch_desc(&mapC);
+        tma_prefetch_desc(&mapX64);
+        tma_prefetch_desc(&mapX32);
+        tma_prefetch_desc(&mapW64);
+        tma_prefetch_desc(&mapW32);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -95,20 +112,16 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
     const WaitCtl wc{p.wait_ns, p.err, abort_flag};
 
     // The whole B operand (27 c_out rows, rows up to npad read as zeros) once.
-    const uint32_t row_b = (uint32_t)p.sw * 2u;
-    const uint32_t bsub = (uint32_t)p.npad * row_b;  // one sw-channel sub-tile of B
     if (tid == 0) {
         mbar_arrive_expect_tx(bars.wld(), p.b_tx);
-        for (int s = 0; s < p.c_in / p.sw; ++s)
-            tma_load_2d(sbase + p.off_b + (uint32_t)s * bsub, &mapW, bars.wld(), s * p.sw, 0);
+        for (int k = 0; k < p.nch; ++k)
+            tma_load_2d(sbase + (k == 0 ? p.off_b0 : p.off_b1), chunk_w(p, k) == 64 ? &mapW64 : &mapW32, bars.wld(),
+                        64 * k, 0);
     }
     bool ok = mbar_wait_warp(bars.wld(), 0u, wc);
     ok = !bar_any(1, kThreadsN, !ok);
 
     const uint32_t idesc = idesc_bf16_f32(128, p.npad);
-    const uint32_t layout = p.sw == 32 ? kLayoutSw64 : kLayoutSw32;
-    const uint64_t bdesc = sdesc_kmajor(sbase + p.off_b, row_b, layout);
-    const int ksteps = p.c_in / 16, kk_per_sub = p.sw / 16;
     const int qh = tid >> 4, qw = tid & 15;       // this thread's output pixel in the patch
     const int qd = warp & 3, jw = warp >> 2;       // TMEM lane quarter; first M tile copied
     const int f0 = p.has_cache ? -2 : 0;
@@ -117,17 +130,16 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
     int pending_mma = 0;                           // MMAs committed but not waited for
     int lost_full = -1;  // thread 0: phase of a halo load whose wait gave up (still in flight)
 
-    // halo load of frame f (f < 0: cache frame f + 2) into the halo buffer
+    // halo of frame f (f < 0: cache frame f + 2): one box of 18 x 18 pixels per
+    // channel chunk, one swizzled row per pixel (out-of-frame pixels: zeros)
     auto load_halo = [&](int b, int f, int h0, int w0) {
         mbar_arrive_expect_tx(bars.full(), p.halo_tx);
-        const CUtensorMap *m = f < 0 ? &mapC : &mapX;
         const int frame = f < 0 ? b * 2 + f + 2 : b * p.T + f;
-        asm volatile(
-            "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(sbase),
-            "l"(reinterpret_cast<uint64_t>(m)), "r"(bars.full()), "r"(0), "r"(w0 - 1),
-            "r"(h0 - 1), "r"(0), "r"(frame)
-            : "memory");
+        for (int k = 0; k < p.nch; ++k) {
+            const bool w64 = chunk_w(p, k) == 64;
+            const CUtensorMap *m = f < 0 ? (w64 ? &mapC64 : &mapC32) : (w64 ? &mapX64 : &mapX32);
+            tma_load_4d(sbase + (k == 0 ? p.off_a0 : p.off_a1), m, bars.full(), 64 * k, w0 - 1, h0 - 1, frame);
+        }
     };
 
     constexpr int kZS = (27 * CO) | 1;  // floats per halo pixel of Z in smem (odd: conflict-free)
@@ -135,13 +147,14 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
     // TMEM -> shared memory, so TMEM is free for the next frame's MMAs.
     auto copy_z = [&]() {
         for (int j = jw; j < 3; j += 2) {
-            const int px = j * 128 + qd * 32 + lane;
+            const int px = tile_row(j) + qd * 32 + lane;
+            const bool mine = px < kHaloPx && (j < 2 || px >= 256);  // tile 2 overlaps tile 1
 #pragma unroll
             for (int c0 = 0; c0 < 27 * CO; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld_cols(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(j * p.npad + c0), 32,
                              r);
-                if (px < kHaloPx) {
+                if (mine) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         if (c0 + c < 27 * CO) zs[px * kZS + c0 + c] = __uint_as_float(r[c]);
@@ -150,16 +163,18 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
         }
     };
     auto issue_mma = [&]() {
-        // Z_f for the three 128-row tiles of the halo: A rows are consecutive
-        // halo pixels (16 B each within a plane), K planes one plane apart.
-        const uint64_t a0 = sdesc_plain(sbase, kPlaneN, 128u);
+        // Z_f for the three 128-row tiles of the halo (rows = consecutive halo
+        // pixels), K in 16-channel steps of 32 bytes through each chunk.
         for (int j = 0; j < 3; ++j) {
-            for (int ks = 0; ks < ksteps; ++ks) {
-                const int s = ks / kk_per_sub, kk = ks - s * kk_per_sub;
-                const uint64_t ad = a0 + (uint64_t)((j * 128 * 16 + ks * 2 * (int)kPlaneN) >> 4);
-                const uint64_t bd =
-                    bdesc + (uint64_t)(((uint32_t)s * bsub + (uint32_t)kk * 32u) >> 4);
-                mma_bf16_ss(tmem + (uint32_t)(j * p.npad), ad, bd, idesc, ks > 0 ? 1u : 0u);
+            for (int k = 0; k < p.nch; ++k) {
+                const int cw = chunk_w(p, k);
+                const uint32_t rowb = (uint32_t)cw * 2u, lay = cw == 64 ? kLayoutSw128 : kLayoutSw64;
+                const uint64_t a0 =
+                    sdesc_kmajor(sbase + (k == 0 ? p.off_a0 : p.off_a1) + (uint32_t)tile_row(j) * rowb, rowb, lay);
+                const uint64_t b0 = sdesc_kmajor(sbase + (k == 0 ? p.off_b0 : p.off_b1), rowb, lay);
+                for (int ks = 0; ks < cw / 16; ++ks)
+                    mma_bf16_ss(tmem + (uint32_t)(j * p.npad), a0 + (uint64_t)(2 * ks),
+                                b0 + (uint64_t)(2 * ks), idesc, (k > 0 || ks > 0) ? 1u : 0u);
             }
         }
         mma_commit(bars.mmad());
@@ -282,14 +297,14 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX,
 }
 
 template <int CO>
-cudaError_t launch_narrow(const NarrowArgs &a, const CUtensorMap &mX, const CUtensorMap &mC,
-                          const CUtensorMap &mW, uint32_t smem, const LaunchCtx &ctx) {
+cudaError_t launch_narrow(const NarrowArgs &a, const CUtensorMap *m, uint32_t smem,
+                          const LaunchCtx &ctx) {
     auto kern = conv3d_narrow_kernel<CO>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = a.num_items < ctx.num_sms ? a.num_items : ctx.num_sms;
-    kern<<<grid, kThreadsN, smem, ctx.stream>>>(mX, mC, mW, a);
+    kern<<<grid, kThreadsN, smem, ctx.stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
     return cudaGetLastError();
 }
 
@@ -304,7 +319,7 @@ bool narrow_enabled() {
 int conv3d_narrow_supported(const ConvSpec &s) {
     if (!narrow_enabled()) return -1;
     if (s.k != 3 || s.c_out < 1 || s.c_out > 3 || s.sc_in || s.epi != kEpiBias) return -1;
-    if (s.c_in < 16 || s.c_in % 16 || s.c_in > 128) return -1;
+    if (s.c_in < 32 || s.c_in % 32 || s.c_in > 128) return -1;
     return 0;
 }
 
@@ -318,20 +333,27 @@ cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx) {
     a.c_in = s.c_in;
     a.c_out = s.c_out;
     a.npad = (27 * s.c_out + 15) / 16 * 16;
-    a.sw = s.c_in % 32 == 0 ? 32 : 16;
+    a.nch = (s.c_in + 63) / 64;
     a.patches_w = (s.W + 15) / 16;
     a.patches_h = (s.H + 15) / 16;
     a.num_items = s.B * a.patches_w * a.patches_h;
     a.has_cache = s.cache != nullptr;
-    // Shared memory: halo planes (+ slack: the third 128-row tile reads 60
-    // rows past the halo's 324 pixels, garbage rows whose results are never
-    // used), B, Z, barriers.
-    const uint32_t halo_bytes = (uint32_t)(s.c_in / 8) * kPlaneN;
-    const uint32_t halo_alloc = (halo_bytes + 1024u + 1023u) & ~1023u;
-    a.halo_tx = halo_bytes;
-    a.off_b = halo_alloc;
+    // Shared memory per chunk: 328 halo rows and npad B rows of the chunk's
+    // width (1024-aligned: the swizzle atoms), then Z and the barriers.
+    uint32_t off = 0;
+    for (int k = 0; k < a.nch; ++k) {
+        const uint32_t rowb = (k == a.nch - 1 && s.c_in % 64) ? 64u : 128u;
+        (k == 0 ? a.off_a0 : a.off_a1) = off;
+        off += ((uint32_t)kHaloRows * rowb + 1023u) & ~1023u;
+    }
+    for (int k = 0; k < a.nch; ++k) {
+        const uint32_t rowb = (k == a.nch - 1 && s.c_in % 64) ? 64u : 128u;
+        (k == 0 ? a.off_b0 : a.off_b1) = off;
+        off += ((uint32_t)a.npad * rowb + 1023u) & ~1023u;
+    }
+    a.halo_tx = (uint32_t)kHaloPx * (uint32_t)s.c_in * 2u;
     a.b_tx = (uint32_t)a.npad * (uint32_t)s.c_in * 2u;
-    a.off_z = (a.off_b + a.b_tx + 1023u) & ~1023u;
+    a.off_z = off;
     const uint32_t zs_floats = (uint32_t)((27 * s.c_out) | 1);
     a.off_bars = (a.off_z + (uint32_t)kHaloPx * zs_floats * 4u + 15u) & ~15u;
     uint32_t smem = 1024u + a.off_bars + 64u;
@@ -341,33 +363,46 @@ cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx) {
     a.err = ctx.err;
     a.wait_ns = ctx.wait_ns;
 
-    // NHWC input as (8 channels, W, H, C/8 planes, frames): an 18 x 18 box of
-    // all C channels lands as [C/8][18][18][8] (out-of-frame pixels: zeros).
+    // NHWC input as (C, W, H, frames); boxes of 64 or 32 channels x 18 x 18
+    // pixels land as one swizzled row per pixel.  Weights [c_out][27][c_in] =
+    // a [27 c_out][c_in] K-major matrix; boxes of npad rows (rows past 27 c_out
+    // read as zeros).  Maps: X64, X32, C64, C32, W64, W32 (unused ones repeat
+    // a valid one).
     const int frames = s.B * s.T;
-    CUtensorMap mX, mC, mW;
-    memset(&mC, 0, sizeof(mC));
-    cuuint64_t dx[5] = {8, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)(s.c_in / 8),
-                        (cuuint64_t)frames};
-    cuuint64_t sx[4] = {(cuuint64_t)s.c_in * 2, (cuuint64_t)s.W * s.c_in * 2, 16,
+    CUtensorMap m[6];
+    memset(m, 0, sizeof(m));
+    cuuint64_t dx[4] = {(cuuint64_t)s.c_in, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)frames};
+    cuuint64_t sx[3] = {(cuuint64_t)s.c_in * 2, (cuuint64_t)s.W * s.c_in * 2,
                         (cuuint64_t)s.H * s.W * s.c_in * 2};
-    cuuint32_t bx[5] = {8, kHalo, kHalo, (cuuint32_t)(s.c_in / 8), 1};
-    bool ok = encode_tiled_bf16(&mX, 5, s.in, dx, sx, bx, 0);
-    if (s.cache) {
-        cuuint64_t dc[5] = {dx[0], dx[1], dx[2], dx[3], (cuuint64_t)s.B * 2};
-        ok = ok && encode_tiled_bf16(&mC, 5, s.cache, dc, sx, bx, 0);
-    }
-    // Weights [c_out][27][c_in] = a [27 c_out][c_in] K-major matrix; a box of
-    // npad rows (rows past 27 c_out read as zeros) x sw channels.
     cuuint64_t dw[2] = {(cuuint64_t)s.c_in, (cuuint64_t)(27 * s.c_out)};
-    cuuint64_t sww[1] = {(cuuint64_t)s.c_in * 2};
-    cuuint32_t bw[2] = {(cuuint32_t)a.sw, (cuuint32_t)a.npad};
-    ok = ok && encode_tiled_bf16(&mW, 2, s.w, dw, sww, bw, a.sw * 2);
+    cuuint64_t sw[1] = {(cuuint64_t)s.c_in * 2};
+    bool ok = true;
+    for (int w = 0; w < 2; ++w) {
+        const uint32_t cw = w == 0 ? 64u : 32u;
+        if ((w == 0 && s.c_in < 64) || (w == 1 && s.c_in % 64 == 0)) continue;
+        cuuint32_t bx[4] = {cw, kHalo, kHalo, 1};
+        ok = ok && encode_tiled_bf16(&m[w], 4, s.in, dx, sx, bx, (int)cw * 2);
+        if (s.cache) {
+            cuuint64_t dc[4] = {dx[0], dx[1], dx[2], (cuuint64_t)s.B * 2};
+            ok = ok && encode_tiled_bf16(&m[2 + w], 4, s.cache, dc, sx, bx, (int)cw * 2);
+        }
+        cuuint32_t bw[2] = {cw, (cuuint32_t)a.npad};
+        ok = ok && encode_tiled_bf16(&m[4 + w], 2, s.w, dw, sw, bw, (int)cw * 2);
+    }
     if (!ok) return cudaErrorInvalidValue;
-    if (!s.cache) mC = mX;
+    const int have = s.c_in >= 64 ? 0 : 1;  // a map that exists, for the unused slots
+    for (int w = 0; w < 2; ++w) {
+        if ((w == 0 && s.c_in < 64) || (w == 1 && s.c_in % 64 == 0)) {
+            m[w] = m[have];
+            m[4 + w] = m[4 + have];
+        }
+        if (!s.cache) m[2 + w] = m[w];
+        else if ((w == 0 && s.c_in < 64) || (w == 1 && s.c_in % 64 == 0)) m[2 + w] = m[2 + have];
+    }
     switch (s.c_out) {
-        case 1: return launch_narrow<1>(a, mX, mC, mW, smem, ctx);
-        case 2: return launch_narrow<2>(a, mX, mC, mW, smem, ctx);
-        case 3: return launch_narrow<3>(a, mX, mC, mW, smem, ctx);
+        case 1: return launch_narrow<1>(a, m, smem, ctx);
+        case 2: return launch_narrow<2>(a, m, smem, ctx);
+        case 3: return launch_narrow<3>(a, m, smem, ctx);
         default: return cudaErrorInvalidValue;
     }
 }
