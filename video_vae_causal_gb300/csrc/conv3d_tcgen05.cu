@@ -78,7 +78,9 @@ struct ConvArgs {
     int patches_w;       // patches per frame row (halo mode)
     int nq;              // 128-row sub-tiles per CTA tile (halo mode: 1, or 2 for 16x16 patches)
     int halo_w;          // halo width in pixels: 8 * nq + 2
-    uint32_t plane_bytes;  // one 8-channel plane of the halo: 18 * halo_w * 16
+    int halo_rows;         // halo as swizzled pixel rows (sw = 64) instead of 8-channel planes
+    uint32_t sub_stride;   // rows: bytes between the halo's sw-channel regions (1024-aligned)
+    uint32_t plane_bytes;  // planes: one 8-channel plane of the halo, 18 * halo_w * 16
     int tb;              // spatial taps per weight stage (halo mode: 1, 3)
     int narrow;          // c_out < 16: N padded to 16 per CTA, rows past c_out read as zeros
     int bc_row, bc_rank; // B box coordinates of this CTA's rows: (rank * bc_row, rank * bc_rank)
@@ -130,11 +132,13 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const ConvArgs &p) {
 }
 
 // Halo mode: every smem halo is 18 x halo_w pixels (a 16 x 8nq patch grown
-// by the 3x3 window; halo_w = 10 or 18), stored as planes of 8 channels:
-// plane j holds 16 bytes for each pixel, row-major.  The MMA A operand of
-// tap (kh, kw) for sub-tile s is the window starting at pixel (kh, kw + 8s):
-// rows 16 bytes apart inside a patch row, patch rows one halo row (halo_w *
-// 16 bytes) apart, K-planes one plane apart -- a no-swizzle K-major operand.
+// by the 3x3 window; halo_w = 10 or 18), stored per sw-channel chunk as one
+// swizzled row per pixel, row-major over the halo.  The MMA A operand of tap
+// (kh, kw) for sub-tile s is the window starting at pixel (kh, kw + 8s):
+// consecutive rows inside a patch row, 8-row groups one halo row (halo_w
+// rows) apart -- a swizzled K-major operand whose start and group stride are
+// not atom-aligned, which the tensor core reads correctly because it applies
+// the swizzle by absolute address.
 constexpr uint32_t kHaloH = 18;
 
 
@@ -401,8 +405,16 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                         ok = false;
                         break;
                     }
-                    if (g == 0)
-                        load5<kPair>(da, am, fb, 0, ti.w0 - 1, ti.h0 - 1, cc * (chunk / 8), fidx);
+                    if (g == 0) {
+                        if (p.halo_rows) {
+                            for (int s = 0; s < p.nsub; ++s)  // one region per sw channels
+                                load4<kPair>(da + (uint32_t)s * p.sub_stride, am, fb,
+                                             (cc * p.nsub + s) * p.sw, ti.w0 - 1, ti.h0 - 1, fidx);
+                        } else {
+                            load5<kPair>(da, am, fb, 0, ti.w0 - 1, ti.h0 - 1,
+                                         cc * (chunk / 8), fidx);
+                        }
+                    }
                     // tb consecutive spatial taps of this chunk in one box
                     const int tap = kt * 9 + g * p.tb;
                     load5<kPair>(db, mapB, fb, tap * p.c_in + cc * chunk, (int)rank * p.bc_row,
@@ -435,16 +447,16 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
     }
 }
 
-// Halo-mode MMAs of one spatial tap and one 128-row sub-tile: k-step ks uses
-// A planes 2ks, 2ks+1 of the halo window (plane2 descriptor units per k-step)
-// and B sub-tile ks / KK at k-offset ks % KK (sub-tiles b_sub16 units apart).
+// Halo-mode MMAs of one spatial tap and one 128-row sub-tile: k-step ks =
+// s KK + kk reads the halo window at a0 + s a_sub16 + kk a_kk16 (descriptor
+// units) and B sub-tile s (b_sub16 apart) at k-offset kk.
 template <int kPair, int KK, int NSUB, int NP>
 __device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc, uint64_t a0,
-                                               uint64_t b0, uint32_t b_sub16, uint32_t plane2,
-                                               uint32_t idesc, bool first) {
+                                               uint64_t b0, uint32_t b_sub16, uint32_t a_sub16,
+                                               uint32_t a_kk16, uint32_t idesc, bool first) {
     const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
     auto mma = [&](int s, int kk, int ks, int j) {
-        const uint64_t ad = a0 + (uint64_t)(ks * plane2);
+        const uint64_t ad = a0 + (uint64_t)(s * a_sub16 + kk * a_kk16);
         const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
         const uint32_t accum = (first && ks == 0) ? 0u : 1u;
         const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
@@ -530,9 +542,17 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
     const uint32_t b_sub16 = p.b_sub_bytes >> 4;
     const uint32_t tap_b16 = (uint32_t)p.nsub * b_sub16;  // one tap's weights
     const uint32_t stage16 = p.stage_bytes >> 4, astride16 = p.a_stride >> 4;
-    const uint32_t plane2 = (2u * p.plane_bytes) >> 4, hrow16 = (uint32_t)p.halo_w;
+    // Halo windows, 8-pixel groups one halo row apart.  Rows: one swizzled
+    // row per pixel, sw-channel regions sub_stride apart, k-steps 32 B apart.
+    // Planes: 16 bytes per pixel, k-steps two 8-channel planes apart.
+    const uint32_t px16 = p.halo_rows ? row_bytes >> 4 : 1u;
+    const uint32_t hrow16 = (uint32_t)p.halo_w * px16;
+    const uint32_t a_kk16 = p.halo_rows ? 2u : (2u * p.plane_bytes) >> 4;
+    const uint32_t a_sub16 = p.halo_rows ? p.sub_stride >> 4 : (uint32_t)(p.sw / 16) * a_kk16;
     const uint64_t bdesc0 = sdesc_kmajor(sbase + p.a_bytes, row_bytes, p.layout);
-    const uint64_t adesc0 = sdesc_plain(sbase + p.off_a, p.plane_bytes, (uint32_t)p.halo_w * 16u);
+    const uint64_t adesc0 =
+        p.halo_rows ? sdesc_kmajor_sbo(sbase + p.off_a, (uint32_t)p.halo_w * row_bytes, p.layout)
+                    : sdesc_plain(sbase + p.off_a, p.plane_bytes, (uint32_t)p.halo_w * 16u);
     const bool tb3 = p.tb == 3;
     FullRing<kPair == 2> ring;
     int ia = 0, it = 0;
@@ -550,14 +570,15 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
                      bool first) {
         constexpr int NQ = decltype(nq_c)::value, NTAP = decltype(ntap_c)::value;
         const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16);
-        const uint64_t ah = abase + (uint64_t)(kh * hrow16 + kw0);
+        const uint64_t ah = abase + (uint64_t)(kh * hrow16 + kw0 * px16);
 #pragma unroll
         for (int kw = 0; kw < NTAP; ++kw)
 #pragma unroll
             for (int sq = 0; sq < NQ; ++sq)
                 issue_tap_halo<kPair, KK, NSUB, NP>(
-                    p, dacc + (uint32_t)(sq * p.acc_cols), ah + (uint64_t)(kw + 8 * sq),
-                    b0 + (uint64_t)(kw * tap_b16), b_sub16, plane2, idesc, first && kw == 0);
+                    p, dacc + (uint32_t)(sq * p.acc_cols),
+                    ah + (uint64_t)((kw + 8 * sq) * px16), b0 + (uint64_t)(kw * tap_b16),
+                    b_sub16, a_sub16, a_kk16, idesc, first && kw == 0);
     };
     using I1 = std::integral_constant<int, 1>;
     using I2 = std::integral_constant<int, 2>;
@@ -1294,13 +1315,27 @@ bool encode_weight_taps(CUtensorMap *m, const void *base, uint64_t K, int c_in, 
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// NHWC input viewed as (8 channels, W, H, C/8 chunks, frames): the chunk
-// dimension (16 bytes apart) is outside the spatial ones, so one 18 x halo_w
-// pixel box of `chunk` channels lands as planes [chunk/8][18][halo_w][8 ch],
-// the no-swizzle layout the halo-mode MMAs read.  Pixels outside the frame
-// read as zeros (the conv's spatial pad).
-bool encode_halo(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int chunk,
+// NHWC input as (C, W, H, frames) with a (sw, halo_w, 18, 1) box: the 18 x
+// halo_w pixels around a patch, sw channels each, land as one swizzled row
+// per pixel (row-major over the halo) -- the layout the halo-mode windows
+// read.  Pixels outside the frame read as zeros (the conv's spatial pad).
+bool encode_halo(CUtensorMap *m, const void *base, int C, int W, int H, int frames, int sw,
                  int halo_w) {
+    cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)frames};
+    cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
+    cuuint32_t box[4] = {(cuuint32_t)sw, (cuuint32_t)halo_w, kHaloH, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(sw),
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// NHWC input viewed as (8 channels, W, H, C/8 planes, frames): one 18 x
+// halo_w pixel box of `chunk` channels lands as planes [chunk/8][18][halo_w][8]
+// with 16 bytes per pixel, the no-swizzle layout of halo planes.
+bool encode_halo_planes(CUtensorMap *m, const void *base, int C, int W, int H, int frames,
+                        int chunk, int halo_w) {
     cuuint64_t dims[5] = {8, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)(C / 8),
                           (cuuint64_t)frames};
     cuuint64_t strides[4] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, 16,
@@ -1341,7 +1376,8 @@ struct Plan {
     int tb;  // spatial taps per weight stage (halo mode)
     int nq, halo_w;  // sub-tiles per CTA tile, halo width in pixels (halo mode)
     int narrow, npad;  // c_out < 16: N padded to npad
-    uint32_t plane_bytes;
+    uint32_t sub_stride;  // halo rows: bytes between sw-channel regions
+    int halo_rows;        // halo layout: swizzled pixel rows (sw = 64) or 8-channel planes
     int acc_stride;
     uint32_t off_a, a_stride, a_tx;
 };
@@ -1384,13 +1420,17 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.nq = (halo && wide) ? 2 : 1;
     if (pl.nq == 2 && (s.sc_in || s.c_out > 128)) return false;
     pl.halo_w = 8 * pl.nq + 2;
-    pl.plane_bytes = (uint32_t)(kHaloH * pl.halo_w * 16);
     int sw = pick_sw(s.c_in);
     if (s.sc_in) {
         const int sw2 = pick_sw(s.c_sc);
         if (sw2 < sw) sw = sw2;
     }
     pl.sw = sw;
+    // Halo layout: 64-channel chunks as one 128-byte swizzled row per pixel
+    // (one TMA row per pixel and chunk), narrower ones as 8-channel planes
+    // (measured faster for them).  A rows region: 18 x halo_w rows.
+    pl.halo_rows = sw == 64;
+    pl.sub_stride = ((uint32_t)(kHaloH * pl.halo_w) * (uint32_t)sw * 2u + 1023u) & ~1023u;
     // N split into equal pieces of at most 256 columns, each a multiple of
     // 16 * pair (a pair splits every piece's rows between its two CTAs).
     // Narrow layers (c_out < 16) pad N to 16 rows per CTA; their weight rows
@@ -1446,7 +1486,9 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         int best_waits = 0, best_stages = 0;
         for (int d = 4; d >= 1; --d) {
             if (d * sw > 128 || g_main % d || g_sc % d) continue;
-            const uint32_t ha = ((uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
+            const uint32_t ha =
+                pl.halo_rows ? (uint32_t)d * pl.sub_stride
+                             : ((uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
             for (int tb = 3; tb >= 1; tb -= 2) {
                 if (tb > 1 && pl.n_pieces != 1) continue;
                 const uint32_t bs = ((uint32_t)(tb * d) * b_rows * sw * 2u + 1023u) & ~1023u;
@@ -1470,7 +1512,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.a_sub = (uint32_t)kBlockM * sw * 2;  // one x-patch sub-tile (shortcut)
         pl.b_sub = b_rows * sw * 2;
         pl.a_tx = (uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u;
-        pl.a_stride = (pl.a_tx + 1023u) & ~1023u;
+        pl.a_stride = pl.halo_rows ? (uint32_t)d * pl.sub_stride : (pl.a_tx + 1023u) & ~1023u;
         pl.off_a = 0;
         pl.a_bytes = 2u * pl.a_stride;  // the weight ring starts here
         pl.stage_bytes = (pl.b_sub * d * (uint32_t)pl.tb + 1023u) & ~1023u;
@@ -1658,11 +1700,16 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     memset(&mSA, 0, sizeof(mSA));
     memset(&mSB, 0, sizeof(mSB));
     bool ok = true;
-    if (pl.halo) {
-        const int chunk = pl.nsub * pl.sw;
-        ok = ok && encode_halo(&mA, s.in, s.c_in, s.W, s.H, frames, chunk, pl.halo_w);
+    if (pl.halo && pl.halo_rows) {
+        ok = ok && encode_halo(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw, pl.halo_w);
         if (s.cache)
-            ok = ok && encode_halo(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, chunk, pl.halo_w);
+            ok = ok && encode_halo(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, pl.sw, pl.halo_w);
+    } else if (pl.halo) {
+        const int chunk = pl.nsub * pl.sw;
+        ok = ok && encode_halo_planes(&mA, s.in, s.c_in, s.W, s.H, frames, chunk, pl.halo_w);
+        if (s.cache)
+            ok = ok && encode_halo_planes(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, chunk,
+                                          pl.halo_w);
     } else if (s.k == 3) {
         ok = ok && encode_im2col(&mA, s.in, s.c_in, s.W, s.H, frames, pl.sw);
         if (s.cache) ok = ok && encode_im2col(&mC, s.cache, s.c_in, s.W, s.H, s.B * 2, pl.sw);
@@ -1716,7 +1763,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.halo = pl.halo;
     a.nq = pl.halo ? pl.nq : 1;
     a.halo_w = pl.halo_w;
-    a.plane_bytes = pl.plane_bytes;
+    a.halo_rows = pl.halo_rows;
+    a.sub_stride = pl.sub_stride;
+    a.plane_bytes = (uint32_t)(kHaloH * pl.halo_w * 16);
     a.patches_w = (s.W + 8 * a.nq - 1) / (8 * a.nq);
     a.tb = pl.tb;
     a.narrow = pl.narrow;

@@ -375,6 +375,23 @@ __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, uint32_t row_by
     return d;
 }
 
+// Swizzled K-major descriptor with an explicit stride between 8-row groups.
+// The tensor core applies the swizzle by absolute shared-memory address, so
+// the start may be any row and `sbo` any multiple of the row size: a window
+// of rows cut out of a larger swizzled array (a shifted conv tap) is read
+// correctly, as long as that array was written (by TMA from a 1024-byte
+// aligned box) with the same address-based swizzle.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sbo(uint32_t saddr, uint32_t sbo,
+                                                     uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)layout << 61;
+    return d;
+}
+
 // Descriptor of a no-swizzle K-major operand: core matrices of 8 rows x 16
 // bytes (rows 16 bytes apart), `lbo` bytes between core matrices along K and
 // `sbo` bytes between 8-row groups along M/N.
