@@ -1385,17 +1385,12 @@ struct Plan {
 // Halo tiles (16 x 8 patches, one halo load per temporal tap and channel
 // chunk feeding all nine spatial taps) move ~6x fewer A bytes and 9x fewer A
 // loads than per-tap im2col, but cover H x W in whole patches: chosen when
-// the patches tile the frame exactly, or when W does and the whole call is
-// at most about one wave of tiles (a streaming call of one frame), where the
-// shorter per-tile pipeline outweighs the padded rows (measured: +4 % on a
-// 90 x 160 frame, -12 % on a 21-frame 60 x 104 clip).  WANVAE_CONV_HALO=0/1
-// forces either.
+// the patches tile the frame exactly.  WANVAE_CONV_HALO=0/1 forces either.
 int halo_choice(const ConvSpec &s) {
     if (s.k != 3) return 0;
     const char *e = getenv("WANVAE_CONV_HALO");
     if (e && e[0] && e[1] == 0 && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
-    if (s.W % 8) return 0;
-    return s.H % 16 == 0 || (int64_t)s.B * s.T * s.H * s.W <= (int64_t)kBlockM * 160;
+    return s.H % 16 == 0 && s.W % 8 == 0;
 }
 
 // CTA pairs halve each CTA's share of the B (weight) operand -- half the
