@@ -74,25 +74,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def conv_source_sha():
+def conv_source_sha(files=("conv3d_tcgen05.cu", "ptx.cuh")):
     h = hashlib.sha256()
-    for f in ("conv3d_tcgen05.cu", "ptx.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "video_vae_causal_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name):
-    """DRAM bytes per conv launch of workload `name` from its committed ncu
-    summary, if there is one taken on the current conv source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"conv3d_tcgen05_{name}.md")
+def profiled_traffic(name, kernel="conv3d_tcgen05", files=("conv3d_tcgen05.cu", "ptx.cuh")):
+    """DRAM bytes per launch of `kernel` in workload `name` from its committed
+    ncu summary, if there is one taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{name}.md")
     try:
         kv = {}
         for line in open(path):
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
                 kv[k.strip()] = v.strip().strip("`")
-        if kv.get("source_sha") == conv_source_sha():
+        if kv.get("source_sha") == conv_source_sha(files):
             return int(kv["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -382,7 +382,11 @@ def bench_conv(args):
     hbm = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": nbytes}
     main, other = (tensor, hbm) if flop / nbytes >= ridge else (hbm, tensor)
-    main.update({"kernel": "conv3d_tcgen05_kernel", "traffic": None,
+    narrow = ci >= 32 and ci % 32 == 0 and ci <= 128 and co <= 3 and k == 3
+    kname = "conv3d_narrow" if narrow else "conv3d_tcgen05"
+    traffic = None if args.frames else profiled_traffic(
+        name, kname, (kname + ".cu", "ptx.cuh"))
+    main.update({"kernel": kname + "_kernel", "traffic": traffic,
                  "peak_source": peaks["source"] + (" bf16 burst" if main is tensor else " HBM copy"),
                  "arith_intensity_flop_per_byte": flop / nbytes, "ridge_flop_per_byte": ridge})
     if rank != 0:
