@@ -59,7 +59,8 @@ struct ConvArgs {
     int taps;            // 27 or 1
     int has_cache;
     int sw;              // channels per swizzled sub-tile (64, 32 or 16)
-    int nsub;            // sub-tiles per pipeline stage
+    int nsub;            // sub-tiles per pipeline stage (im2col: itb taps x channel sub-tiles)
+    int itb;             // im2col: taps per stage (3 for small c_in, else 1)
     int kc_main;         // stages per tap
     int kc_short;        // stages of the shortcut segment (0 = none)
     int n_pieces, piece_n;
@@ -163,7 +164,7 @@ __device__ __forceinline__ int unit_first_kt(int unit, const ConvArgs &p) {
 
 template <int kPair>
 __device__ __forceinline__ int unit_stages(int unit, const ConvArgs &p) {
-    const int main_taps = p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * 9 : 1;
+    const int main_taps = p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * 9 / p.itb : 1;
     return main_taps * p.kc_main + p.kc_short;
 }
 
@@ -216,28 +217,14 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
         const TileInfo ti = tile_info(u * kPair + (int)rank, p);
         const int kt0 = unit_first_kt<kPair>(u, p);
-        const int nseg = p.taps == 27 ? (3 - kt0) * 9 : 1;
+        // A segment is itb consecutive taps (one tap unless c_in is small),
+        // each stage of it itb taps x nch channel sub-tiles.
+        const int nseg = p.taps == 27 ? (3 - kt0) * 9 / p.itb : 1;
         const int segs = nseg + (p.kc_short > 0 ? 1 : 0);
+        const int row0 = ti.dummy ? M : ti.row0;
         for (int seg = 0; ok && seg < segs; ++seg) {
             const bool shortcut = seg == nseg;
-            int tap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
-            const CUtensorMap *am = mapA;
-            if (!shortcut && p.taps == 27) {
-                tap = kt0 * 9 + seg;
-                const int kt = tap / 9;
-                kh = (tap / 3) % 3;
-                kw = tap % 3;
-                const int tt = ti.t + kt - 2;
-                if (!ti.dummy) {
-                    if (tt >= 0) {
-                        fidx = ti.n * p.T + tt;
-                    } else if (p.has_cache) {
-                        am = mapC;
-                        fidx = ti.n * 2 + tt + 2;
-                    }
-                }
-            }
-            const int row0 = ti.dummy ? M : ti.row0;
+            const int ntap = shortcut ? 1 : p.itb, nch = shortcut ? p.nsub : p.nsub / p.itb;
             const int nkc = shortcut ? p.kc_short : p.kc_main;
             for (int kc = 0; kc < nkc; ++kc) {
                 if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) {
@@ -249,36 +236,56 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                 const uint32_t fb = kPair == 2 ? mapa_shared(fb_local, 0) : fb_local;
                 const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
                 const uint32_t sb = sa + p.a_bytes;
-                for (int s = 0; s < p.nsub; ++s) {
-                    const int c0 = (kc * p.nsub + s) * p.sw;
-                    const uint32_t da = sa + (uint32_t)s * p.a_sub_bytes;
-                    if (kPair == 2) {
-                        if (shortcut)
-                            tma_load_2d_pair(da, mapSA, fb, c0, row0);
-                        else if (p.taps == 27)
-                            tma_load_im2col_4d_pair(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
-                                                    (uint16_t)kw, (uint16_t)kh);
-                        else
-                            tma_load_2d_pair(da, mapA, fb, c0, row0);
-                    } else {
-                        if (shortcut)
-                            tma_load_2d(da, mapSA, fb, c0, row0);
-                        else if (p.taps == 27)
-                            tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
-                                               (uint16_t)kw, (uint16_t)kh);
-                        else
-                            tma_load_2d(da, mapA, fb, c0, row0);
+                for (int j = 0; j < ntap; ++j) {
+                    int tap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
+                    const CUtensorMap *am = mapA;
+                    if (!shortcut && p.taps == 27) {
+                        tap = kt0 * 9 + seg * p.itb + j;
+                        const int kt = tap / 9;
+                        kh = (tap / 3) % 3;
+                        kw = tap % 3;
+                        const int tt = ti.t + kt - 2;
+                        if (!ti.dummy) {
+                            if (tt >= 0) {
+                                fidx = ti.n * p.T + tt;
+                            } else if (p.has_cache) {
+                                am = mapC;
+                                fidx = ti.n * 2 + tt + 2;
+                            }
+                        }
                     }
-                    // This CTA's rows of every N-piece in one box: the weight
-                    // map is viewed as [piece][pair rank][half_n rows][K].
-                    const uint32_t db = sb + (uint32_t)s * p.b_sub_bytes;
-                    const CUtensorMap *bm = shortcut ? mapSB : mapB;
-                    const int bk = shortcut ? c0 : tap * p.c_in + c0;
-                    if (kPair == 2)
-                        tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
-                                         (int)rank * p.bc_rank, 0);
-                    else
-                        tma_load_4d(db, bm, fb, bk, 0, 0, 0);
+                    for (int s = 0; s < nch; ++s) {
+                        const int c0 = (kc * nch + s) * p.sw;
+                        const int idx = j * nch + s;  // sub-tile of the stage
+                        const uint32_t da = sa + (uint32_t)idx * p.a_sub_bytes;
+                        if (kPair == 2) {
+                            if (shortcut)
+                                tma_load_2d_pair(da, mapSA, fb, c0, row0);
+                            else if (p.taps == 27)
+                                tma_load_im2col_4d_pair(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1,
+                                                        fidx, (uint16_t)kw, (uint16_t)kh);
+                            else
+                                tma_load_2d_pair(da, mapA, fb, c0, row0);
+                        } else {
+                            if (shortcut)
+                                tma_load_2d(da, mapSA, fb, c0, row0);
+                            else if (p.taps == 27)
+                                tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
+                                                   (uint16_t)kw, (uint16_t)kh);
+                            else
+                                tma_load_2d(da, mapA, fb, c0, row0);
+                        }
+                        // This CTA's rows of every N-piece in one box: the weight
+                        // map is viewed as [piece][pair rank][half_n rows][K].
+                        const uint32_t db = sb + (uint32_t)idx * p.b_sub_bytes;
+                        const CUtensorMap *bm = shortcut ? mapSB : mapB;
+                        const int bk = shortcut ? c0 : tap * p.c_in + c0;
+                        if (kPair == 2)
+                            tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
+                                             (int)rank * p.bc_rank, 0);
+                        else
+                            tma_load_4d(db, bm, fb, bk, 0, 0, 0);
+                    }
                 }
                 ++fills;
                 if (++stage == p.stages) {
@@ -1373,6 +1380,7 @@ struct Plan {
     int staged;
     uint32_t off_stage;
     int halo;  // 16 x 8 patch tiles with halo loads
+    int itb;   // im2col: taps per stage
     int tb;  // spatial taps per weight stage (halo mode)
     int nq, halo_w;  // sub-tiles per CTA tile, halo width in pixels (halo mode)
     int narrow, npad;  // c_out < 16: N padded to npad
@@ -1483,6 +1491,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         // weights of one CTA in one piece (n_pieces == 1).
         pl.nsub = 0;
         pl.tb = 1;
+        pl.itb = 1;
         int best_waits = 0, best_stages = 0;
         for (int d = 4; d >= 1; --d) {
             if (d * sw > 128 || g_main % d || g_sc % d) continue;
@@ -1545,6 +1554,18 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     }
     pl.kc_main = g_main / pl.nsub;
     pl.kc_short = s.sc_in ? g_sc / pl.nsub : 0;
+    // Small c_in (one chunk of at most 32 channels): one k-step or two per tap
+    // would cost the MMA issuer a barrier wait per one or two MMAs, so a stage
+    // holds three consecutive taps (same K order as one tap per stage).
+    pl.itb = 1;
+    if (s.k == 3 && !s.sc_in && pl.kc_main == 1 && pl.nsub * sw <= 32) {
+        const uint32_t sb3 = 3u * (uint32_t)pl.nsub * (kBlockM + b_rows) * sw * 2u;
+        if ((uint32_t)need_stages * ((sb3 + 1023u) & ~1023u) + reserve <=
+            (uint32_t)kSmemBudget) {
+            pl.itb = 3;
+            pl.nsub *= 3;
+        }
+    }
     pl.a_sub = (uint32_t)kBlockM * sw * 2;
     pl.b_sub = b_rows * sw * 2;
     pl.a_bytes = pl.a_sub * pl.nsub;
@@ -1755,6 +1776,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.has_cache = s.cache != nullptr && s.k == 3;
     a.sw = pl.sw;
     a.nsub = pl.nsub;
+    a.itb = pl.halo ? 1 : pl.itb;
     a.kc_main = pl.kc_main;
     a.kc_short = pl.kc_short;
     a.n_pieces = pl.n_pieces;
