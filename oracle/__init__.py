@@ -46,6 +46,8 @@ def lib():
         L.oracle_resblock_points.argtypes = [vp, vp, i64, i64, ctypes.POINTER(OracleParams), vp,
                                              vp, i64, vp, vp]
         L.oracle_resblock_points.restype = ci
+        L.oracle_upsample2d_conv.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+        L.oracle_upsample2d_conv.restype = ci
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -88,6 +90,20 @@ def causal_conv3d(x, w, bias, cache=None):
                                     B, T, H, W, Ci, Co, k, _ptr(out))
     if rc:
         raise ValueError("oracle_causal_conv3d rejected its arguments")
+    return out
+
+
+def upsample2d_conv(x, w, bias):
+    """Nearest 2x upsampling in H and W, then a 3x3 conv (zero pad 1) with
+    bias, per frame.  x [B,T,H,W,Ci], w [Co,3,3,Ci] -> [B,T,2H,2W,Co]."""
+    x, w, bias = _f64(x), _f64(w), _f64(bias)
+    B, T, H, W, Ci = x.shape
+    Co = w.shape[0]
+    out = np.empty((B, T, 2 * H, 2 * W, Co))
+    rc = lib().oracle_upsample2d_conv(_ptr(x), _ptr(w), _ptr(bias), B, T, H, W, Ci, Co,
+                                      _ptr(out))
+    if rc:
+        raise ValueError("oracle_upsample2d_conv rejected its arguments")
     return out
 
 

@@ -334,6 +334,48 @@ out_free:
     return bad ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------ */
+/* Spatial upsampling of the decoder's up blocks ("Sharding of WAN 2.2 */
+/* VAE", decoder tree: WanUpBlock(..., upsample2d); section "Further   */
+/* sharding consideration: WanResample": resample[1] carries the conv  */
+/* weight).  The pages give no more; the plainest reading taken: each  */
+/* frame is upsampled 2x in H and W by nearest neighbour (every pixel  */
+/* becomes a 2x2 block), then a 3x3 conv with one pixel of zero pad on */
+/* the upsampled grid and a bias.                                      */
+/*   in  [B][T][H][W][Ci], w [Co][3][3][Ci], bias [Co]                  */
+/*   out [B][T][2H][2W][Co]                                             */
+/* ------------------------------------------------------------------ */
+API int oracle_upsample2d_conv(const double *in, const double *w, const double *bias,
+                               int64_t B, int64_t T, int64_t H, int64_t W, int64_t Ci,
+                               int64_t Co, double *out)
+{
+    if (B < 1 || T < 1 || H < 1 || W < 1 || Ci < 1 || Co < 1) return -1;
+    const int64_t H2 = 2 * H, W2 = 2 * W;
+    const int64_t nvox = B * T * H2 * W2;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t v = 0; v < nvox; ++v) {
+        const int64_t X = v % W2, Y = (v / W2) % H2, bt = v / (W2 * H2);
+        double *o = out + v * Co;
+        for (int64_t oc = 0; oc < Co; ++oc) {
+            double acc = bias ? bias[oc] : 0.0;
+            for (int kh = 0; kh < 3; ++kh) {
+                const int64_t yy = Y + kh - 1;          /* row of the upsampled grid */
+                if (yy < 0 || yy >= H2) continue;       /* zero pad */
+                for (int kw = 0; kw < 3; ++kw) {
+                    const int64_t xx = X + kw - 1;
+                    if (xx < 0 || xx >= W2) continue;
+                    /* nearest neighbour: upsampled (yy, xx) is input (yy/2, xx/2) */
+                    const double *src = in + ((bt * H + yy / 2) * W + xx / 2) * Ci;
+                    const double *wr = w + ((oc * 3 + kh) * 3 + kw) * Ci;
+                    for (int64_t c = 0; c < Ci; ++c) acc += wr[c] * src[c];
+                }
+            }
+            o[oc] = acc;
+        }
+    }
+    return 0;
+}
+
 /* Threads the oracle's OpenMP loops will use (1 when built without it). */
 API int oracle_num_threads(void)
 {

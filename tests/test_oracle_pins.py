@@ -305,3 +305,64 @@ def test_bf16_widening_is_exact():
     t = synth.make_tensor((64,), seed=3)
     v = t.float().numpy().astype(np.float64)
     assert np.array_equal(oracle._f64(t), v)
+
+
+# ---------------------------------------------------------------- upsample2d
+# The decoder's spatial upsampler (nearest 2x in H and W, then a 3x3 conv with
+# zero pad 1 and a bias) -- pinned against a library routine, a delta kernel
+# and brute force on an explicitly upsampled array.
+def test_U1_upsample2d_matches_torch_functional():
+    x = rand((2, 3, 4, 5, 6), 90)
+    w = rand((7, 3, 3, 6), 91)
+    b = rand((7,), 92)
+    y = oracle.upsample2d_conv(x, w, b)
+    B, T, H, W, C = x.shape
+    xt = torch.from_numpy(x).reshape(B * T, H, W, C).permute(0, 3, 1, 2)
+    up = F.interpolate(xt, scale_factor=2, mode="nearest")
+    ref = F.conv2d(up, torch.from_numpy(w).permute(0, 3, 1, 2), torch.from_numpy(b), padding=1)
+    ref = ref.permute(0, 2, 3, 1).reshape(B, T, 2 * H, 2 * W, 7).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_U2_upsample2d_delta_is_nearest_upsampling():
+    x = rand((1, 2, 3, 4, 5), 93)
+    w = np.zeros((5, 3, 3, 5))
+    w[:, 1, 1, :] = np.eye(5)
+    y = oracle.upsample2d_conv(x, w, np.zeros(5))
+    assert np.array_equal(y, x.repeat(2, axis=2).repeat(2, axis=3))
+
+
+@pytest.mark.parametrize("kh,kw", [(0, 0), (2, 1), (1, 2)])
+def test_U2_upsample2d_delta_shift_zero_border(kh, kw):
+    x = rand((1, 1, 3, 3, 2), 94)
+    w = np.zeros((2, 3, 3, 2))
+    w[:, kh, kw, :] = np.eye(2)
+    y = oracle.upsample2d_conv(x, w, np.zeros(2))
+    up = x.repeat(2, axis=2).repeat(2, axis=3)
+    ref = np.zeros_like(up)
+    for Y in range(6):
+        for X in range(6):
+            yy, xx = Y + kh - 1, X + kw - 1
+            if 0 <= yy < 6 and 0 <= xx < 6:
+                ref[:, :, Y, X] = up[:, :, yy, xx]
+    assert np.array_equal(y, ref)
+
+
+def test_U3_upsample2d_brute_force_tiny():
+    x = rand((1, 1, 2, 3, 2), 95)
+    w = rand((3, 3, 3, 2), 96)
+    b = rand((3,), 97)
+    y = oracle.upsample2d_conv(x, w, b)
+    up = np.zeros((4, 6, 2))
+    for i in range(4):
+        for j in range(6):
+            up[i, j] = x[0, 0, i // 2, j // 2]
+    for Y in range(4):
+        for X in range(6):
+            for o in range(3):
+                acc = b[o]
+                for kh in range(3):
+                    for kw in range(3):
+                        if 0 <= Y + kh - 1 < 4 and 0 <= X + kw - 1 < 6:
+                            acc += float(np.dot(w[o, kh, kw], up[Y + kh - 1, X + kw - 1]))
+                assert abs(y[0, 0, Y, X, o] - acc) < 1e-12
