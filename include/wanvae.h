@@ -133,6 +133,25 @@ wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bi
                                    void *y, wanvae_dims d, int64_t c_in, int64_t c_out,
                                    int k, void *cache, wanvae_stream stream);
 
+/* The decoder's spatial upsampler ("Sharding of WAN 2.2 VAE", decoder tree:
+ * WanUpBlock(..., upsample2d); its resample[1] is the conv): every frame is
+ * upsampled 2x in H and W by nearest neighbour, then convolved 3x3 with one
+ * pixel of zero pad and a bias (the pages give no more; this is the plainest
+ * reading).
+ *   x     : bf16 [B][T][H][W][c_in]  (d gives the low-res B, T, H, W)
+ *   w     : bf16 [c_out][3][3][c_in] bias: fp32 [c_out] (NULL = zeros)
+ *   y     : bf16 [B][T][2H][2W][c_out]
+ *   workspace : device buffer of wanvae_upsample2d_workspace_size(c_in, c_out)
+ *           bytes, 256-byte aligned, for the weights expanded into the four
+ *           sub-pixel phases (bf16 sums of the taps each phase folds together:
+ *           one more rounding of the weights than the plain definition).
+ *   c_in  : a multiple of 16 up to 512; c_out: a multiple of 16 up to 256.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+size_t wanvae_upsample2d_workspace_size(int64_t c_in, int64_t c_out);
+wanvae_status wanvae_upsample2d_conv(const void *x, const void *w, const float *bias, void *y,
+                                     wanvae_dims d, int64_t c_in, int64_t c_out,
+                                     void *workspace, size_t ws_bytes, wanvae_stream stream);
+
 /* Bytes of device workspace wanvae_resblock_forward needs for these sizes
  * (the bf16 conv inputs a1 and a2, 256-byte aligned).  0 on invalid sizes. */
 size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out);

@@ -183,6 +183,29 @@ def test_conv3d_no_bias_and_output_guard_bands(cuda_lib):
     compare(to_f64(y), oracle.causal_conv3d(x, w, np.zeros(co)), what="conv no bias")
 
 
+# ------------------------------------------------------------------ upsampler
+UP_CASES = [
+    # (B, T, H, W, c_in, c_out) at the low resolution; output is 2H x 2W
+    (1, 2, 5, 7, 32, 16),       # ragged tiles
+    (2, 1, 8, 12, 64, 32),
+    (1, 3, 16, 16, 96, 48),
+    (1, 1, 9, 13, 192, 96),     # the decoder's 192 -> 96 channels
+]
+
+
+@pytest.mark.parametrize("case", UP_CASES)
+def test_upsample2d_conv(cuda_lib, case, variant):
+    B, T, H, W, ci, co = case
+    x = synth.make_tensor((B, T, H, W, ci), seed=100 + sum(case))
+    bound = 1.0 / np.sqrt(9 * ci)
+    w = synth.make_tensor((co, 3, 3, ci), seed=101 + sum(case), kind="uniform", lo=-bound,
+                          hi=bound)
+    b = synth.make_tensor((co,), seed=102, dtype=torch.float32, kind="uniform", lo=-.1, hi=.1)
+    y = cuda_lib.upsample2d_conv(x.to(DEV), w.to(DEV), b.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.upsample2d_conv(x, w, b), what=f"upsample2d {case}")
+
+
 # ------------------------------------------------------------------ block
 BLOCK_CASES = [
     # (B, T, H, W, c_in, c_out)

@@ -67,6 +67,9 @@ struct ConvArgs {
     uint32_t layout;     // UMMA swizzle mode matching sw
     int tiles_per_frame, num_tiles;
     int frames;          // B * T
+    int nphase;          // 4: upsampler conv (units = tile units x sub-pixel phases), else 1
+    int tile_units;      // units per phase: ceil(num_tiles / pair)
+    int wtap0;           // first tap of the weight tensor (18: upsampler, only kt = 2)
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
     uint32_t off_bars, off_misc, off_vec;
@@ -147,8 +150,17 @@ constexpr uint32_t kHaloH = 18;
 // pair, which share every B stage and so run the same taps): taps reading
 // t+kt-2 < 0 are zero (skipped) unless a feat_cache supplies those frames.
 // A pair member whose own frame needs a skipped-for-it tap loads zeros.
+// Tile unit and sub-pixel phase of a work unit (upsampler: phase-major).
+__device__ __forceinline__ int unit_tile(int u, const ConvArgs &p) {
+    return p.nphase > 1 ? u % p.tile_units : u;
+}
+__device__ __forceinline__ int unit_phase(int u, const ConvArgs &p) {
+    return p.nphase > 1 ? u / p.tile_units : 0;
+}
+
 template <int kPair>
 __device__ __forceinline__ int unit_first_kt(int unit, const ConvArgs &p) {
+    if (p.wtap0) return p.wtap0 / 9;  // upsampler: the current frame's taps only
     if (p.taps != 27 || p.has_cache) return 0;
     int kt0 = 3;
 #pragma unroll
@@ -215,8 +227,8 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
     uint32_t phase = 0, fills = 0;
     bool ok = true;
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
-        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
-        const int kt0 = unit_first_kt<kPair>(u, p);
+        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
+        const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         // A segment is itb consecutive taps (one tap unless c_in is small),
         // each stage of it itb taps x nch channel sub-tiles.
         const int nseg = p.taps == 27 ? (3 - kt0) * 9 / p.itb : 1;
@@ -279,12 +291,13 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                         // map is viewed as [piece][pair rank][half_n rows][K].
                         const uint32_t db = sb + (uint32_t)idx * p.b_sub_bytes;
                         const CUtensorMap *bm = shortcut ? mapSB : mapB;
-                        const int bk = shortcut ? c0 : tap * p.c_in + c0;
+                        const int bk = shortcut ? c0 : (tap - p.wtap0) * p.c_in + c0;
+                        const int bp = unit_phase(u, p) * p.n_pieces;  // upsampler phase rows
                         if (kPair == 2)
                             tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
-                                             (int)rank * p.bc_rank, 0);
+                                             (int)rank * p.bc_rank, bp);
                         else
-                            tma_load_4d(db, bm, fb, bk, 0, 0, 0);
+                            tma_load_4d(db, bm, fb, bk, 0, 0, bp);
                     }
                 }
                 ++fills;
@@ -386,8 +399,8 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         return true;
     };
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
-        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
-        const int kt0 = unit_first_kt<kPair>(u, p);
+        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
+        const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         for (int kt = kt0; ok && kt < 3; ++kt) {
             const int tt = ti.t + kt - 2;
             const CUtensorMap *am = mapA;
@@ -596,7 +609,7 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
-        const int kt0 = unit_first_kt<kPair>(u, p);
+        const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
@@ -671,7 +684,7 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
         if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
-        const int nst = unit_stages<kPair>(u, p);
+        const int nst = unit_stages<kPair>(unit_tile(u, p), p);
         for (int k = 0; k < nst; ++k) {
             if (!ring.acquire(bars, wc)) {
                 ok = false;
@@ -805,7 +818,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
             break;
         }
         tc_fence_after();
-        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
+        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         for (int sub = 0; sub < p.nq; ++sub) {
         // This warp's 32 rows of sub-tile `sub`; rows outside the frame (or
         // of an empty pair slot) are not stored.
@@ -901,7 +914,26 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 uint32_t o[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                store_chunk(stg, o, n, out_w, p.c_out, c, rm);
+                if (p.nphase > 1) {
+                    // Upsampler: low-res pixel (i, j) of this row is output
+                    // pixel (2i + a, 2j + b) of the unit's phase (a, b).
+                    if (valid) {
+                        const int64_t pos = (int64_t)ti.pos + q * 32 + lane;
+                        const int64_t i = pos / p.W, j = pos - i * p.W;
+                        const int ph = unit_phase(u, p);
+                        const int64_t dst =
+                            (((int64_t)ti.frame * 2 * p.H + 2 * i + (ph >> 1)) * 2 * p.W + 2 * j +
+                             (ph & 1)) * p.c_out + c;
+                        uint4 *d = reinterpret_cast<uint4 *>(p.out + dst);
+#pragma unroll
+                        for (int vv = 0; vv < 4; ++vv)
+                            if (8 * vv < n)
+                                d[vv] = make_uint4(o[4 * vv], o[4 * vv + 1], o[4 * vv + 2],
+                                                   o[4 * vv + 3]);
+                    }
+                } else {
+                    store_chunk(stg, o, n, out_w, p.c_out, c, rm);
+                }
             }
         }
         }  // sub-tiles
@@ -946,7 +978,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
     bool res_pending = false;  // issuer: a residual load is in flight
 
     auto issue_residual = [&](int u) {
-        const TileInfo tn = tile_info(u * kPair + (int)rank, p);
+        const TileInfo tn = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         if (tn.dummy) return;
         mbar_arrive_expect_tx(bars.resf(), res_bytes);
         for (int b = 0; b < nblk; ++b) {
@@ -963,7 +995,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
 
     int it = 0;
     for (int u = unit0; u < num_units; u += unit_stride, ++it) {
-        const TileInfo ti = tile_info(u * kPair + (int)rank, p);
+        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         bool got = mbar_wait_warp<kPair == 2>(bars.accf(0), (uint32_t)it & 1u, wc);
         if (got && resid && !ti.dummy) {
             got = mbar_wait_warp<false>(bars.resf(), res_phase, wc);
@@ -1096,7 +1128,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
     const int unit0 = kPair == 2 ? (int)cluster_id_x() : (int)blockIdx.x;
     const int unit_stride = kPair == 2 ? (int)cluster_count_x() : (int)gridDim.x;
-    const int num_units = (p.num_tiles + kPair - 1) / kPair;
+    const int num_units = p.tile_units * p.nphase;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -1283,11 +1315,12 @@ bool encode_frames(CUtensorMap *m, const void *base, int C, int HW, int frames) 
 // CTA): the row dimension is the true c_out and the pair dimension has extent
 // 1; a CTA's box starts at row rank * half_n, and rows past c_out read as zeros.
 bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int pair,
-                    int n_pieces, int sw, int nsub, int npad = 0) {
+                    int n_pieces, int sw, int nsub, int npad = 0, int nphase = 1) {
     const bool narrow = npad > c_out;
     const int piece_n = (narrow ? npad : c_out) / n_pieces, half_n = piece_n / pair;
+    // (an upsampler's nphase weight sets follow each other: nphase x n_pieces pieces)
     cuuint64_t dims[5] = {K, (cuuint64_t)(narrow ? c_out : half_n),
-                          (cuuint64_t)(narrow ? 1 : pair), (cuuint64_t)n_pieces,
+                          (cuuint64_t)(narrow ? 1 : pair), (cuuint64_t)(n_pieces * nphase),
                           (cuuint64_t)(nsub > 0 ? nsub : 1)};
     cuuint64_t strides[4] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)piece_n * K * 2,
                              (cuuint64_t)sw * 2};
@@ -1474,6 +1507,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     const uint32_t fixed = 1024 /*align*/ + 1024 /*bars+misc*/ + 2u * 4u * s.c_out +
                            4u * 4u * kBlockM /*norm partial sums*/;
     pl.staged = 0;
+    if (s.up2d && pl.nacc != 2) return false;  // its scattered stores use the direct epilogue
     if (pl.nacc == 1 && s.c_out % 64 == 0) {
         const uint32_t sb1 = (kBlockM + b_rows) * (uint32_t)sw * 2u;
         if (3u * ((sb1 + 1023u) & ~1023u) + fixed + stage_tile <= (uint32_t)kSmemBudget)
@@ -1661,7 +1695,7 @@ cudaError_t kernel_facts(ConvKernelFn fn, bool pair, int &max_pairs) {
 // The first plan that fits: the preferred CTA grouping with wide halo tiles,
 // then plain halo tiles, then the same on single CTAs, then im2col.
 bool pick_plan(const ConvSpec &s, Plan &pl, int pair) {
-    const int hc = halo_choice(s), wc = wide_choice(s, hc);
+    const int hc = s.up2d ? 0 : halo_choice(s), wc = wide_choice(s, hc);
     return (wc && make_plan(s, pl, pair, hc, 1)) || make_plan(s, pl, pair, hc, 0) ||
            (wc && make_plan(s, pl, 1, hc, 1)) || make_plan(s, pl, 1, hc, 0) ||
            make_plan(s, pl, 1, 0, 0);
@@ -1741,8 +1775,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
         ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)27 * s.c_in, s.c_in, s.c_out, pl.pair,
                                       pl.sw, pl.nsub, pl.tb, pl.npad);
     else
-        ok = ok && encode_weights(&mB, s.w, (uint64_t)s.k * s.k * s.k * s.c_in, s.c_out, pl.pair,
-                                  pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0, pl.npad);
+        ok = ok && encode_weights(&mB, s.w, (uint64_t)(s.up2d ? 9 : s.k * s.k * s.k) * s.c_in,
+                                  s.c_out, pl.pair, pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0,
+                                  pl.npad, s.up2d ? 4 : 1);
     if (s.sc_in) {
         if (pl.halo)
             ok = ok && encode_patch(&mSA, s.sc_in, s.c_sc, s.W, s.H, frames, pl.sw, pl.sw);
@@ -1799,6 +1834,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.tiles_per_frame = pl.halo ? ((s.H + 15) / 16) * a.patches_w : (HW + kBlockM - 1) / kBlockM;
     a.num_tiles = a.tiles_per_frame * frames;
     a.frames = frames;
+    a.nphase = s.up2d ? 4 : 1;
+    a.tile_units = (a.num_tiles + pl.pair - 1) / pl.pair;
+    a.wtap0 = s.up2d ? 18 : 0;
     a.stages = pl.stages;
     a.a_sub_bytes = pl.a_sub;
     a.b_sub_bytes = pl.b_sub;
@@ -1832,11 +1870,12 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     if (pl.pair == 1) {
-        const int grid = a.num_tiles < ctx.num_sms ? a.num_tiles : ctx.num_sms;
+        const int units = a.tile_units * a.nphase;
+        const int grid = units < ctx.num_sms ? units : ctx.num_sms;
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
         cfg.numAttrs = 0;
     } else {
-        const int units = (a.num_tiles + 1) / 2;
+        const int units = a.tile_units * a.nphase;
         const int pairs = units < max_pairs ? units : max_pairs;
         cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
         cfg.attrs = attr;

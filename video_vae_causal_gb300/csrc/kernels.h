@@ -28,6 +28,11 @@ cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool
 cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,
                                 const LaunchCtx &ctx);
 
+// Phase-expanded weights of the upsampler conv: w [Co][3][3][Ci] ->
+// w4 [4][Co][3][3][Ci] (bf16), see rmsnorm_silu.cu.
+cudaError_t launch_expand_up2d_weights(const void *w, void *w4, int Co, int Ci,
+                                       const LaunchCtx &ctx);
+
 // Epilogue of the implicit-GEMM conv.
 enum EpiMode : int {
     kEpiBias = 0,      // out = acc + bias (+ bias2)
@@ -54,6 +59,11 @@ struct ConvSpec {
     int c_in, c_out, c_sc;
     int k;               // 3 or 1
     int epi;             // EpiMode
+    // Spatial upsampler conv: nearest 2x in H and W then a 3x3 conv, as four
+    // sub-pixel phases over the low-res input (H x W here).  w holds the
+    // phase-expanded weights [4][c_out][3][3][c_in] (only the current frame's
+    // taps), out is [B][T][2H][2W][c_out]; k = 3, no cache, bias epilogue.
+    int up2d;
 };
 
 // Host-side validation of a ConvSpec this build can run (channel counts,

@@ -21,7 +21,8 @@ EXPORTS = (
     "wanvae_status_string", "wanvae_version", "wanvae_rmsnorm_silu", "wanvae_causal_conv3d",
     "wanvae_resblock_workspace_size", "wanvae_resblock_forward",
     "wanvae_resblock_forward_profiled", "wanvae_sync_status", "wanvae_set_wait_limit_ns",
-    "wanvae_launch_count", "wanvae_resblock_forward_static",
+    "wanvae_launch_count", "wanvae_resblock_forward_static", "wanvae_upsample2d_workspace_size",
+    "wanvae_upsample2d_conv",
 )
 
 # Size of the library's own workspace used by resblock_forward_static.
@@ -91,6 +92,10 @@ def load(path=LIB_PATH):
     L.wanvae_resblock_forward_static.argtypes = [ctypes.POINTER(ResblockParams), vp, vp, Dims,
                                                  ctypes.POINTER(ResblockCache), vp]
     L.wanvae_resblock_forward_static.restype = st
+    L.wanvae_upsample2d_workspace_size.argtypes = [i64, i64]
+    L.wanvae_upsample2d_workspace_size.restype = ctypes.c_size_t
+    L.wanvae_upsample2d_conv.argtypes = [vp, vp, vp, vp, Dims, i64, i64, vp, ctypes.c_size_t, vp]
+    L.wanvae_upsample2d_conv.restype = st
     _lib = L
     return L
 
@@ -156,6 +161,23 @@ def causal_conv3d(x, w, bias=None, y=None, cache=None, stream=None):
     st = load().wanvae_causal_conv3d(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), _dims(x.shape),
                                      x.shape[4], c_out, k, _ptr(cache), _stream(stream))
     _check(st, "wanvae_causal_conv3d")
+    return y
+
+
+def upsample2d_conv(x, w, bias=None, y=None, workspace=None, stream=None):
+    """Nearest 2x upsampling in H and W, then a 3x3 conv with bias, per frame.
+    x [B,T,H,W,c_in] bf16, w [c_out,3,3,c_in] bf16 -> y [B,T,2H,2W,c_out]."""
+    B, T, H, W, c_in = x.shape
+    c_out = w.shape[0]
+    if y is None:
+        y = torch.empty((B, T, 2 * H, 2 * W, c_out), dtype=torch.bfloat16, device=x.device)
+    L = load()
+    if workspace is None:
+        n = int(L.wanvae_upsample2d_workspace_size(c_in, c_out))
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = L.wanvae_upsample2d_conv(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), _dims(x.shape), c_in,
+                                  c_out, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "wanvae_upsample2d_conv")
     return y
 
 
