@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["tiny", "latent_fullT", "stream_720p", "reduce_384_192",
                              "fullres_96", "conv_in_latent", "post_quant_latent",
-                             "conv_out_fullres"],
+                             "conv_out_fullres", "upsample2d_fullres"],
                     help="latent_fullT (default) is the headline; the others are the remaining "
                          "workloads of the design notes (the conv_* / post_quant_* ones time "
                          "one CausalConv3d call: the decoder's boundary convs)")
@@ -182,6 +182,9 @@ WORKLOAD_TEXT = {
                          "16 -> 16 (the decoder's post_quant_conv)",
     "conv_out_fullres": "conv_out_fullres: CausalConv3d k=3 over x bf16 [1,81,480,832,96], "
                         "96 -> 3 (the decoder's conv_out to RGB), full clip",
+    "upsample2d_fullres": "upsample2d_fullres: nearest 2x upsampling + 3x3 conv of x bf16 "
+                          "[1,81,240,416,192] -> [1,81,480,832,96] (the last up block's "
+                          "upsampler)",
 }
 
 
@@ -225,7 +228,7 @@ def bench_reference(args):
     import oracle
     from video_vae_causal_gb300 import synth
     name = args.workload
-    if name in synth.CONV_WORKLOADS:
+    if name in synth.CONV_WORKLOADS or name in synth.UPSAMPLE_WORKLOADS:
         return bench_reference_conv(args)
     dims, ci, co, _ = synth.WORKLOADS[name]
     B, T, H, W = dims
@@ -262,24 +265,37 @@ def bench_reference_conv(args):
     import oracle
     from video_vae_causal_gb300 import synth
     name = args.workload
-    dims, ci, co, k = synth.CONV_WORKLOADS[name]
-    B, T, H, W = dims
-    x, w, b = synth.make_conv_inputs((B, min(T, 3), H, W), ci, co, k, seed=0)
+    up = name in synth.UPSAMPLE_WORKLOADS
+    if up:
+        dims, ci, co = synth.UPSAMPLE_WORKLOADS[name]
+        B, T, H, W = dims
+        x, w, b = synth.make_upsample_inputs((B, min(T, 3), H, W), ci, co, seed=0)
+        fn = oracle.upsample2d_conv
+    else:
+        dims, ci, co, k = synth.CONV_WORKLOADS[name]
+        B, T, H, W = dims
+        x, w, b = synth.make_conv_inputs((B, min(T, 3), H, W), ci, co, k, seed=0)
+        fn = oracle.causal_conv3d
+    per_row = 4 if up else 1  # output voxels per input voxel
     steps = args.steps if args.steps else 10
     budget = max(1.0, 60.0 / max(1, steps + args.warmup))
     t0 = time.perf_counter()
-    oracle.causal_conv3d(x[:, :, :1], w, b)
+    fn(x[:, :, :1], w, b)
     rows = int(max(1, min(H, budget / max(time.perf_counter() - t0, 1e-3))))
     vals = []
     for i in range(args.warmup + steps):
         t0 = time.perf_counter()
-        oracle.causal_conv3d(x[:, :, :rows], w, b)
+        fn(x[:, :, :rows], w, b)
         if i >= args.warmup:
-            vals.append(x.shape[0] * x.shape[1] * rows * W / (time.perf_counter() - t0))
+            vals.append(per_row * x.shape[0] * x.shape[1] * rows * W /
+                        (time.perf_counter() - t0))
     v = statistics.median(vals)
     sample = f"the clip's first {x.shape[1]} frames over {rows} of {H} rows x {W} columns"
     print(json.dumps({
-        "impl": "reference", "metric": "CausalConv3d voxels/s", "value": v, "unit": "voxels/s",
+        "impl": "reference",
+        "metric": ("Upsampler output voxels/s" if up else "CausalConv3d voxels/s") +
+                  " (roofline: the bound its arithmetic intensity sets)",
+        "value": v, "unit": "voxels/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(name, B, T, H, W, ci, co, 1),
@@ -291,7 +307,7 @@ def bench_reference_conv(args):
 
 DEFAULT_STEPS = {"tiny": 300, "latent_fullT": 300, "stream_720p": 20, "reduce_384_192": 20,
                  "fullres_96": 12, "conv_in_latent": 300, "post_quant_latent": 300,
-                 "conv_out_fullres": 30}
+                 "conv_out_fullres": 30, "upsample2d_fullres": 20}
 
 
 def bench_conv(args):
@@ -313,23 +329,41 @@ def bench_conv(args):
         dist.init_process_group("nccl", device_id=dev)
     wanvae.load()
     name = args.workload
-    dims, ci, co, k = synth.CONV_WORKLOADS[name]
+    up = name in synth.UPSAMPLE_WORKLOADS
+    if up:
+        dims, ci, co = synth.UPSAMPLE_WORKLOADS[name]
+        k = 3
+    else:
+        dims, ci, co, k = synth.CONV_WORKLOADS[name]
     if args.frames:
         dims = (dims[0], args.frames) + tuple(dims[2:])
     B, T, H, W = dims
-    M = B * T * H * W
+    Ho, Wo = (2 * H, 2 * W) if up else (H, W)
+    M = B * T * Ho * Wo                       # output voxels
     on_dev = M * max(ci, co) > (1 << 30)
-    x, w, b = synth.make_conv_inputs(dims, ci, co, k, seed=0, device=dev if on_dev else "cpu")
+    make = synth.make_upsample_inputs if up else (
+        lambda d, a, c, seed, device: synth.make_conv_inputs(d, a, c, k, seed=seed, device=device))
+    x, w, b = make(dims, ci, co, seed=0, device=dev if on_dev else "cpu")
     x_cpu = None if on_dev else x
     w_cpu, b_cpu = w.cpu(), b.cpu()
     x, w, b = x.to(dev), w.to(dev), b.to(dev)
-    y = torch.empty((B, T, H, W, co), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((B, T, Ho, Wo, co), dtype=torch.bfloat16, device=dev)
+    ws_up = None
+    if up:
+        n = int(wanvae.load().wanvae_upsample2d_workspace_size(ci, co))
+        ws_up = torch.empty(n, dtype=torch.uint8, device=dev)
+
+    def call(xin):
+        if up:
+            wanvae.upsample2d_conv(xin, w, b, y=y, workspace=ws_up)
+        else:
+            wanvae.causal_conv3d(xin, w, b, y=y)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     K = args.steps if args.steps else DEFAULT_STEPS[name]
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        wanvae.causal_conv3d(x, w, b, y=y)
+        call(x)
     torch.cuda.synchronize(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
@@ -341,7 +375,7 @@ def bench_conv(args):
         for e in evs:
             flush.zero_()
             e[0].record(stream)
-            wanvae.causal_conv3d(x, w, b, y=y)
+            call(x)
             e[1].record(stream)
         torch.cuda.synchronize(dev)
     launches = wanvae.launch_count() - n0
@@ -353,27 +387,28 @@ def bench_conv(args):
     if x_cpu is None:
         x_cpu = x.cpu()
     x_host = x_cpu.pin_memory()
-    y_host = torch.empty((B, T, H, W, co), dtype=torch.bfloat16).pin_memory()
+    y_host = torch.empty((B, T, Ho, Wo, co), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
     E = max(1, min(args.e2e_steps, K))
     for _ in range(2):
         x_dev.copy_(x_host, non_blocking=True)
-        wanvae.causal_conv3d(x_dev, w, b, y=y)
+        call(x_dev)
         y_host.copy_(y, non_blocking=True)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
         x_dev.copy_(x_host, non_blocking=True)
-        wanvae.causal_conv3d(x_dev, w, b, y=y)
+        call(x_dev)
         y_host.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_value = replica_throughput(M, ws, E, max_over_ranks(e0.elapsed_time(e1), ws, dev))
 
     peaks = load_peaks()
-    flop = 2.0 * k ** 3 * ci * co * M                    # useful work (the padded N is not counted)
-    nbytes = (ci + co) * 2.0 * M + w.numel() * 2.0 + co * 4.0  # read x once, write y once
+    # useful work (a padded N is not counted; the upsampler: a 3x3 conv per output voxel)
+    flop = 2.0 * (9 if up else k ** 3) * ci * co * M
+    nbytes = (ci * 2.0 * B * T * H * W + co * 2.0 * M + w.numel() * 2.0 + co * 4.0)  # x, y once
     tflops = flop / (ms / 1e3) / 1e12
     gbs = nbytes / (ms / 1e3) / 1e9
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -382,7 +417,7 @@ def bench_conv(args):
     hbm = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": nbytes}
     main, other = (tensor, hbm) if flop / nbytes >= ridge else (hbm, tensor)
-    narrow = ci >= 32 and ci % 32 == 0 and ci <= 128 and co <= 3 and k == 3
+    narrow = not up and ci >= 32 and ci % 32 == 0 and ci <= 128 and co <= 3 and k == 3
     kname = "conv3d_narrow" if narrow else "conv3d_tcgen05"
     traffic = None if args.frames else profiled_traffic(
         name, kname, (kname + ".cu", "ptx.cuh"))
@@ -394,7 +429,8 @@ def bench_conv(args):
             dist.destroy_process_group()
         return
     line = {
-        "metric": "CausalConv3d voxels/s (roofline: the bound its arithmetic intensity sets)",
+        "metric": ("Upsampler output voxels/s" if up else "CausalConv3d voxels/s") +
+                  " (roofline: the bound its arithmetic intensity sets)",
         "value": value, "unit": "voxels/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
@@ -409,14 +445,15 @@ def bench_conv(args):
         import oracle
         # The oracle on the first frames of the clip over as many rows as fit ~10 s.
         xs = x_cpu[:, :min(T, 3)]
+        fn = oracle.upsample2d_conv if up else oracle.causal_conv3d
         t0 = time.perf_counter()
-        oracle.causal_conv3d(xs[:, :, :1], w_cpu, b_cpu)
+        fn(xs[:, :, :1], w_cpu, b_cpu)
         t1 = max(time.perf_counter() - t0, 1e-3)
         rows = int(max(1, min(H, 10.0 / t1)))
         t0 = time.perf_counter()
-        oracle.causal_conv3d(xs[:, :, :rows], w_cpu, b_cpu)
+        fn(xs[:, :, :rows], w_cpu, b_cpu)
         dt = time.perf_counter() - t0
-        vox = xs.shape[0] * xs.shape[1] * rows * W
+        vox = xs.shape[0] * xs.shape[1] * rows * W * (4 if up else 1)  # output voxels
         line["cpu_baseline"] = {"value": vox / dt, "unit": "voxels/s",
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": f"the clip's first {xs.shape[1]} frames over {rows} "
@@ -596,7 +633,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         bench_reference(args)
-    elif args.workload in ("conv_in_latent", "post_quant_latent", "conv_out_fullres"):
+    elif args.workload in ("conv_in_latent", "post_quant_latent", "conv_out_fullres",
+                           "upsample2d_fullres"):
         bench_conv(args)
     else:
         bench_ours(args)

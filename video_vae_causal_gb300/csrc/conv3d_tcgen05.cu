@@ -70,6 +70,7 @@ struct ConvArgs {
     int nphase;          // 4: upsampler conv (units = tile units x sub-pixel phases), else 1
     int tile_units;      // units per phase: ceil(num_tiles / pair)
     int wtap0;           // first tap of the weight tensor (18: upsampler, only kt = 2)
+    int ph_c2, ph_c3;    // upsampler: B box coordinates 2 and 3 advance by phase x these
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
     uint32_t off_bars, off_misc, off_vec;
@@ -292,12 +293,13 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                         const uint32_t db = sb + (uint32_t)idx * p.b_sub_bytes;
                         const CUtensorMap *bm = shortcut ? mapSB : mapB;
                         const int bk = shortcut ? c0 : (tap - p.wtap0) * p.c_in + c0;
-                        const int bp = unit_phase(u, p) * p.n_pieces;  // upsampler phase rows
+                        const int ph = unit_phase(u, p);  // upsampler: the phase's weight rows
                         if (kPair == 2)
                             tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
-                                             (int)rank * p.bc_rank, bp);
+                                             (int)rank * p.bc_rank + ph * p.ph_c2,
+                                             ph * p.ph_c3);
                         else
-                            tma_load_4d(db, bm, fb, bk, 0, 0, bp);
+                            tma_load_4d(db, bm, fb, bk, 0, ph * p.ph_c2, ph * p.ph_c3);
                     }
                 }
                 ++fills;
@@ -437,8 +439,10 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                     }
                     // tb consecutive spatial taps of this chunk in one box
                     const int tap = kt * 9 + g * p.tb;
-                    load5<kPair>(db, mapB, fb, tap * p.c_in + cc * chunk, (int)rank * p.bc_row,
-                                 (int)rank * p.bc_rank, 0, 0);
+                    const int ph = unit_phase(u, p);  // upsampler: the phase's weight rows
+                    load5<kPair>(db, mapB, fb, (tap - p.wtap0) * p.c_in + cc * chunk,
+                                 (int)rank * p.bc_row, (int)rank * p.bc_rank + ph * p.ph_c2,
+                                 ph * p.ph_c3, 0);
                 }
             }
         }
@@ -918,7 +922,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                     // Upsampler: low-res pixel (i, j) of this row is output
                     // pixel (2i + a, 2j + b) of the unit's phase (a, b).
                     if (valid) {
-                        const int64_t pos = (int64_t)ti.pos + q * 32 + lane;
+                        const int64_t pos = g - (int64_t)ti.frame * p.HW;  // in the frame
                         const int64_t i = pos / p.W, j = pos - i * p.W;
                         const int ph = unit_phase(u, p);
                         const int64_t dst =
@@ -1339,11 +1343,13 @@ bool encode_weights(CUtensorMap *m, const void *base, uint64_t K, int c_out, int
 // box holds this CTA's rows of tb consecutive taps of one channel chunk, laid
 // out [tap][sub-tile][row][sw], the order the halo-mode MMAs step through.
 bool encode_weight_taps(CUtensorMap *m, const void *base, uint64_t K, int c_in, int c_out,
-                        int pair, int sw, int nsub, int tb, int npad = 0) {
+                        int pair, int sw, int nsub, int tb, int npad = 0, int nphase = 1) {
     const bool narrow = npad > c_out;  // as in encode_weights
     const int half_n = (narrow ? npad : c_out) / pair;
+    // (an upsampler's nphase weight sets follow each other along the rank dimension)
     cuuint64_t dims[5] = {K, (cuuint64_t)(narrow ? c_out : half_n),
-                          (cuuint64_t)(narrow ? 1 : pair), (cuuint64_t)nsub, (cuuint64_t)tb};
+                          (cuuint64_t)(narrow ? 1 : pair * nphase), (cuuint64_t)nsub,
+                          (cuuint64_t)tb};
     cuuint64_t strides[4] = {K * 2, (cuuint64_t)half_n * K * 2, (cuuint64_t)sw * 2,
                              (cuuint64_t)c_in * 2};
     cuuint32_t box[5] = {(cuuint32_t)sw, (cuuint32_t)half_n, 1, (cuuint32_t)nsub,
@@ -1695,7 +1701,7 @@ cudaError_t kernel_facts(ConvKernelFn fn, bool pair, int &max_pairs) {
 // The first plan that fits: the preferred CTA grouping with wide halo tiles,
 // then plain halo tiles, then the same on single CTAs, then im2col.
 bool pick_plan(const ConvSpec &s, Plan &pl, int pair) {
-    const int hc = s.up2d ? 0 : halo_choice(s), wc = wide_choice(s, hc);
+    const int hc = halo_choice(s), wc = wide_choice(s, hc);
     return (wc && make_plan(s, pl, pair, hc, 1)) || make_plan(s, pl, pair, hc, 0) ||
            (wc && make_plan(s, pl, 1, hc, 1)) || make_plan(s, pl, 1, hc, 0) ||
            make_plan(s, pl, 1, 0, 0);
@@ -1772,8 +1778,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
         ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
     }
     if (pl.halo && pl.tb > 1)
-        ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)27 * s.c_in, s.c_in, s.c_out, pl.pair,
-                                      pl.sw, pl.nsub, pl.tb, pl.npad);
+        ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)(s.up2d ? 9 : 27) * s.c_in, s.c_in,
+                                      s.c_out, pl.pair, pl.sw, pl.nsub, pl.tb, pl.npad,
+                                      s.up2d ? 4 : 1);
     else
         ok = ok && encode_weights(&mB, s.w, (uint64_t)(s.up2d ? 9 : s.k * s.k * s.k) * s.c_in,
                                   s.c_out, pl.pair, pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0,
@@ -1837,6 +1844,11 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.nphase = s.up2d ? 4 : 1;
     a.tile_units = (a.num_tiles + pl.pair - 1) / pl.pair;
     a.wtap0 = s.up2d ? 18 : 0;
+    // which B box coordinate a phase moves: the rank dimension of the 3-tap
+    // map (its pieces are one), else the piece dimension
+    const bool taps_map = pl.halo && pl.tb > 1;
+    a.ph_c2 = s.up2d && taps_map ? pl.pair : 0;
+    a.ph_c3 = s.up2d && !taps_map ? pl.n_pieces : 0;
     a.stages = pl.stages;
     a.a_sub_bytes = pl.a_sub;
     a.b_sub_bytes = pl.b_sub;

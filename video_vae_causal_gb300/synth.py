@@ -33,6 +33,12 @@ CONV_WORKLOADS = {
     "conv_out_fullres": ((1, 81, 480, 832), 96, 3, 3),
 }
 
+# The decoder's spatial upsampler (nearest 2x in H and W, then a 3x3 conv),
+# as in the last upsampling up block: (name, low-res (B, T, H, W), c_in, c_out).
+UPSAMPLE_WORKLOADS = {
+    "upsample2d_fullres": ((1, 81, 240, 416), 192, 96),
+}
+
 
 def _uniform(g, shape, lo, hi, device):
     return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
@@ -79,6 +85,20 @@ def make_conv_inputs(dims, c_in, c_out, k, seed=0, device="cpu"):
                     dtype=torch.float32).to(torch.bfloat16)
     bound = 1.0 / math.sqrt(k * k * k * c_in)
     w = _uniform(g, (c_out, k, k, k, c_in), -bound, bound, device).to(torch.bfloat16)
+    b = _uniform(g, (c_out,), -0.1, 0.1, device)
+    return x, w, b
+
+
+def make_upsample_inputs(dims, c_in, c_out, seed=0, device="cpu"):
+    """x [B,T,H,W,c_in] bf16 ~ N(0,1), w [c_out,3,3,c_in] bf16 ~ U(+-1/sqrt(9 c_in)),
+    bias fp32 ~ U(-0.1, 0.1), drawn in that order from one seeded generator."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, T, H, W = dims
+    x = torch.randn((B, T, H, W, c_in), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    bound = 1.0 / math.sqrt(9 * c_in)
+    w = _uniform(g, (c_out, 3, 3, c_in), -bound, bound, device).to(torch.bfloat16)
     b = _uniform(g, (c_out,), -0.1, 0.1, device)
     return x, w, b
 
