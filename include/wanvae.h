@@ -142,9 +142,10 @@ wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bi
  *   w     : bf16 [c_out][3][3][c_in] bias: fp32 [c_out] (NULL = zeros)
  *   y     : bf16 [B][T][2H][2W][c_out]
  *   workspace : device buffer of wanvae_upsample2d_workspace_size(c_in, c_out)
- *           bytes, 256-byte aligned, for the weights expanded into the four
- *           sub-pixel phases (bf16 sums of the taps each phase folds together:
- *           one more rounding of the weights than the plain definition).
+ *           bytes, 256-byte aligned, for the weights of the four sub-pixel
+ *           phases: each phase of the output is a 2 x 2 conv of x whose taps
+ *           are bf16 sums of the 3 x 3 taps it folds together (one more
+ *           rounding of the weights than the plain definition).
  *   c_in  : a multiple of 16 up to 512; c_out: a multiple of 16 up to 256.
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
 size_t wanvae_upsample2d_workspace_size(int64_t c_in, int64_t c_out);

@@ -97,7 +97,7 @@ def test_upsample_argument_errors(lib):
     d = _dims(1, 2, 4, 4)
     Y, WS = 0x900000, 0x2000000
     n = lib.wanvae_upsample2d_workspace_size(32, 16)
-    assert n == 4 * 9 * 32 * 16 * 2
+    assert n == 4 * 4 * 32 * 16 * 2  # 4 phases x 2 x 2 taps
     assert f(None, A, None, Y, d, 32, 16, WS, n, None) == wanvae.ERR_INVALID_ARG
     assert f(A, A, None, Y, d, 32, 16, None, n, None) == wanvae.ERR_INVALID_ARG
     assert f(A, A, None, Y, d, 32, 272, WS, 1 << 30, None) == wanvae.ERR_UNSUPPORTED

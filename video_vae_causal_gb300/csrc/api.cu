@@ -175,7 +175,7 @@ wanvae_status wanvae_causal_conv3d(const void *x, const void *w, const float *bi
 
 size_t wanvae_upsample2d_workspace_size(int64_t c_in, int64_t c_out) {
     if (c_in < 1 || c_out < 1 || c_in > 4096 || c_out > 4096) return 0;
-    return align256((size_t)4 * 9 * c_in * c_out * 2);
+    return align256((size_t)4 * 4 * c_in * c_out * 2);  // 4 phases x 2 x 2 taps
 }
 
 wanvae_status wanvae_upsample2d_conv(const void *x, const void *w, const float *bias, void *y,
@@ -199,7 +199,7 @@ wanvae_status wanvae_upsample2d_conv(const void *x, const void *w, const float *
     ConvSpec s;
     memset(&s, 0, sizeof(s));
     s.in = x;
-    s.w = workspace;  // phase-expanded weights
+    s.w = workspace;  // sub-pixel weights [4][c_out][2][2][c_in]
     s.bias = bias;
     s.out = y;
     s.B = (int)d.B;

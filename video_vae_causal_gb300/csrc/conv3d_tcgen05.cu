@@ -69,7 +69,8 @@ struct ConvArgs {
     int frames;          // B * T
     int nphase;          // 4: upsampler conv (units = tile units x sub-pixel phases), else 1
     int tile_units;      // units per phase: ceil(num_tiles / pair)
-    int wtap0;           // first tap of the weight tensor (18: upsampler, only kt = 2)
+    int wtap0;           // 9 x the temporal tap the weights start at (18: upsampler, kt = 2 only)
+    int sp_taps, sp_w;   // spatial taps per temporal tap and per tap row: 9, 3 (upsampler: 4, 2)
     int ph_c2, ph_c3;    // upsampler: B box coordinates 2 and 3 advance by phase x these
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
@@ -151,12 +152,24 @@ constexpr uint32_t kHaloH = 18;
 // pair, which share every B stage and so run the same taps): taps reading
 // t+kt-2 < 0 are zero (skipped) unless a feat_cache supplies those frames.
 // A pair member whose own frame needs a skipped-for-it tap loads zeros.
-// Tile unit and sub-pixel phase of a work unit (upsampler: phase-major).
+// Tile unit and sub-pixel phase of a work unit.  Upsampler: phase-minor, so
+// the four phases of a tile run side by side on neighbouring CTAs and read
+// its input from L2 rather than each from HBM.
 __device__ __forceinline__ int unit_tile(int u, const ConvArgs &p) {
-    return p.nphase > 1 ? u % p.tile_units : u;
+    return p.nphase > 1 ? u / p.nphase : u;
 }
 __device__ __forceinline__ int unit_phase(int u, const ConvArgs &p) {
-    return p.nphase > 1 ? u / p.tile_units : 0;
+    return p.nphase > 1 ? u % p.nphase : 0;
+}
+// Upsampler phase (a, b) = (ph >> 1, ph & 1): its sub-pixel kernel is the 2 x 2
+// block of low-res taps whose corner is (a, b) in the 3 x 3 window; a plain
+// conv's spatial taps start at (0, 0).
+struct TapBase {
+    int kh, kw;
+};
+__device__ __forceinline__ TapBase unit_tap_base(int u, const ConvArgs &p) {
+    const int ph = unit_phase(u, p);
+    return TapBase{ph >> 1, ph & 1};
 }
 
 template <int kPair>
@@ -177,7 +190,8 @@ __device__ __forceinline__ int unit_first_kt(int unit, const ConvArgs &p) {
 
 template <int kPair>
 __device__ __forceinline__ int unit_stages(int unit, const ConvArgs &p) {
-    const int main_taps = p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * 9 / p.itb : 1;
+    const int main_taps =
+        p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * p.sp_taps / p.itb : 1;
     return main_taps * p.kc_main + p.kc_short;
 }
 
@@ -232,7 +246,8 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         // A segment is itb consecutive taps (one tap unless c_in is small),
         // each stage of it itb taps x nch channel sub-tiles.
-        const int nseg = p.taps == 27 ? (3 - kt0) * 9 / p.itb : 1;
+        const int nseg = p.taps == 27 ? (3 - kt0) * p.sp_taps / p.itb : 1;
+        const TapBase tbase = unit_tap_base(u, p);
         const int segs = nseg + (p.kc_short > 0 ? 1 : 0);
         const int row0 = ti.dummy ? M : ti.row0;
         for (int seg = 0; ok && seg < segs; ++seg) {
@@ -250,13 +265,15 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                 const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
                 const uint32_t sb = sa + p.a_bytes;
                 for (int j = 0; j < ntap; ++j) {
-                    int tap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
+                    // wtap: the tap's slice of the weight rows
+                    int wtap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
                     const CUtensorMap *am = mapA;
                     if (!shortcut && p.taps == 27) {
-                        tap = kt0 * 9 + seg * p.itb + j;
-                        const int kt = tap / 9;
-                        kh = (tap / 3) % 3;
-                        kw = tap % 3;
+                        const int q = seg * p.itb + j;
+                        const int kt = kt0 + q / p.sp_taps, qs = q - (q / p.sp_taps) * p.sp_taps;
+                        kh = tbase.kh + qs / p.sp_w;
+                        kw = tbase.kw + qs % p.sp_w;
+                        wtap = (kt - p.wtap0 / 9) * p.sp_taps + qs;
                         const int tt = ti.t + kt - 2;
                         if (!ti.dummy) {
                             if (tt >= 0) {
@@ -292,7 +309,7 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                         // map is viewed as [piece][pair rank][half_n rows][K].
                         const uint32_t db = sb + (uint32_t)idx * p.b_sub_bytes;
                         const CUtensorMap *bm = shortcut ? mapSB : mapB;
-                        const int bk = shortcut ? c0 : (tap - p.wtap0) * p.c_in + c0;
+                        const int bk = shortcut ? c0 : wtap * p.c_in + c0;
                         const int ph = unit_phase(u, p);  // upsampler: the phase's weight rows
                         if (kPair == 2)
                             tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
@@ -372,7 +389,7 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                                    int unit_stride, int num_units, uint32_t rank) {
     const int frames = p.num_tiles / p.tiles_per_frame;
     const int chunk = p.nsub * p.sw;  // channels per halo / per weight sub-stage
-    const int groups = 9 / p.tb;
+    const int groups = p.sp_taps / p.tb;
     int stage = 0, ia = 0;
     uint32_t phase = 0, pha = 0, fills = 0;
     bool ok = true;
@@ -438,9 +455,9 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                         }
                     }
                     // tb consecutive spatial taps of this chunk in one box
-                    const int tap = kt * 9 + g * p.tb;
+                    const int wtap = (kt - p.wtap0 / 9) * p.sp_taps + g * p.tb;
                     const int ph = unit_phase(u, p);  // upsampler: the phase's weight rows
-                    load5<kPair>(db, mapB, fb, (tap - p.wtap0) * p.c_in + cc * chunk,
+                    load5<kPair>(db, mapB, fb, wtap * p.c_in + cc * chunk,
                                  (int)rank * p.bc_row, (int)rank * p.bc_rank + ph * p.ph_c2,
                                  ph * p.ph_c3, 0);
                 }
@@ -577,7 +594,7 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
     const uint64_t adesc0 =
         p.halo_rows ? sdesc_kmajor_sbo(sbase + p.off_a, (uint32_t)p.halo_w * row_bytes, p.layout)
                     : sdesc_plain(sbase + p.off_a, p.plane_bytes, (uint32_t)p.halo_w * 16u);
-    const bool tb3 = p.tb == 3;
+    const bool tb3 = p.tb == 3, tb4 = p.tb == 4;
     FullRing<kPair == 2> ring;
     int ia = 0, it = 0;
     bool ok = true;
@@ -590,23 +607,30 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
     // One stage: taps kw = 0 .. NTAP-1 of row kh (or the single tap `tap0`),
     // for every sub-tile.  NQ and NTAP are compile-time so the whole stage
     // is one straight run of MMAs.
-    auto stage = [&](auto nq_c, auto ntap_c, uint32_t dacc, uint64_t abase, int kh, int kw0,
-                     bool first) {
+    // One stage: NTAP taps from (kh, kw0), NW to a tap row (3 x 1 of a plain
+    // conv's row, 2 x 2 of an upsampler phase, or one tap), for every
+    // sub-tile.  All compile-time, so the whole stage is one straight run of
+    // MMAs.
+    auto stage = [&](auto nq_c, auto ntap_c, auto nw_c, uint32_t dacc, uint64_t abase, int kh,
+                     int kw0, bool first) {
         constexpr int NQ = decltype(nq_c)::value, NTAP = decltype(ntap_c)::value;
+        constexpr int NW = decltype(nw_c)::value;
         const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16);
         const uint64_t ah = abase + (uint64_t)(kh * hrow16 + kw0 * px16);
 #pragma unroll
-        for (int kw = 0; kw < NTAP; ++kw)
+        for (int j = 0; j < NTAP; ++j)
 #pragma unroll
             for (int sq = 0; sq < NQ; ++sq)
                 issue_tap_halo<kPair, KK, NSUB, NP>(
                     p, dacc + (uint32_t)(sq * p.acc_cols),
-                    ah + (uint64_t)((kw + 8 * sq) * px16), b0 + (uint64_t)(kw * tap_b16),
-                    b_sub16, a_sub16, a_kk16, idesc, first && kw == 0);
+                    ah + (uint64_t)((j / NW) * hrow16 + (j % NW + 8 * sq) * px16),
+                    b0 + (uint64_t)(j * tap_b16), b_sub16, a_sub16, a_kk16, idesc,
+                    first && j == 0);
     };
     using I1 = std::integral_constant<int, 1>;
     using I2 = std::integral_constant<int, 2>;
     using I3 = std::integral_constant<int, 3>;
+    using I4 = std::integral_constant<int, 4>;
     for (int u = unit0; ok && u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
@@ -614,25 +638,29 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         tc_fence_after();
         const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
+        const TapBase tbase = unit_tap_base(u, p);
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
                 const uint64_t abase = adesc0 + (uint64_t)(ia * astride16);
                 // the first stage of (kt, cc) also carries the halo
-                const int nst = tb3 ? 3 : 9;
+                const int nst = p.sp_taps / p.tb;
                 for (int g = 0; g < nst; ++g) {
                     if (!ring.acquire(bars, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int kh = tb3 ? g : g / 3, kw0 = tb3 ? 0 : g - 3 * (g / 3);
+                    const int q0 = g * p.tb;  // the stage's first spatial tap
+                    const int kh = tbase.kh + q0 / p.sp_w, kw0 = tbase.kw + q0 % p.sp_w;
                     if (p.nq == 2) {
-                        if (tb3) stage(I2{}, I3{}, dacc, abase, kh, kw0, first);
-                        else stage(I2{}, I1{}, dacc, abase, kh, kw0, first);
+                        if (tb3) stage(I2{}, I3{}, I3{}, dacc, abase, kh, kw0, first);
+                        else if (tb4) stage(I2{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
+                        else stage(I2{}, I1{}, I1{}, dacc, abase, kh, kw0, first);
                     } else {
-                        if (tb3) stage(I1{}, I3{}, dacc, abase, kh, kw0, first);
-                        else stage(I1{}, I1{}, dacc, abase, kh, kw0, first);
+                        if (tb3) stage(I1{}, I3{}, I3{}, dacc, abase, kh, kw0, first);
+                        else if (tb4) stage(I1{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
+                        else stage(I1{}, I1{}, I1{}, dacc, abase, kh, kw0, first);
                     }
                     first = false;
                     commit(bars.empty(ring.stage));
@@ -1538,14 +1566,16 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
             const uint32_t ha =
                 pl.halo_rows ? (uint32_t)d * pl.sub_stride
                              : ((uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u + 1023u) & ~1023u;
-            for (int tb = 3; tb >= 1; tb -= 2) {
+            // 3-tap stages (a row of the 3 x 3 taps), or for the upsampler
+            // 4-tap stages (a phase's 2 x 2 taps); else one tap per stage
+            for (int tb = s.up2d ? 4 : 3; tb >= 1; tb = tb > 1 ? 1 : 0) {
                 if (tb > 1 && pl.n_pieces != 1) continue;
                 const uint32_t bs = ((uint32_t)(tb * d) * b_rows * sw * 2u + 1023u) & ~1023u;
                 if (2u * ha + reserve >= (uint32_t)kSmemBudget) continue;
                 int st = (int)(((uint32_t)kSmemBudget - reserve - 2u * ha) / bs);
                 if (st > 8) st = 8;
                 if (st < (tb > 1 ? 3 : need_stages)) continue;
-                const int waits = 27 * (g_main / d) / tb + (s.sc_in ? g_sc / d : 0);
+                const int waits = (s.up2d ? 4 : 27) * (g_main / d) / tb + (s.sc_in ? g_sc / d : 0);
                 if (!pl.nsub || waits < best_waits || (waits == best_waits && st > best_stages)) {
                     pl.nsub = d;
                     pl.tb = tb;
@@ -1597,13 +1627,17 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     // Small c_in (one chunk of at most 32 channels): one k-step or two per tap
     // would cost the MMA issuer a barrier wait per one or two MMAs, so a stage
     // holds three consecutive taps (same K order as one tap per stage).
+    // (The upsampler's four taps per phase: two or four per stage.)
     pl.itb = 1;
     if (s.k == 3 && !s.sc_in && pl.kc_main == 1 && pl.nsub * sw <= 32) {
-        const uint32_t sb3 = 3u * (uint32_t)pl.nsub * (kBlockM + b_rows) * sw * 2u;
-        if ((uint32_t)need_stages * ((sb3 + 1023u) & ~1023u) + reserve <=
-            (uint32_t)kSmemBudget) {
-            pl.itb = 3;
-            pl.nsub *= 3;
+        for (int itb : {s.up2d ? 4 : 3, s.up2d ? 2 : 3}) {
+            const uint32_t sbt = (uint32_t)itb * pl.nsub * (kBlockM + b_rows) * sw * 2u;
+            if (pl.itb == 1 &&
+                (uint32_t)need_stages * ((sbt + 1023u) & ~1023u) + reserve <=
+                    (uint32_t)kSmemBudget) {
+                pl.itb = itb;
+                pl.nsub *= itb;
+            }
         }
     }
     pl.a_sub = (uint32_t)kBlockM * sw * 2;
@@ -1778,11 +1812,11 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
         ok = ok && encode_2d(&mA, s.in, (uint64_t)s.c_in, (uint64_t)M, pl.sw, kBlockM, pl.sw);
     }
     if (pl.halo && pl.tb > 1)
-        ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)(s.up2d ? 9 : 27) * s.c_in, s.c_in,
+        ok = ok && encode_weight_taps(&mB, s.w, (uint64_t)(s.up2d ? 4 : 27) * s.c_in, s.c_in,
                                       s.c_out, pl.pair, pl.sw, pl.nsub, pl.tb, pl.npad,
                                       s.up2d ? 4 : 1);
     else
-        ok = ok && encode_weights(&mB, s.w, (uint64_t)(s.up2d ? 9 : s.k * s.k * s.k) * s.c_in,
+        ok = ok && encode_weights(&mB, s.w, (uint64_t)(s.up2d ? 4 : s.k * s.k * s.k) * s.c_in,
                                   s.c_out, pl.pair, pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0,
                                   pl.npad, s.up2d ? 4 : 1);
     if (s.sc_in) {
@@ -1844,6 +1878,8 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.nphase = s.up2d ? 4 : 1;
     a.tile_units = (a.num_tiles + pl.pair - 1) / pl.pair;
     a.wtap0 = s.up2d ? 18 : 0;
+    a.sp_taps = s.up2d ? 4 : 9;
+    a.sp_w = s.up2d ? 2 : 3;
     // which B box coordinate a phase moves: the rank dimension of the 3-tap
     // map (its pieces are one), else the piece dimension
     const bool taps_map = pl.halo && pl.tb > 1;

@@ -28,9 +28,9 @@ cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool
 cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,
                                 const LaunchCtx &ctx);
 
-// Phase-expanded weights of the upsampler conv: w [Co][3][3][Ci] ->
-// w4 [4][Co][3][3][Ci] (bf16), see rmsnorm_silu.cu.
-cudaError_t launch_expand_up2d_weights(const void *w, void *w4, int Co, int Ci,
+// Sub-pixel weights of the upsampler conv: w [Co][3][3][Ci] ->
+// w2 [4 phases][Co][2][2][Ci] (bf16), see rmsnorm_silu.cu.
+cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
                                        const LaunchCtx &ctx);
 
 // Epilogue of the implicit-GEMM conv.
@@ -60,9 +60,10 @@ struct ConvSpec {
     int k;               // 3 or 1
     int epi;             // EpiMode
     // Spatial upsampler conv: nearest 2x in H and W then a 3x3 conv, as four
-    // sub-pixel phases over the low-res input (H x W here).  w holds the
-    // phase-expanded weights [4][c_out][3][3][c_in] (only the current frame's
-    // taps), out is [B][T][2H][2W][c_out]; k = 3, no cache, bias epilogue.
+    // sub-pixel phases over the low-res input (H x W here), each a 2 x 2 conv.
+    // w holds the sub-pixel weights [4][c_out][2][2][c_in] (the current
+    // frame's taps only), out is [B][T][2H][2W][c_out]; k = 3, no cache, bias
+    // epilogue.
     int up2d;
 };
 

@@ -193,46 +193,47 @@ __global__ void cache_update_kernel(uint4 *__restrict__ cache, const uint4 *__re
     }
 }
 
-// Phase-expanded weights of the upsampler conv.  Nearest 2x upsampling then
-// a 3x3 conv gives output pixel (2i + a, 2j + b) as a 3x3 conv over the
-// low-res input at (i, j) whose taps are sums of the original ones: tap
-// (kh, kw) of the upsampled grid reads low-res row i + floor((a + kh - 1) / 2)
-// (offsets -1, 0, 0 for a = 0 and 0, 0, 1 for a = 1), likewise for columns.
-// w [Co][3][3][Ci] -> w4 [4 = 2a + b][Co][3][3][Ci], fp32 sums rounded to bf16.
+// Sub-pixel weights of the upsampler conv.  Nearest 2x upsampling then a 3x3
+// conv gives output pixel (2i + a, 2j + b) as a conv over the low-res input
+// around (i, j): tap (kh, kw) of the upsampled grid reads low-res row
+// i + floor((a + kh - 1) / 2) (offsets -1, 0, 0 for a = 0 and 0, 0, 1 for
+// a = 1), likewise for columns, so each phase (a, b) touches only the 2 x 2
+// low-res offsets (a + e - 1, b + f - 1), e, f in {0, 1}, and its tap (e, f)
+// is the sum of the original taps that land there.
+// w [Co][3][3][Ci] -> w2 [4 = 2a + b][Co][2][2][Ci], fp32 sums rounded to bf16.
 __global__ void expand_up2d_weights_kernel(const __nv_bfloat16 *__restrict__ w,
-                                           __nv_bfloat16 *__restrict__ w4, int Co, int Ci) {
-    const int64_t total = (int64_t)4 * Co * 9 * Ci;
+                                           __nv_bfloat16 *__restrict__ w2, int Co, int Ci) {
+    const int64_t total = (int64_t)4 * Co * 4 * Ci;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(idx % Ci);
         int64_t r = idx / Ci;
-        const int dw = (int)(r % 3);
-        r /= 3;
-        const int dh = (int)(r % 3);
-        r /= 3;
+        const int f = (int)(r & 1);
+        const int e = (int)((r >> 1) & 1);
+        r >>= 2;
         const int o = (int)(r % Co);
         const int ph = (int)(r / Co), a = ph >> 1, b = ph & 1;
         float acc = 0.f;
         for (int kh = 0; kh < 3; ++kh) {
-            if (((a + kh + 1) >> 1) != dh) continue;  // floor((a + kh - 1) / 2) + 1
+            if (((a + kh + 1) >> 1) != a + e) continue;  // floor((a + kh - 1) / 2) + 1
             for (int kw = 0; kw < 3; ++kw) {
-                if (((b + kw + 1) >> 1) != dw) continue;
+                if (((b + kw + 1) >> 1) != b + f) continue;
                 acc += __bfloat162float(w[((int64_t)(o * 3 + kh) * 3 + kw) * Ci + c]);
             }
         }
-        w4[idx] = __float2bfloat16_rn(acc);
+        w2[idx] = __float2bfloat16_rn(acc);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_expand_up2d_weights(const void *w, void *w4, int Co, int Ci,
+cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
                                        const LaunchCtx &ctx) {
-    const int64_t total = (int64_t)4 * Co * 9 * Ci;
+    const int64_t total = (int64_t)4 * Co * 4 * Ci;
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)ctx.num_sms * 8) blocks = (int64_t)ctx.num_sms * 8;
     expand_up2d_weights_kernel<<<(unsigned)blocks, 256, 0, ctx.stream>>>(
-        static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w4), Co, Ci);
+        static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2), Co, Ci);
     return cudaGetLastError();
 }
 
