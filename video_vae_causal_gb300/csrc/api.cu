@@ -372,7 +372,9 @@ wanvae_status wanvae_sync_status(wanvae_stream stream) {
         const unsigned zero = 0;
         if (cudaMemcpyToSymbol(g_wanvae_err, &zero, sizeof(zero)) != cudaSuccess)
             return WANVAE_ERR_CUDA;
-        return WANVAE_ERR_TIMEOUT;
+        // bit 0: a bounded device wait gave up; other bits: a kernel skipped an
+        // access its own checks refused
+        return v == 1u ? WANVAE_ERR_TIMEOUT : WANVAE_ERR_CUDA;
     }
     return WANVAE_OK;
 }

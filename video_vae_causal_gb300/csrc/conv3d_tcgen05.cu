@@ -71,6 +71,8 @@ struct ConvArgs {
     int tile_units;      // units per phase: ceil(num_tiles / pair)
     int wtap0;           // 9 x the temporal tap the weights start at (18: upsampler, kt = 2 only)
     int sp_taps, sp_w;   // spatial taps per temporal tap and per tap row: 9, 3 (upsampler: 4, 2)
+    int na;              // halo mode: buffers in the A (halo) ring, 2 to 4
+    int up_tma;          // upsampler on halo tiles: TMA stores through the phase view of y
     int ph_c2, ph_c3;    // upsampler: B box coordinates 2 and 3 advance by phase x these
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
@@ -411,7 +413,7 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
     auto next_abuf = [&](uint32_t &dst) -> bool {
         if (!mbar_wait<kPair == 2>(bars.emptya(ia), pha ^ 1u, wc)) return false;
         dst = sbase + p.off_a + (uint32_t)ia * p.a_stride;
-        if (++ia == 2) {
+        if (++ia == p.na) {
             ia = 0;
             pha ^= 1u;
         }
@@ -668,7 +670,7 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
                 }
                 if (!ok) break;
                 commit(bars.emptya(ia));
-                ia ^= 1;
+                if (++ia == p.na) ia = 0;
             }
         }
         for (int cc = 0; ok && cc < p.kc_short; ++cc) {
@@ -687,7 +689,7 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
             commit(bars.empty(ring.stage));
             commit(bars.emptya(ia));
             ring.advance(bars);
-            ia ^= 1;
+            if (++ia == p.na) ia = 0;
         }
         if (!ok) break;
         commit(bars.accf(a));
@@ -828,9 +830,9 @@ __device__ __forceinline__ void store_chunk(uint8_t *stg, const uint32_t (&o)[16
 // through shared memory.
 template <int kPair>
 __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
-                              const float *s_gamma, float *s_part, uint8_t *stg, const Bars &bars,
-                              const WaitCtl &wc, int unit0, int unit_stride, int num_units,
-                              uint32_t rank) {
+                              const float *s_gamma, float *s_part, uint8_t *stg,
+                              const CUtensorMap *mapY, const Bars &bars, const WaitCtl &wc,
+                              int unit0, int unit_stride, int num_units, uint32_t rank) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;           // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2; // 0 or 1: which column half
@@ -838,6 +840,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
     const int c_split = ((p.c_out / 2) + 15) / 16 * 16;
     const int c_begin = half ? c_split : 0, c_end = half ? p.c_out : c_split;
     int it = 0;
+    uint32_t nst = 0;  // staging half of this warp's next TMA store (upsampler)
     for (int u = unit0; u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
@@ -946,7 +949,40 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 uint32_t o[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                if (p.nphase > 1) {
+                if (p.up_tma) {
+                    // Upsampler on halo tiles: the warp's 4 x 8 low-res pixels
+                    // are one box of the phase view of y (its pixels 2 apart),
+                    // 16 channels per store, staged through two 1 KB halves of
+                    // the warp's buffer; the view clips what lies past W or H.
+                    const int ph = unit_phase(u, p);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (16 * h < n) {
+                            uint8_t *buf = stg + (nst & 1) * 1024;
+                            if (lane == 0) bulk_wait_read_but1();  // its last store has read it
+                            __syncwarp();
+                            uint4 *d = reinterpret_cast<uint4 *>(buf + lane * 32);
+                            d[0] = make_uint4(o[8 * h], o[8 * h + 1], o[8 * h + 2], o[8 * h + 3]);
+                            d[1] = make_uint4(o[8 * h + 4], o[8 * h + 5], o[8 * h + 6],
+                                              o[8 * h + 7]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            const uint32_t src = smem_u32(buf);
+                            if (lane == 0 && !ti.dummy && ti.h0 + 4 * q < p.H &&
+                                ti.w0 + 8 * sub < p.W) {  // (a box past the frame: nothing)
+                                if (src & 127u) {  // a bulk tensor copy needs 128-byte alignment
+                                    atomicOr(p.err, kDevErrAlign);
+                                } else {
+                                    tma_store_5d(mapY, src, (ph & 1) * p.c_out + c + 16 * h,
+                                                 ti.w0 + 8 * sub, ph >> 1, ti.h0 + 4 * q,
+                                                 ti.frame);
+                                    bulk_commit();
+                                }
+                            }
+                            ++nst;
+                        }
+                    }
+                } else if (p.nphase > 1) {
                     // Upsampler: low-res pixel (i, j) of this row is output
                     // pixel (2i + a, 2j + b) of the unit's phase (a, b).
                     if (valid) {
@@ -979,6 +1015,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 mbar_arrive(bars.acce(a));
         }
     }
+    if (p.up_tma && lane == 0) bulk_wait_all();  // stores done before the CTA leaves
 }
 
 // Whole-tile staged epilogue (one TMEM accumulator, c_out a multiple of 64).
@@ -1154,7 +1191,9 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
     float *s_part = s_gamma + p.c_out;  // [2 sub-tiles][2][128] partial sums of squares
-    uint8_t *s_stage = reinterpret_cast<uint8_t *>(s_part + 4 * kBlockM);  // output staging
+    // output staging, 128-byte aligned: the upsampler's TMA stores read it
+    uint8_t *s_stage = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(s_part + 4 * kBlockM) + 127) & ~static_cast<uintptr_t>(127));
 
     // Work units: single tiles, or pairs of consecutive tiles per cluster.
     const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
@@ -1173,7 +1212,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         mbar_init(bars.drain(), 1);
         mbar_init(bars.resf(), 1);
-        for (int i = 0; i < 2; ++i) mbar_init(bars.emptya(i), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bars.emptya(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1239,8 +1278,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                                         unit_stride, num_units, rank);
         else
             conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, s_part,
-                                 s_stage + (threadIdx.x / 32 - 2) * kStageBytesPerWarp, bars, wc,
-                                 unit0, unit_stride, num_units, rank);
+                                 s_stage + (threadIdx.x / 32 - 2) * kStageBytesPerWarp, &mapY,
+                                 bars, wc, unit0, unit_stride, num_units, rank);
     }
     __syncwarp();
     tc_fence_before();
@@ -1436,6 +1475,24 @@ bool encode_patch(CUtensorMap *m, const void *base, int C, int W, int H, int fra
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The upsampler's output y [frames][2H][2W][C] seen per sub-pixel phase
+// (a, b): as (b C + c, j, a, i, frame), the element at phase coordinates
+// b C + c (dimension 0 spans both column phases' channels), column j, row
+// phase a, row i is y[frame][2i + a][2j + b][c].  A (16, 8, 1, 4, 1) box is
+// one epilogue warp's 4 x 8 low-res pixels of one phase, 16 channels each.
+bool encode_phase_view(CUtensorMap *m, const void *base, int C, int W, int H, int frames) {
+    cuuint64_t dims[5] = {(cuuint64_t)2 * C, (cuuint64_t)W, 2, (cuuint64_t)H,
+                          (cuuint64_t)frames};
+    cuuint64_t strides[4] = {(cuuint64_t)2 * C * 2, (cuuint64_t)2 * W * C * 2,
+                             (cuuint64_t)4 * W * C * 2, (cuuint64_t)4 * H * W * C * 2};
+    cuuint32_t box[5] = {16, 8, 1, 4, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int pick_sw(int c) { return c % 64 == 0 ? 64 : (c % 32 == 0 ? 32 : 16); }
 
 struct Plan {
@@ -1455,6 +1512,7 @@ struct Plan {
     int halo_rows;        // halo layout: swizzled pixel rows (sw = 64) or 8-channel planes
     int acc_stride;
     uint32_t off_a, a_stride, a_tx;
+    int na;  // halo mode: A ring buffers
 };
 
 // Halo tiles (16 x 8 patches, one halo load per temporal tap and channel
@@ -1593,8 +1651,14 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.a_tx = (uint32_t)(pl.halo_w * kHaloH) * d * sw * 2u;
         pl.a_stride = pl.halo_rows ? (uint32_t)d * pl.sub_stride : (pl.a_tx + 1023u) & ~1023u;
         pl.off_a = 0;
-        pl.a_bytes = 2u * pl.a_stride;  // the weight ring starts here
         pl.stage_bytes = (pl.b_sub * d * (uint32_t)pl.tb + 1023u) & ~1023u;
+        // A halo of the upsampler feeds a single stage (one phase's four
+        // taps), so two halo buffers would let its loads run only one stage
+        // ahead of the MMAs: a third where three weight stages still fit.
+        pl.na = 2;
+        if (s.up2d && 3u * pl.a_stride + 3u * pl.stage_bytes + reserve <= (uint32_t)kSmemBudget)
+            pl.na = 3;
+        pl.a_bytes = (uint32_t)pl.na * pl.a_stride;  // the weight ring starts here
         pl.stages = (int)((kSmemBudget - reserve - pl.a_bytes) / pl.stage_bytes);
         if (pl.stages > 8) pl.stages = 8;
         if (pl.stages < 2) return false;
@@ -1602,9 +1666,9 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.off_stage = off;
         if (pl.staged) off += stage_tile;
         pl.off_bars = off;
-        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 8);
+        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
         pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
+        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM + 128u +
                         (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
         if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
         return pl.smem_bytes <= (uint32_t)kSmemBudget;
@@ -1612,6 +1676,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.off_a = 0;
     pl.a_stride = 0;
     pl.a_tx = 0;
+    pl.na = 2;
     pl.tb = 1;
     pl.nsub = 1;
     for (int d = 4; d >= 1; --d) {
@@ -1651,9 +1716,9 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.off_stage = off;
     if (pl.staged) off += stage_tile;
     pl.off_bars = off;
-    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 8);
+    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
+    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM + 128u +
                     (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
     if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
@@ -1838,6 +1903,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
             if (s.epi == kEpiResidual) ok = ok && encode_frames(&mR, s.resid, s.c_out, HW, frames);
         }
     }
+    if (s.up2d && pl.halo) ok = ok && encode_phase_view(&mY, s.out, s.c_out, s.W, s.H, frames);
     if (!ok) return cudaErrorInvalidValue;
 
     ConvArgs a;
@@ -1871,6 +1937,8 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.bc_rank = pl.narrow ? 0 : 1;
     a.off_a = pl.off_a;
     a.a_stride = pl.a_stride;
+    a.na = pl.na;
+    a.up_tma = s.up2d && pl.halo;
     a.a_tx = pl.a_tx;
     a.tiles_per_frame = pl.halo ? ((s.H + 15) / 16) * a.patches_w : (HW + kBlockM - 1) / kBlockM;
     a.num_tiles = a.tiles_per_frame * frames;

@@ -10,7 +10,10 @@
 namespace wanvae {
 
 // Device error bits, OR-ed into the flag the host reads back.
-enum : unsigned { kDevErrTimeout = 1u };
+enum : unsigned {
+    kDevErrTimeout = 1u,  // a bounded wait gave up
+    kDevErrAlign = 2u,    // a TMA store's shared-memory source was misaligned (skipped)
+};
 
 // How long a bounded wait may spin before giving up, and where it reports.
 struct WaitCtl {
@@ -227,12 +230,25 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src,
         "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap *m, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::
+            "l"(reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 // Wait until every committed bulk store has finished READING shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until all but the newest committed bulk store have finished READING
+// shared memory.
+__device__ __forceinline__ void bulk_wait_read_but1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait_all() {
