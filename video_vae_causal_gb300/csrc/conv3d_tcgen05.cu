@@ -71,6 +71,7 @@ struct ConvArgs {
     int tile_units;      // units per phase: ceil(num_tiles / pair)
     int wtap0;           // 9 x the temporal tap the weights start at (18: upsampler, kt = 2 only)
     int sp_taps, sp_w;   // spatial taps per temporal tap and per tap row: 9, 3 (upsampler: 4, 2)
+    int segs_per_kt;     // im2col: stages per temporal tap and channel chunk, sp_taps / itb
     int na;              // halo mode: buffers in the A (halo) ring, 2 to 4
     int up_tma;          // upsampler on halo tiles: TMA stores through the phase view of y
     int ph_c2, ph_c3;    // upsampler: B box coordinates 2 and 3 advance by phase x these
@@ -193,7 +194,7 @@ __device__ __forceinline__ int unit_first_kt(int unit, const ConvArgs &p) {
 template <int kPair>
 __device__ __forceinline__ int unit_stages(int unit, const ConvArgs &p) {
     const int main_taps =
-        p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * p.sp_taps / p.itb : 1;
+        p.taps == 27 ? (3 - unit_first_kt<kPair>(unit, p)) * p.segs_per_kt : 1;
     return main_taps * p.kc_main + p.kc_short;
 }
 
@@ -232,7 +233,7 @@ struct FullRing {
 // TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
 // 128-row A tile and its half of every B piece; all loads complete on the
 // leader CTA's `full` barrier, which the leader arms for both CTAs' bytes.
-template <int kPair>
+template <int kPair, bool kUp>
 __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                               const CUtensorMap *mapB, const CUtensorMap *mapSA,
                               const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
@@ -248,8 +249,8 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         // A segment is itb consecutive taps (one tap unless c_in is small),
         // each stage of it itb taps x nch channel sub-tiles.
-        const int nseg = p.taps == 27 ? (3 - kt0) * p.sp_taps / p.itb : 1;
-        const TapBase tbase = unit_tap_base(u, p);
+        const int nseg = p.taps == 27 ? (3 - kt0) * p.segs_per_kt : 1;
+        const TapBase tbase = kUp ? unit_tap_base(u, p) : TapBase{0, 0};
         const int segs = nseg + (p.kc_short > 0 ? 1 : 0);
         const int row0 = ti.dummy ? M : ti.row0;
         for (int seg = 0; ok && seg < segs; ++seg) {
@@ -271,11 +272,22 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                     int wtap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
                     const CUtensorMap *am = mapA;
                     if (!shortcut && p.taps == 27) {
+                        // (constant divisors on either path: this thread must
+                        // keep ahead of the MMAs)
                         const int q = seg * p.itb + j;
-                        const int kt = kt0 + q / p.sp_taps, qs = q - (q / p.sp_taps) * p.sp_taps;
-                        kh = tbase.kh + qs / p.sp_w;
-                        kw = tbase.kw + qs % p.sp_w;
-                        wtap = (kt - p.wtap0 / 9) * p.sp_taps + qs;
+                        int kt;
+                        if (kUp) {  // the phase's 2 x 2 taps, current frame only
+                            kt = 2;
+                            kh = tbase.kh + ((q >> 1) & 1);
+                            kw = tbase.kw + (q & 1);
+                            wtap = q & 3;
+                        } else {
+                            const int tap = kt0 * 9 + q;
+                            kt = tap / 9;
+                            kh = (tap / 3) % 3;
+                            kw = tap % 3;
+                            wtap = tap;
+                        }
                         const int tt = ti.t + kt - 2;
                         if (!ti.dummy) {
                             if (tt >= 0) {
@@ -312,7 +324,7 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                         const uint32_t db = sb + (uint32_t)idx * p.b_sub_bytes;
                         const CUtensorMap *bm = shortcut ? mapSB : mapB;
                         const int bk = shortcut ? c0 : wtap * p.c_in + c0;
-                        const int ph = unit_phase(u, p);  // upsampler: the phase's weight rows
+                        const int ph = kUp ? unit_phase(u, p) : 0;  // upsampler: its weights
                         if (kPair == 2)
                             tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
                                              (int)rank * p.bc_rank + ph * p.ph_c2,
@@ -383,7 +395,7 @@ __device__ __forceinline__ void load4(uint32_t dst, const CUtensorMap *m, uint32
 // spatial taps each (B ring); the halo completes on the barrier of the first
 // of those stages, so the MMA issuer waits once per stage.  Then the shortcut
 // segment's chunks (x patch into the A ring + its weights, one stage each).
-template <int kPair>
+template <int kPair, bool kUp>
 __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *mapC,
                                    const CUtensorMap *mapB, const CUtensorMap *mapSA,
                                    const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
@@ -458,7 +470,7 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                     }
                     // tb consecutive spatial taps of this chunk in one box
                     const int wtap = (kt - p.wtap0 / 9) * p.sp_taps + g * p.tb;
-                    const int ph = unit_phase(u, p);  // upsampler: the phase's weight rows
+                    const int ph = kUp ? unit_phase(u, p) : 0;  // upsampler: its weights
                     load5<kPair>(db, mapB, fb, wtap * p.c_in + cc * chunk,
                                  (int)rank * p.bc_row, (int)rank * p.bc_rank + ph * p.ph_c2,
                                  ph * p.ph_c3, 0);
@@ -576,7 +588,7 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
 // released after the ninth tap.  Descriptors are the ring bases plus
 // offsets, so nothing but the stage bookkeeping sits between two stages'
 // MMAs.
-template <int kPair, int KK, int NSUB, int NP>
+template <int kPair, int KK, int NSUB, int NP, bool kUp>
 __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base,
                               const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
                               int num_units) {
@@ -596,7 +608,8 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
     const uint64_t adesc0 =
         p.halo_rows ? sdesc_kmajor_sbo(sbase + p.off_a, (uint32_t)p.halo_w * row_bytes, p.layout)
                     : sdesc_plain(sbase + p.off_a, p.plane_bytes, (uint32_t)p.halo_w * 16u);
-    const bool tb3 = p.tb == 3, tb4 = p.tb == 4;
+    const bool tb3 = p.tb == 3, tb4 = kUp && p.tb == 4;
+    const int nst = p.tb == 1 ? p.sp_taps : (tb3 ? 3 : 1);  // weight stages per (kt, chunk)
     FullRing<kPair == 2> ring;
     int ia = 0, it = 0;
     bool ok = true;
@@ -640,33 +653,38 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         tc_fence_after();
         const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
-        const TapBase tbase = unit_tap_base(u, p);
+        const TapBase tbase = kUp ? unit_tap_base(u, p) : TapBase{0, 0};
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
                 const uint64_t abase = adesc0 + (uint64_t)(ia * astride16);
-                // the first stage of (kt, cc) also carries the halo
-                const int nst = p.sp_taps / p.tb;
+                // the first stage of (kt, cc) also carries the halo; the
+                // stage's first tap (kh, kw0) steps by tb along rows of sp_w
+                int kh = tbase.kh, kw0 = tbase.kw;
                 for (int g = 0; g < nst; ++g) {
                     if (!ring.acquire(bars, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int q0 = g * p.tb;  // the stage's first spatial tap
-                    const int kh = tbase.kh + q0 / p.sp_w, kw0 = tbase.kw + q0 % p.sp_w;
+                    // (4-tap stages exist in the upsampler's kernels only)
                     if (p.nq == 2) {
                         if (tb3) stage(I2{}, I3{}, I3{}, dacc, abase, kh, kw0, first);
-                        else if (tb4) stage(I2{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
+                        else if (kUp && tb4) stage(I2{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
                         else stage(I2{}, I1{}, I1{}, dacc, abase, kh, kw0, first);
                     } else {
                         if (tb3) stage(I1{}, I3{}, I3{}, dacc, abase, kh, kw0, first);
-                        else if (tb4) stage(I1{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
+                        else if (kUp && tb4) stage(I1{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
                         else stage(I1{}, I1{}, I1{}, dacc, abase, kh, kw0, first);
                     }
                     first = false;
                     commit(bars.empty(ring.stage));
                     ring.advance(bars);
+                    kw0 += p.tb;
+                    if (kw0 - tbase.kw >= p.sp_w) {  // tb is 1, a whole row or a whole phase
+                        kw0 = tbase.kw;
+                        kh += p.tb > p.sp_w ? 2 : 1;
+                    }
                 }
                 if (!ok) break;
                 commit(bars.emptya(ia));
@@ -828,7 +846,7 @@ __device__ __forceinline__ void store_chunk(uint8_t *stg, const uint32_t (&o)[16
 // rule -- and owns half of the columns (half (w - 2) / 4), so two warps share
 // every row.  The fused RMS_norm combines their two partial sums of squares
 // through shared memory.
-template <int kPair>
+template <int kPair, bool kUp>
 __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float *s_bias,
                               const float *s_gamma, float *s_part, uint8_t *stg,
                               const CUtensorMap *mapY, const Bars &bars, const WaitCtl &wc,
@@ -949,7 +967,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 uint32_t o[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                if (p.up_tma) {
+                if (kUp && p.up_tma) {
                     // Upsampler on halo tiles: the warp's 4 x 8 low-res pixels
                     // are one box of the phase view of y (its pixels 2 apart),
                     // 16 channels per store, staged through two 1 KB halves of
@@ -982,7 +1000,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                             ++nst;
                         }
                     }
-                } else if (p.nphase > 1) {
+                } else if (kUp) {
                     // Upsampler: low-res pixel (i, j) of this row is output
                     // pixel (2i + a, 2j + b) of the unit's phase (a, b).
                     if (valid) {
@@ -1015,7 +1033,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 mbar_arrive(bars.acce(a));
         }
     }
-    if (p.up_tma && lane == 0) bulk_wait_all();  // stores done before the CTA leaves
+    if (kUp && p.up_tma && lane == 0) bulk_wait_all();  // stores done before the CTA leaves
 }
 
 // Whole-tile staged epilogue (one TMEM accumulator, c_out a multiple of 64).
@@ -1171,7 +1189,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
     }
 }
 
-template <int kPair, int KK, int NSUB, int NP>
+template <int kPair, int KK, int NSUB, int NP, bool kUp>
 __global__ void __launch_bounds__(kThreads, 1)
 conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapC,
@@ -1191,9 +1209,11 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
     float *s_part = s_gamma + p.c_out;  // [2 sub-tiles][2][128] partial sums of squares
-    // output staging, 128-byte aligned: the upsampler's TMA stores read it
+    // output staging; 128-byte aligned where the upsampler's TMA stores read it
+    // (the plan reserves the slack for that case only)
+    const uintptr_t stg0 = reinterpret_cast<uintptr_t>(s_part + 4 * kBlockM);
     uint8_t *s_stage = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(s_part + 4 * kBlockM) + 127) & ~static_cast<uintptr_t>(127));
+        p.up_tma ? (stg0 + 127) & ~static_cast<uintptr_t>(127) : stg0);
 
     // Work units: single tiles, or pairs of consecutive tiles per cluster.
     const uint32_t rank = kPair == 2 ? cluster_ctarank() : 0u;
@@ -1256,16 +1276,16 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     if (warp == 0) {
         if (lane == 0) {
             if (p.halo)
-                conv_producer_halo<kPair>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
+                conv_producer_halo<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
                                           unit0, unit_stride, num_units, rank);
             else
-                conv_producer<kPair>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
+                conv_producer<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
                                      unit0, unit_stride, num_units, rank);
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             if (p.halo)
-                conv_mma_halo<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0,
+                conv_mma_halo<kPair, KK, NSUB, NP, kUp>(p, sbase, tmem_base, bars, wc, unit0,
                                                    unit_stride, num_units);
             else
                 conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
@@ -1277,7 +1297,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                                         smem + p.off_stage, &mapY, &mapR, bars, wc, unit0,
                                         unit_stride, num_units, rank);
         else
-            conv_epilogue<kPair>(p, tmem_base, s_bias, s_gamma, s_part,
+            conv_epilogue<kPair, kUp>(p, tmem_base, s_bias, s_gamma, s_part,
                                  s_stage + (threadIdx.x / 32 - 2) * kStageBytesPerWarp, &mapY,
                                  bars, wc, unit0, unit_stride, num_units, rank);
     }
@@ -1668,7 +1688,8 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.off_bars = off;
         pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
         pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM + 128u +
+        pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
+                        (s.up2d ? 128u : 0u) /*staging alignment for TMA stores*/ +
                         (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
         if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
         return pl.smem_bytes <= (uint32_t)kSmemBudget;
@@ -1718,7 +1739,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.off_bars = off;
     pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
-    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM + 128u +
+    pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                     (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
     if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
@@ -1735,8 +1756,10 @@ typedef void (*ConvKernelFn)(const CUtensorMap, const CUtensorMap, const CUtenso
 template <int kPair>
 ConvKernelFn pick_kernel(int kk, int nsub, int np) {
 #define WANVAE_CONV_SPEC(KK_, NS_)                                                     \
-    if (kk == KK_ && nsub == NS_ && np == 1) return conv3d_tcgen05_kernel<kPair, KK_, NS_, 1>; \
-    if (kk == KK_ && nsub == NS_ && np == 2) return conv3d_tcgen05_kernel<kPair, KK_, NS_, 2>;
+    if (kk == KK_ && nsub == NS_ && np == 1)                                           \
+        return conv3d_tcgen05_kernel<kPair, KK_, NS_, 1, false>;                       \
+    if (kk == KK_ && nsub == NS_ && np == 2)                                           \
+        return conv3d_tcgen05_kernel<kPair, KK_, NS_, 2, false>;
     WANVAE_CONV_SPEC(4, 1)
     WANVAE_CONV_SPEC(4, 2)
     WANVAE_CONV_SPEC(2, 1)
@@ -1748,7 +1771,16 @@ ConvKernelFn pick_kernel(int kk, int nsub, int np) {
     WANVAE_CONV_SPEC(1, 3)
     WANVAE_CONV_SPEC(1, 4)
 #undef WANVAE_CONV_SPEC
-    return conv3d_tcgen05_kernel<kPair, 0, 0, 0>;
+    return conv3d_tcgen05_kernel<kPair, 0, 0, 0, false>;
+}
+
+// The upsampler's kernels (its phase and sub-pixel-tap code kept out of the
+// others' register budget): 64-channel sub-tiles unrolled, run-time loops
+// otherwise.
+template <int kPair>
+ConvKernelFn pick_kernel_up(int kk, int nsub, int np) {
+    if (kk == 4 && nsub == 1 && np == 1) return conv3d_tcgen05_kernel<kPair, 4, 1, 1, true>;
+    return conv3d_tcgen05_kernel<kPair, 0, 0, 0, true>;
 }
 
 // Per-device, per-kernel launch facts: the dynamic shared-memory opt-in and
@@ -1838,14 +1870,20 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     Plan pl;
     if (!pick_plan(s, pl, pair_choice())) return cudaErrorInvalidValue;
     if (!load_encoders()) return cudaErrorInvalidValue;
-    ConvKernelFn fn = pl.pair == 2 ? pick_kernel<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
-                                   : pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
+    auto pick = [&](int pair) {
+        if (s.up2d)
+            return pair == 2 ? pick_kernel_up<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
+                             : pick_kernel_up<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
+        return pair == 2 ? pick_kernel<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
+                         : pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
+    };
+    ConvKernelFn fn = pick(pl.pair);
     int max_pairs = 0;
     cudaError_t fe = kernel_facts(fn, pl.pair == 2, max_pairs);
     if (fe != cudaSuccess) return fe;
     if (pl.pair == 2 && max_pairs < 1) {
         if (!pick_plan(s, pl, 1)) return cudaErrorInvalidValue;
-        fn = pick_kernel<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
+        fn = pick(1);
         fe = kernel_facts(fn, false, max_pairs);
         if (fe != cudaSuccess) return fe;
     }
@@ -1948,6 +1986,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.wtap0 = s.up2d ? 18 : 0;
     a.sp_taps = s.up2d ? 4 : 9;
     a.sp_w = s.up2d ? 2 : 3;
+    a.segs_per_kt = a.sp_taps / (pl.halo ? 1 : pl.itb);  // (as a.itb)
     // which B box coordinate a phase moves: the rank dimension of the 3-tap
     // map (its pieces are one), else the piece dimension
     const bool taps_map = pl.halo && pl.tb > 1;
