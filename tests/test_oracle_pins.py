@@ -366,3 +366,36 @@ def test_U3_upsample2d_brute_force_tiny():
                         if 0 <= Y + kh - 1 < 4 and 0 <= X + kw - 1 < 6:
                             acc += float(np.dot(w[o, kh, kw], up[Y + kh - 1, X + kw - 1]))
                 assert abs(y[0, 0, Y, X, o] - acc) < 1e-12
+
+
+def test_U4_upsample2d_is_four_subpixel_2x2_convs():
+    """The identity the GPU path computes by: output pixel (2i+a, 2j+b) reads the
+    upsampled row 2i+a+kh-1, i.e. low-res row floor((a+kh-1)/2) + i, which is
+    i+a-1 or i+a; so each phase (a, b) is a 2x2 conv of the low-res x at offsets
+    (a+e-1, b+f-1), e, f in {0, 1}, whose taps sum the 3x3 taps landing there.
+    Exact in fp64 up to summation order (the oracle itself is the definition)."""
+    x = rand((2, 2, 5, 6, 4), 98)
+    w = rand((3, 3, 3, 4), 99)
+    b = rand((3,), 100)
+    ref = oracle.upsample2d_conv(x, w, b)
+    B, T, H, W, C = x.shape
+    xp = np.zeros((B, T, H + 2, W + 2, C))
+    xp[:, :, 1:-1, 1:-1] = x  # low-res zero pad 1
+    y = np.zeros((B, T, 2 * H, 2 * W, 3))
+    for a in range(2):
+        for bb in range(2):
+            w2 = np.zeros((3, 2, 2, C))
+            for kh in range(3):
+                for kw in range(3):
+                    e = (a + kh - 1) // 2 - (a - 1)   # low-res row offset relative to a-1
+                    f = (bb + kw - 1) // 2 - (bb - 1)
+                    w2[:, e, f] += w[:, kh, kw]
+            # every 3x3 tap lands on exactly one 2x2 tap of every phase
+            np.testing.assert_allclose(w2.sum(axis=(1, 2)), w.sum(axis=(1, 2)), rtol=0, atol=1e-14)
+            for e in range(2):
+                for f in range(2):
+                    # padded index of low-res row i + a + e - 1 is i + a + e
+                    win = xp[:, :, a + e:a + e + H, bb + f:bb + f + W]
+                    y[:, :, a::2, bb::2] += np.einsum("btijc,oc->btijo", win, w2[:, e, f])
+            y[:, :, a::2, bb::2] += b
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
