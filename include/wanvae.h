@@ -212,8 +212,9 @@ wanvae_status wanvae_resblock_forward_static(const wanvae_resblock_params *p, co
 
 /* Synchronises `stream`, then returns WANVAE_ERR_TIMEOUT (and clears the
  * flag) if any kernel of this library on the current device gave up a
- * bounded wait since the last call, WANVAE_ERR_CUDA if the stream reports an
- * error, else WANVAE_OK.  Not for the hot path. */
+ * bounded wait since the last call, WANVAE_ERR_CUDA (flag cleared too) if a
+ * kernel skipped an access its own checks refused (a misaligned TMA source)
+ * or if the stream reports an error, else WANVAE_OK.  Not for the hot path. */
 wanvae_status wanvae_sync_status(wanvae_stream stream);
 
 /* Upper bound, in nanoseconds, of every device-side wait in later launches
