@@ -48,6 +48,8 @@ def lib():
         L.oracle_resblock_points.restype = ci
         L.oracle_upsample2d_conv.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
         L.oracle_upsample2d_conv.restype = ci
+        L.oracle_time_upsample_conv.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+        L.oracle_time_upsample_conv.restype = ci
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -105,6 +107,28 @@ def upsample2d_conv(x, w, bias):
     if rc:
         raise ValueError("oracle_upsample2d_conv rejected its arguments")
     return out
+
+
+def time_upsample_conv(x, w, bias):
+    """Temporal half of upsample3d: every frame repeated twice in T, then a
+    causal 3x1x1 conv (two zero frames before the first) with bias.
+    x [B,T,H,W,Ci], w [Co,3,Ci] (tap 2 = current frame) -> [B,2T,H,W,Co]."""
+    x, w, bias = _f64(x), _f64(w), _f64(bias)
+    B, T, H, W, Ci = x.shape
+    Co = w.shape[0]
+    out = np.empty((B, 2 * T, H, W, Co))
+    rc = lib().oracle_time_upsample_conv(_ptr(x), _ptr(w), _ptr(bias), B, T, H, W, Ci, Co,
+                                         _ptr(out))
+    if rc:
+        raise ValueError("oracle_time_upsample_conv rejected its arguments")
+    return out
+
+
+def upsample3d(x, w_t, b_t, w_s, b_s):
+    """The decoder's upsample3d as read from the pages: the temporal half
+    (time_upsample_conv) and then the spatial upsampler (upsample2d_conv) on
+    every frame of its output.  x [B,T,H,W,C] -> [B,2T,2H,2W,Co]."""
+    return upsample2d_conv(time_upsample_conv(x, w_t, b_t), w_s, b_s)
 
 
 def cache_next(cache, x):

@@ -23,6 +23,13 @@
  *  - "Sharding of WAN 2.2 VAE", section "Why depth sharding is not
  *    beneficial": frame-by-frame decode carries a feat_cache holding the last
  *    frames of each CausalConv3d's input.
+ *  - Same page, decoder tree: the up blocks end in an upsample2d or an
+ *    upsample3d resample whose second module is a conv; "Closing the gap",
+ *    section 3, names 3x1x1 conv kernels in the graph.  Nothing else about
+ *    them is on the pages, so the plain reading of "upsample + conv" is taken:
+ *    upsample2d = nearest 2x in H and W, then a 3x3 conv (zero pad 1, bias);
+ *    the temporal half of upsample3d = nearest 2x in T, then a causal 3x1x1
+ *    conv (two zero frames before the first, bias).
  *
  * Readings taken where the pages are silent (each also listed in the design
  * notes): eps = 1e-12 clamps the L2 norm (F.normalize's default); no norm
@@ -369,6 +376,42 @@ API int oracle_upsample2d_conv(const double *in, const double *w, const double *
                     const double *wr = w + ((oc * 3 + kh) * 3 + kw) * Ci;
                     for (int64_t c = 0; c < Ci; ++c) acc += wr[c] * src[c];
                 }
+            }
+            o[oc] = acc;
+        }
+    }
+    return 0;
+}
+
+/* Temporal half of the decoder's upsample3d ("Sharding of WAN 2.2 VAE", decoder
+ * tree: WanUpBlock(..., upsample3d); the graph's 3x1x1 conv kernels, "Closing the
+ * gap", conv3d blocking).  The pages give no more, so the plain reading of
+ * "upsample + conv": every frame is repeated twice in T (nearest neighbour),
+ * then a causal conv with a 3x1x1 kernel -- two zero frames before the first,
+ * like every CausalConv3d of the decoder -- and a bias, C_in -> C_out.
+ *   in [B][T][H][W][Ci], w [Co][3][Ci] (tap 2 reads the current upsampled
+ *   frame, tap 0 the one two before it), bias [Co] or NULL,
+ *   out [B][2T][H][W][Co]. */
+API int oracle_time_upsample_conv(const double *in, const double *w, const double *bias,
+                                  int64_t B, int64_t T, int64_t H, int64_t W, int64_t Ci,
+                                  int64_t Co, double *out)
+{
+    if (B < 1 || T < 1 || H < 1 || W < 1 || Ci < 1 || Co < 1) return -1;
+    const int64_t T2 = 2 * T, HW = H * W;
+    const int64_t nvox = B * T2 * HW;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t v = 0; v < nvox; ++v) {
+        const int64_t pix = v % HW, s = (v / HW) % T2, b = v / (HW * T2);
+        double *o = out + v * Co;
+        for (int64_t oc = 0; oc < Co; ++oc) {
+            double acc = bias ? bias[oc] : 0.0;
+            for (int kt = 0; kt < 3; ++kt) {
+                const int64_t u = s + kt - 2;   /* frame of the upsampled sequence */
+                if (u < 0) continue;            /* causal zero pad */
+                /* nearest neighbour: upsampled frame u is input frame u / 2 */
+                const double *src = in + ((b * T + u / 2) * HW + pix) * Ci;
+                const double *wr = w + (oc * 3 + kt) * Ci;
+                for (int64_t c = 0; c < Ci; ++c) acc += wr[c] * src[c];
             }
             o[oc] = acc;
         }

@@ -399,3 +399,81 @@ def test_U4_upsample2d_is_four_subpixel_2x2_convs():
                     y[:, :, a::2, bb::2] += np.einsum("btijc,oc->btijo", win, w2[:, e, f])
             y[:, :, a::2, bb::2] += b
     np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------ upsample3d, temporal half
+# Nearest 2x in T, then a causal 3x1x1 conv with bias -- pinned against a
+# library routine, delta kernels, causality and brute force.
+def _torch_time_upsample(x, w, b):
+    xt = torch.from_numpy(x).permute(0, 4, 1, 2, 3)              # N C T H W
+    up = xt.repeat_interleave(2, dim=2)
+    up = F.pad(up, (0, 0, 0, 0, 2, 0))                            # two zero frames first
+    wt = torch.from_numpy(w).permute(0, 2, 1)[..., None, None]    # Co Ci 3 1 1
+    return F.conv3d(up, wt, torch.from_numpy(b)).permute(0, 2, 3, 4, 1).numpy()
+
+
+def test_T1_time_upsample_matches_torch_functional():
+    x = rand((2, 3, 2, 3, 5), 110)
+    w = rand((4, 3, 5), 111)
+    b = rand((4,), 112)
+    y = oracle.time_upsample_conv(x, w, b)
+    assert y.shape == (2, 6, 2, 3, 4)
+    np.testing.assert_allclose(y, _torch_time_upsample(x, w, b), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("kt", [0, 1, 2])
+def test_T2_time_upsample_delta_taps(kt):
+    x = rand((1, 3, 2, 2, 3), 113)
+    w = np.zeros((3, 3, 3))
+    w[:, kt, :] = np.eye(3)
+    y = oracle.time_upsample_conv(x, w, np.zeros(3))
+    up = x.repeat(2, axis=1)          # frame s of the upsampled sequence is x[s // 2]
+    shift = 2 - kt                    # tap kt reads upsampled frame s - shift
+    ref = np.zeros_like(up)
+    ref[:, shift:] = up[:, :up.shape[1] - shift]
+    assert np.array_equal(y, ref)
+
+
+def test_T3_time_upsample_is_causal():
+    x = rand((1, 4, 2, 2, 3), 114)
+    w = rand((2, 3, 3), 115)
+    b = rand((2,), 116)
+    y0 = oracle.time_upsample_conv(x, w, b)
+    for t in range(4):
+        x1 = x.copy()
+        x1[:, t] += 1.0
+        y1 = oracle.time_upsample_conv(x1, w, b)
+        assert np.array_equal(y1[:, :2 * t], y0[:, :2 * t])       # nothing before 2t moves
+        assert not np.array_equal(y1[:, 2 * t], y0[:, 2 * t])
+
+
+def test_T4_time_upsample_brute_force_tiny():
+    x = rand((1, 2, 1, 2, 2), 117)
+    w = rand((2, 3, 2), 118)
+    b = rand((2,), 119)
+    y = oracle.time_upsample_conv(x, w, b)
+    for s in range(4):
+        for p in range(2):
+            for o in range(2):
+                acc = b[o]
+                for kt in range(3):
+                    u = s + kt - 2
+                    if u >= 0:
+                        acc += float(np.dot(w[o, kt], x[0, u // 2, 0, p]))
+                assert abs(y[0, s, 0, p, o] - acc) < 1e-12
+
+
+def test_T5_upsample3d_is_time_then_space():
+    x = rand((1, 2, 2, 3, 4), 120)
+    w_t, b_t = rand((4, 3, 4), 121), rand((4,), 122)
+    w_s, b_s = rand((3, 3, 3, 4), 123), rand((3,), 124)
+    y = oracle.upsample3d(x, w_t, b_t, w_s, b_s)
+    assert y.shape == (1, 4, 4, 6, 3)
+    mid = _torch_time_upsample(x, w_t, b_t)                     # [1, 4, 2, 3, 4]
+    B, T2, H, W, C = mid.shape
+    mt = torch.from_numpy(mid).reshape(B * T2, H, W, C).permute(0, 3, 1, 2)
+    up = F.interpolate(mt, scale_factor=2, mode="nearest")
+    ref = F.conv2d(up, torch.from_numpy(w_s).permute(0, 3, 1, 2), torch.from_numpy(b_s),
+                   padding=1)
+    ref = ref.permute(0, 2, 3, 1).reshape(B, T2, 2 * H, 2 * W, 3).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
