@@ -54,7 +54,7 @@ extern "C" {
 typedef enum {
     WANVAE_OK = 0,
     WANVAE_ERR_INVALID_ARG = 1, /* null pointer, bad size, aliasing, bad enum */
-    WANVAE_ERR_UNSUPPORTED = 2, /* legal block, but a size this build rejects */
+    WANVAE_ERR_UNSUPPORTED = 2, /* legal block, but a size the library rejects */
     WANVAE_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
     WANVAE_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required */
     WANVAE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */

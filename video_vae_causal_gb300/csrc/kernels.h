@@ -67,7 +67,7 @@ struct ConvSpec {
     int up2d;
 };
 
-// Host-side validation of a ConvSpec this build can run (channel counts,
+// Host-side validation of a ConvSpec the library can run (channel counts,
 // sizes); returns 0 if supported.
 int conv3d_supported(const ConvSpec &s);
 
