@@ -477,3 +477,25 @@ def test_T5_upsample3d_is_time_then_space():
                    padding=1)
     ref = ref.permute(0, 2, 3, 1).reshape(B, T2, 2 * H, 2 * W, 3).numpy()
     np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_T6_time_upsample_is_two_frame_phases():
+    """The identity the GPU path computes by: upsampled frame 2t+a+kt-2 is
+    input frame t-1+((a+kt)//2) (or a causal zero), so output frame 2t+a is a
+    2-tap conv of frames t-1 and t whose taps sum the 3 taps landing there."""
+    x = rand((2, 3, 2, 3, 4), 125)
+    w = rand((3, 3, 4), 126)
+    b = rand((3,), 127)
+    ref = oracle.time_upsample_conv(x, w, b)
+    B, T, H, W, C = x.shape
+    xp = np.concatenate([np.zeros((B, 1, H, W, C)), x], axis=1)   # frame -1 = zeros
+    y = np.zeros((B, 2 * T, H, W, 3))
+    for a in range(2):
+        w2 = np.zeros((3, 2, C))
+        for kt in range(3):
+            w2[:, (a + kt) // 2] += w[:, kt]
+        for e in range(2):
+            # padded index of input frame t - 1 + e is t + e
+            y[:, a::2] += np.einsum("bthwc,oc->bthwo", xp[:, e:e + T], w2[:, e])
+        y[:, a::2] += b
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
