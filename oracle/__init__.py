@@ -50,6 +50,9 @@ def lib():
         L.oracle_upsample2d_conv.restype = ci
         L.oracle_time_upsample_conv.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
         L.oracle_time_upsample_conv.restype = ci
+        L.oracle_frame_attention.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl,
+                                             vp]
+        L.oracle_frame_attention.restype = ci
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = ci
         _LIB = L
@@ -129,6 +132,21 @@ def upsample3d(x, w_t, b_t, w_s, b_s):
     (time_upsample_conv) and then the spatial upsampler (upsample2d_conv) on
     every frame of its output.  x [B,T,H,W,C] -> [B,2T,2H,2W,Co]."""
     return upsample2d_conv(time_upsample_conv(x, w_t, b_t), w_s, b_s)
+
+
+def frame_attention(x, gamma, wqkv, bqkv, wo, bo, eps=1e-12):
+    """The mid-block's spatial self-attention, per (batch, frame): RMS_norm,
+    1x1 q/k/v projections, one head of softmax(q k^T / sqrt(C)) v over the
+    frame's H*W positions, 1x1 output projection, plus the input.
+    x [B,T,H,W,C], gamma [C], wqkv [3C,C], bqkv [3C], wo [C,C], bo [C]."""
+    x, gamma, wqkv, bqkv, wo, bo = (_f64(a) for a in (x, gamma, wqkv, bqkv, wo, bo))
+    B, T, H, W, C = x.shape
+    out = np.empty_like(x)
+    rc = lib().oracle_frame_attention(_ptr(x), _ptr(gamma), _ptr(wqkv), _ptr(bqkv), _ptr(wo),
+                                      _ptr(bo), B, T, H, W, C, eps, _ptr(out))
+    if rc:
+        raise ValueError("oracle_frame_attention rejected its arguments")
+    return out
 
 
 def cache_next(cache, x):

@@ -30,6 +30,10 @@
  *    upsample2d = nearest 2x in H and W, then a 3x3 conv (zero pad 1, bias);
  *    the temporal half of upsample3d = nearest 2x in T, then a causal 3x1x1
  *    conv (two zero frames before the first, bias).
+ *  - "Closing the gap", section 5: the mid-block attention is a spatial
+ *    self-attention within each frame (sequence = the H x W grid, batch =
+ *    B x T).  Read plainly: RMS_norm, 1x1 q/k/v projections, one head of
+ *    softmax(q k^T / sqrt(C)) v, a 1x1 output projection, plus the input.
  *
  * Readings taken where the pages are silent (each also listed in the design
  * notes): eps = 1e-12 clamps the L2 norm (F.normalize's default); no norm
@@ -417,6 +421,93 @@ API int oracle_time_upsample_conv(const double *in, const double *w, const doubl
         }
     }
     return 0;
+}
+
+/* The decoder's mid-block attention ("Closing the gap: Wan 2.2 14B VAE
+ * decoder", section 5: the decoder's one attention block is a spatial
+ * self-attention in which, within a frame, every position attends to every
+ * other; the sequence is the H x W grid and each (batch, frame) is an
+ * independent problem).  The pages give no more, so the plain reading:
+ * RMS_norm over channels (the block's norm, without SiLU), 1x1 projections to
+ * q, k and v, one head, softmax(q k^T / sqrt(C)) v over the frame's
+ * positions, a 1x1 output projection, and the block's input added back.
+ *   in [B][T][H][W][C]; gamma [C]; wqkv [3C][C] (rows q, then k, then v);
+ *   bqkv [3C]; wo [C][C]; bo [C]; out [B][T][H][W][C] (not aliasing in). */
+API int oracle_frame_attention(const double *in, const double *gamma, const double *wqkv,
+                               const double *bqkv, const double *wo, const double *bo,
+                               int64_t B, int64_t T, int64_t H, int64_t W, int64_t C,
+                               double eps, double *out)
+{
+    if (B < 1 || T < 1 || H < 1 || W < 1 || C < 1) return -1;
+    const int64_t n = H * W;
+    double *nx = (double *)malloc((size_t)n * C * sizeof(double));
+    double *qkv = (double *)malloc((size_t)n * 3 * C * sizeof(double));
+    if (!nx || !qkv) {
+        free(nx);
+        free(qkv);
+        return -1;
+    }
+    const double scale = 1.0 / sqrt((double)C);
+    int rc = 0;
+    for (int64_t f = 0; f < B * T; ++f) {
+        const double *x = in + f * n * C;
+        double *y = out + f * n * C;
+        oracle_rms_norm_silu(x, gamma, n, C, eps, 0, nx);
+        /* q, k, v of every position: qkv[i][r] = b[r] + sum_c w[r][c] nx[i][c] */
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < n; ++i)
+            for (int64_t r = 0; r < 3 * C; ++r) {
+                double acc = bqkv[r];
+                for (int64_t c = 0; c < C; ++c) acc += wqkv[r * C + c] * nx[i * C + c];
+                qkv[i * 3 * C + r] = acc;
+            }
+#pragma omp parallel
+        {
+            double *p = (double *)malloc((size_t)n * sizeof(double));
+            double *o = (double *)malloc((size_t)C * sizeof(double));
+            if (!p || !o) {
+#pragma omp atomic write
+                rc = -1;
+            }
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t i = 0; i < n; ++i) {
+                if (!p || !o) continue;
+                const double *q = qkv + i * 3 * C;
+                /* scores against every key of the frame, softmax over them */
+                double m = -INFINITY;
+                for (int64_t j = 0; j < n; ++j) {
+                    const double *k = qkv + j * 3 * C + C;
+                    double s = 0.0;
+                    for (int64_t c = 0; c < C; ++c) s += q[c] * k[c];
+                    p[j] = s * scale;
+                    if (p[j] > m) m = p[j];
+                }
+                double z = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    p[j] = exp(p[j] - m);
+                    z += p[j];
+                }
+                for (int64_t c = 0; c < C; ++c) o[c] = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    const double *v = qkv + j * 3 * C + 2 * C;
+                    const double a = p[j] / z;
+                    for (int64_t c = 0; c < C; ++c) o[c] += a * v[c];
+                }
+                /* output projection, bias, residual */
+                for (int64_t oc = 0; oc < C; ++oc) {
+                    double acc = bo[oc];
+                    for (int64_t c = 0; c < C; ++c) acc += wo[oc * C + c] * o[c];
+                    y[i * C + oc] = x[i * C + oc] + acc;
+                }
+            }
+            free(p);
+            free(o);
+        }
+        if (rc) break;
+    }
+    free(nx);
+    free(qkv);
+    return rc;
 }
 
 /* Threads the oracle's OpenMP loops will use (1 when built without it). */

@@ -499,3 +499,80 @@ def test_T6_time_upsample_is_two_frame_phases():
             y[:, a::2] += np.einsum("bthwc,oc->bthwo", xp[:, e:e + T], w2[:, e])
         y[:, a::2] += b
     np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- mid-block attention
+# One head of softmax(q k^T / sqrt(C)) v over each frame's H*W positions,
+# between an RMS_norm and a 1x1 output projection, plus the input.
+def _attn_params(C, seed):
+    g = rand((C,), seed) * 0.5 + 1.0
+    return (g, rand((3 * C, C), seed + 1) / np.sqrt(C), rand((3 * C,), seed + 2) * 0.1,
+            rand((C, C), seed + 3) / np.sqrt(C), rand((C,), seed + 4) * 0.1)
+
+
+def _torch_attention(x, g, wqkv, bqkv, wo, bo, eps=1e-12):
+    B, T, H, W, C = x.shape
+    xt = torch.from_numpy(x).reshape(B * T, H * W, C)
+    n = F.normalize(xt, dim=-1, eps=eps) * np.sqrt(C) * torch.from_numpy(g)
+    qkv = n @ torch.from_numpy(wqkv).T + torch.from_numpy(bqkv)
+    q, k, v = qkv[..., :C], qkv[..., C:2 * C], qkv[..., 2 * C:]
+    o = F.scaled_dot_product_attention(q, k, v)            # scale 1 / sqrt(C)
+    y = xt + o @ torch.from_numpy(wo).T + torch.from_numpy(bo)
+    return y.reshape(B, T, H, W, C).numpy()
+
+
+def test_A1_attention_matches_torch_sdpa():
+    x = rand((2, 2, 3, 4, 8), 130)
+    p = _attn_params(8, 131)
+    np.testing.assert_allclose(oracle.frame_attention(x, *p), _torch_attention(x, *p),
+                               rtol=1e-11, atol=1e-11)
+
+
+def test_A2_attention_uniform_when_q_k_vanish():
+    """Zero q and k weights and biases: every score is 0, attention is the mean
+    of v over the frame, so out = x + bo + Wo mean_j(v_j)."""
+    x = rand((1, 2, 2, 3, 6), 132)
+    g, wqkv, bqkv, wo, bo = _attn_params(6, 133)
+    wqkv[:12] = 0.0
+    bqkv[:12] = 0.0
+    y = oracle.frame_attention(x, g, wqkv, bqkv, wo, bo)
+    C = 6
+    for t in range(2):
+        xf = x[0, t].reshape(-1, C)
+        nrm = xf / np.maximum(np.linalg.norm(xf, axis=1, keepdims=True), 1e-12) * np.sqrt(C) * g
+        v = nrm @ wqkv[12:].T + bqkv[12:]
+        ref = xf + bo + wo @ v.mean(axis=0)
+        np.testing.assert_allclose(y[0, t].reshape(-1, C), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_A3_attention_is_permutation_equivariant():
+    x = rand((1, 1, 3, 5, 4), 134)
+    p = _attn_params(4, 135)
+    perm = np.random.default_rng(7).permutation(15)
+    xp = x.reshape(1, 1, 15, 4)[:, :, perm].reshape(1, 1, 3, 5, 4)
+    y = oracle.frame_attention(x, *p).reshape(1, 1, 15, 4)
+    yp = oracle.frame_attention(xp, *p).reshape(1, 1, 15, 4)
+    np.testing.assert_allclose(yp, y[:, :, perm], rtol=1e-12, atol=1e-12)
+
+
+def test_A4_attention_single_position_is_v():
+    """One position per frame: its only key gets weight 1, so out = x + bo + Wo v."""
+    x = rand((1, 3, 1, 1, 5), 136)
+    g, wqkv, bqkv, wo, bo = _attn_params(5, 137)
+    y = oracle.frame_attention(x, g, wqkv, bqkv, wo, bo)
+    for t in range(3):
+        xv = x[0, t, 0, 0]
+        nrm = xv / max(np.linalg.norm(xv), 1e-12) * np.sqrt(5) * g
+        v = wqkv[10:] @ nrm + bqkv[10:]
+        np.testing.assert_allclose(y[0, t, 0, 0], xv + bo + wo @ v, rtol=1e-12, atol=1e-12)
+
+
+def test_A5_attention_frames_are_independent():
+    x = rand((2, 3, 2, 2, 4), 138)
+    p = _attn_params(4, 139)
+    y0 = oracle.frame_attention(x, *p)
+    x1 = x.copy()
+    x1[1, 2] += 1.0
+    y1 = oracle.frame_attention(x1, *p)
+    changed = np.abs(y1 - y0).reshape(2, 3, -1).max(axis=2) > 0
+    assert changed[1, 2] and changed.sum() == 1
