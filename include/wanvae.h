@@ -58,7 +58,11 @@ typedef enum {
     WANVAE_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
     WANVAE_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required */
     WANVAE_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
-    WANVAE_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out */
+    WANVAE_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out */
+    WANVAE_ERR_UNDRAINED = 7    /* a wait ran out, and then so did the kernel's wait
+                                   for its own in-flight copies or MMAs: they may
+                                   have landed after it returned, so the CUDA context
+                                   should not be reused */
 } wanvae_status;
 
 typedef enum { WANVAE_BF16 = 0, WANVAE_F32 = 1 } wanvae_dtype;
@@ -210,11 +214,16 @@ wanvae_status wanvae_resblock_forward_static(const wanvae_resblock_params *p, co
                                              const wanvae_resblock_cache *cache,
                                              wanvae_stream stream);
 
-/* Synchronises `stream`, then returns WANVAE_ERR_TIMEOUT (and clears the
- * flag) if any kernel of this library on the current device gave up a
- * bounded wait since the last call, WANVAE_ERR_CUDA (flag cleared too) if a
- * kernel skipped an access its own checks refused (a misaligned TMA source)
- * or if the stream reports an error, else WANVAE_OK.  Not for the hot path. */
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word for the current device and returns, in this order of precedence:
+ *   WANVAE_ERR_UNDRAINED if a kernel gave up a bounded wait and afterwards
+ *     also gave up waiting for its own in-flight TMA copies or MMAs (they may
+ *     have completed into memory it no longer owned: do not reuse the context);
+ *   WANVAE_ERR_CUDA if a kernel skipped an access its own checks refused (a
+ *     misaligned TMA source) or if the stream reports an error;
+ *   WANVAE_ERR_TIMEOUT if a kernel gave up a bounded wait and then drained
+ *     cleanly (the context stays usable; the outputs of that call are not);
+ *   WANVAE_OK otherwise.  Not for the hot path. */
 wanvae_status wanvae_sync_status(wanvae_stream stream);
 
 /* Upper bound, in nanoseconds, of every device-side wait in later launches
@@ -222,6 +231,18 @@ wanvae_status wanvae_sync_status(wanvae_stream stream);
  * already satisfied give up at once: a test hook for the timeout path.
  * Host-side setting, process-wide. */
 void wanvae_set_wait_limit_ns(uint64_t ns);
+
+/* Kernel-variant overrides for testing and tuning (process-wide, host-side;
+ * no effect on results beyond the summation order of fp32 partial sums).
+ * Each argument 0 or 1 forces a choice for later calls; -1 (or any other
+ * value) restores the automatic, shape-driven choice:
+ *   pair   : 1 = single-CTA conv kernel (cta_group::1) instead of CTA pairs
+ *   halo   : 1 = halo tiles, 0 = per-tap im2col tiles (k = 3 convs)
+ *   wide   : 1 = 16 x 16 halo patches where they apply, 0 = 16 x 8
+ *   narrow : 1 = the GEMM-plus-stencil kernel for c_out <= 3, 0 = the
+ *            implicit GEMM for those layers too
+ * A forced choice that cannot run a given shape falls back to one that can. */
+void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow);
 
 /* Number of kernels this library has enqueued since load (host counter). */
 uint64_t wanvae_launch_count(void);

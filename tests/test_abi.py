@@ -44,10 +44,11 @@ def test_only_c_abi_is_exported():
 
 
 def test_status_strings_and_version(lib):
-    for s in range(7):
+    for s in range(8):
         assert wanvae.status_string(s)
+    assert "context" in wanvae.status_string(wanvae.ERR_UNDRAINED)
     assert wanvae.status_string(99) == "unknown status"
-    assert wanvae.version() == 100
+    assert wanvae.version() == 101
 
 
 def test_workspace_size(lib):

@@ -16,20 +16,18 @@ DEV = "cuda"
 
 @pytest.fixture(params=["pair-im2col", "pair-halo", "pair-wide", "single-im2col", "single-halo",
                         "single-wide"])
-def variant(request, monkeypatch):
+def variant(request, cuda_lib):
     """Run a conv test on every kernel variant: CTA pair or single CTA, and
     per-tap im2col A loads, halo tiles (16 x 8 patches, one halo load per
     temporal tap feeding the nine spatial taps) or wide halo tiles (16 x 16
     patches, two accumulators per CTA; layers with c_out <= 128 and no
     shortcut, others fall back to 16 x 8)."""
     pair, mode = request.param.split("-")
-    if pair == "single":
-        monkeypatch.setenv("WANVAE_CONV_PAIR", "1")
-    else:
-        monkeypatch.delenv("WANVAE_CONV_PAIR", raising=False)
-    monkeypatch.setenv("WANVAE_CONV_HALO", "0" if mode == "im2col" else "1")
-    monkeypatch.setenv("WANVAE_CONV_WIDE", "1" if mode == "wide" else "0")
-    return request.param
+    cuda_lib.set_kernel_variant(pair=1 if pair == "single" else -1,
+                                halo=0 if mode == "im2col" else 1,
+                                wide=1 if mode == "wide" else 0)
+    yield request.param
+    cuda_lib.set_kernel_variant()
 
 
 def dev(d):
@@ -118,11 +116,17 @@ NARROW_CASES = [
 
 
 @pytest.fixture(params=["stencil", "gemm"])
-def narrow_path(request, monkeypatch):
-    """Layers with c_out <= 4 and k=3 run as one GEMM over all taps plus a
-    stencil sum unless WANVAE_CONV_NARROW=0 sends them to the implicit GEMM."""
-    monkeypatch.setenv("WANVAE_CONV_NARROW", "1" if request.param == "stencil" else "0")
-    return request.param
+def narrow_path(request, cuda_lib, variant):
+    """Layers with c_out <= 3 and k=3 run as one GEMM over all taps plus a
+    stencil sum unless the narrow variant is switched off, which sends them to
+    the implicit GEMM (on the conv variant the `variant` fixture chose)."""
+    pair, mode = variant.split("-")
+    cuda_lib.set_kernel_variant(pair=1 if pair == "single" else -1,
+                                halo=0 if mode == "im2col" else 1,
+                                wide=1 if mode == "wide" else 0,
+                                narrow=1 if request.param == "stencil" else 0)
+    yield request.param
+    cuda_lib.set_kernel_variant()
 
 
 @pytest.mark.parametrize("case", NARROW_CASES)
@@ -282,6 +286,58 @@ def test_resblock_causal_on_gpu(cuda_lib):
     y2 = cuda_lib.resblock_forward(x2.to(DEV), pd)
     cuda_lib.sync_status()
     assert torch.equal(y[:, :3], y2[:, :3])
+
+
+# ------------------------------------------------------------------ closed form at x = 0
+@pytest.mark.parametrize("ci,co", [(96, 96), (384, 384), (64, 32)])
+def test_resblock_zero_input_closed_form(cuda_lib, ci, co):
+    """x = 0 and bA = 0: a1 = 0, h = 0, so conv A's fused RMS_norm2 divides a
+    zero vector by the eps clamp (a2 = 0) and y = bB (+ bS) exactly.  With bA
+    drawn as usual, h = bA at every voxel and y follows the oracle (pinned by
+    the closed form on the CPU)."""
+    B, T, H, W = 1, 4, 16, 24
+    _, p = synth.make_resblock_inputs((B, T, H, W), ci, co, seed=21)
+    x = torch.zeros((B, T, H, W, ci), dtype=torch.bfloat16)
+    y = cuda_lib.resblock_forward(x.to(DEV), dev(p))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.resblock_forward(x, oracle.Params.from_dict(p)), what="x=0")
+    p0 = dict(p, bA=torch.zeros_like(p["bA"]))
+    y0 = cuda_lib.resblock_forward(x.to(DEV), dev(p0))
+    cuda_lib.sync_status()
+    expect = p["bB"] + (p["bS"] if "bS" in p else 0)
+    assert torch.equal(y0.cpu(), expect.to(torch.bfloat16).expand(B, T, H, W, co))
+
+
+# ------------------------------------------------------------------ full sizes, whole tensor
+def test_latent_fullT_whole_tensor(cuda_lib):
+    """Every output element of the latent-resolution block [1,21,60,104,384]
+    against the oracle's full-T run (about 20 s of oracle time)."""
+    dims, ci, co, _ = synth.WORKLOADS["latent_fullT"]
+    x, p = synth.make_resblock_inputs(dims, ci, co, seed=0)
+    y = cuda_lib.resblock_forward(x.to(DEV), dev(p))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
+            what="latent_fullT whole")
+
+
+def test_streaming_720p_whole_tensor(cuda_lib):
+    """The streaming workload's 21 calls of [1,1,90,160,384] with feat_cache:
+    bit-exact against the full-T run, whose every element is compared with
+    the oracle's full-T run (about 45 s of oracle time)."""
+    dims, ci, co, calls = synth.WORKLOADS["stream_720p"]
+    B, T, H, W = dims
+    x, p = synth.make_resblock_inputs(dims, ci, co, seed=0)
+    xd, pd = x.to(DEV), dev(p)
+    cA = torch.zeros((B, 2, H, W, ci), dtype=torch.bfloat16, device=DEV)
+    cB = torch.zeros((B, 2, H, W, co), dtype=torch.bfloat16, device=DEV)
+    ws = cuda_lib.make_workspace((B, 1, H, W), ci, co)
+    y = torch.cat([cuda_lib.resblock_forward(xd[:, t:t + 1].contiguous(), pd, cache=(cA, cB),
+                                             workspace=ws) for t in range(calls)], dim=1)
+    full = cuda_lib.resblock_forward(xd, pd)
+    cuda_lib.sync_status()
+    assert torch.equal(y, full)
+    compare(to_f64(full), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
+            what="stream_720p whole")
 
 
 # ------------------------------------------------------------------ full sizes, sampled

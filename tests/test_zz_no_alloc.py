@@ -1,21 +1,18 @@
 """The allocation-free ResidualBlock entry point (wanvae_resblock_forward_static).
 
 It serves callers that cannot allocate device memory where they run the
-block: its workspace is the library's own fixed-size device array.  Its
-output must match the regular entry point (caller workspace) within the
-suite's bar, call after call (the array keeps the previous call's contents),
-and sizes beyond the array are refused before anything is enqueued.
+block: its workspace is the library's own fixed-size device array.  It runs
+the same kernels on the same inputs as the regular entry point (caller
+workspace), so its output must equal that entry point's bit for bit, call
+after call (the array keeps the previous call's contents), and sizes beyond
+the array are refused before anything is enqueued.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
 """
-import ctypes
-
-import numpy as np
 import pytest
 import torch
 
-from _util import compare, to_f64
 from video_vae_causal_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +34,8 @@ def _run_both(lib, dims, ci, co, seed):
 def test_static_matches_caller_workspace_two_calls_in_a_row(cuda_lib, dims, ci, co):
     for seed in (1, 2):  # second call reuses the array the first one left behind
         _, _, y_ref, y_static = _run_both(cuda_lib, dims, ci, co, seed)
-        compare(to_f64(y_static), to_f64(y_ref), what=f"static vs workspace seed={seed}")
+        assert torch.equal(y_static, y_ref), f"static vs workspace seed={seed}"
+        assert torch.isfinite(y_static.float()).all()
 
 
 def test_static_streaming_two_frames_matches(cuda_lib):
@@ -53,7 +51,8 @@ def test_static_streaming_two_frames_matches(cuda_lib):
         y_st = cuda_lib.resblock_forward_static(xt, params, torch.empty_like(y_ref),
                                                 cache=caches[1])
         cuda_lib.sync_status()
-        compare(to_f64(y_st), to_f64(y_ref), what=f"static streaming t={t}")
+        assert torch.equal(y_st, y_ref), f"static streaming t={t}"
+    assert torch.equal(caches[0][0], caches[1][0]) and torch.equal(caches[0][1], caches[1][1])
 
 
 def test_static_rejects_sizes_beyond_its_array(cuda_lib):

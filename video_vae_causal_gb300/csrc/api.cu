@@ -98,15 +98,22 @@ const char *wanvae_status_string(wanvae_status s) {
         case WANVAE_ERR_WORKSPACE: return "workspace missing or too small";
         case WANVAE_ERR_CUDA: return "CUDA error";
         case WANVAE_ERR_TIMEOUT: return "device-side wait timed out";
+        case WANVAE_ERR_UNDRAINED:
+            return "device-side wait timed out and in-flight copies were not drained "
+                   "(do not reuse the CUDA context)";
     }
     return "unknown status";
 }
 
-int wanvae_version(void) { return 100; }
+int wanvae_version(void) { return 101; }
 
 void wanvae_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
 
 uint64_t wanvae_launch_count(void) { return g_launches.load(); }
+
+void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow) {
+    set_kernel_variant(pair, halo, wide, narrow);
+}
 
 wanvae_status wanvae_rmsnorm_silu(const void *x, void *y, const float *gamma, wanvae_dtype dt,
                                   int64_t n_voxels, int64_t C, float eps, wanvae_stream stream) {
@@ -372,8 +379,10 @@ wanvae_status wanvae_sync_status(wanvae_stream stream) {
         const unsigned zero = 0;
         if (cudaMemcpyToSymbol(g_wanvae_err, &zero, sizeof(zero)) != cudaSuccess)
             return WANVAE_ERR_CUDA;
-        // bit 0: a bounded device wait gave up; other bits: a kernel skipped an
-        // access its own checks refused
+        // bit 0: a bounded device wait gave up; bit 2: so did a later wait for
+        // the kernel's own in-flight work; bit 1: a kernel skipped an access
+        // its own checks refused
+        if (v & 4u) return WANVAE_ERR_UNDRAINED;
         return v == 1u ? WANVAE_ERR_TIMEOUT : WANVAE_ERR_CUDA;
     }
     return WANVAE_OK;

@@ -23,6 +23,8 @@
 // zeros (skipped) or, with a feat_cache, the cache's two frames.
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <atomic>
 #include <string.h>
 
 #include "kernels.h"
@@ -109,7 +111,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX64,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtl wc{p.wait_ns, p.err, abort_flag};
+    const WaitCtl wc{p.wait_ns, p.err, abort_flag, 0u};
 
     // The whole B operand (27 c_out rows, rows up to npad read as zeros) once.
     if (tid == 0) {
@@ -285,7 +287,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX64,
     // the CTA's shared memory and TMEM go away.
     if (!ok && tid == 0) {
         volatile int no_abort = 0;
-        const WaitCtl dc{kDrainNsN, p.err, &no_abort};
+        const WaitCtl dc{kDrainNsN, p.err, &no_abort, kDevErrTimeout | kDevErrDrain};
         if (pending_full) mbar_wait(bars.full(), ph_full, dc);
         if (lost_full >= 0) mbar_wait(bars.full(), (uint32_t)lost_full, dc);
         if (pending_mma) mbar_wait(bars.mmad(), ph_mma, dc);
@@ -296,23 +298,31 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX64,
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// The dynamic shared-memory opt-in of each instantiation, made once per
+// device (it does not change between launches).
 template <int CO>
 cudaError_t launch_narrow(const NarrowArgs &a, const CUtensorMap *m, uint32_t smem,
                           const LaunchCtx &ctx) {
     auto kern = conv3d_narrow_kernel<CO>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    constexpr int kMaxDev = 64;
+    static std::atomic<uint32_t> opted[kMaxDev];  // bytes opted in per device (0 = not yet)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if (opted[dev].load(std::memory_order_acquire) < smem) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        opted[dev].store(smem, std::memory_order_release);
+    }
     const int grid = a.num_items < ctx.num_sms ? a.num_items : ctx.num_sms;
     kern<<<grid, kThreadsN, smem, ctx.stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
     return cudaGetLastError();
 }
 
-// WANVAE_CONV_NARROW=0 routes narrow layers to the implicit-GEMM kernel.
-bool narrow_enabled() {
-    const char *e = getenv("WANVAE_CONV_NARROW");
-    return !(e && e[0] == '0' && e[1] == 0);
-}
+// The kernel-variant setting (set_kernel_variant) can route narrow layers to
+// the implicit-GEMM kernel instead.
+bool narrow_enabled() { return narrow_variant() != 0; }
 
 }  // namespace
 

@@ -37,6 +37,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -51,7 +52,12 @@ constexpr int kEpiWarps = 8;  // two warps per TMEM lane quarter, each half the 
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 rows x 32 bf16 channels
 constexpr int kSmemBudget = 227 * 1024;
+constexpr int kMaxItb = 4;  // im2col: most taps per stage (the upsampler's 2 x 2)
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // cleanup waits after an abort
+
+// Kernel-variant overrides (set_kernel_variant): -1 = chosen per call.
+enum { kVarPair = 0, kVarHalo = 1, kVarWide = 2, kVarNarrow = 3, kNumVar = 4 };
+std::atomic<int> g_variant[kNumVar] = {{-1}, {-1}, {-1}, {-1}};
 
 struct ConvArgs {
     int T, H, W, HW;
@@ -257,6 +263,46 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
             const bool shortcut = seg == nseg;
             const int ntap = shortcut ? 1 : p.itb, nch = shortcut ? p.nsub : p.nsub / p.itb;
             const int nkc = shortcut ? p.kc_short : p.kc_main;
+            // The segment's taps, worked out once for all its channel-chunk
+            // stages (this thread must keep ahead of the MMAs): weight tap,
+            // spatial offset, source frame (out of range -> zeros) and map.
+            int wtap[kMaxItb], kh[kMaxItb], kw[kMaxItb], fidx[kMaxItb];
+            bool from_cache[kMaxItb];
+#pragma unroll
+            for (int j = 0; j < kMaxItb; ++j) {
+                wtap[j] = 0;
+                kh[j] = 1;
+                kw[j] = 1;
+                fidx[j] = frames;
+                from_cache[j] = false;
+                if (j < ntap && !shortcut && p.taps == 27) {
+                    const int q = seg * p.itb + j;
+                    int kt;
+                    if (kUp) {  // the phase's 2 x 2 taps, current frame only
+                        kt = 2;
+                        kh[j] = tbase.kh + ((q >> 1) & 1);
+                        kw[j] = tbase.kw + (q & 1);
+                        wtap[j] = q & 3;
+                    } else {
+                        const int tap = kt0 * 9 + q;
+                        kt = tap / 9;
+                        kh[j] = (tap / 3) % 3;
+                        kw[j] = tap % 3;
+                        wtap[j] = tap;
+                    }
+                    const int tt = ti.t + kt - 2;
+                    if (!ti.dummy) {
+                        if (tt >= 0) {
+                            fidx[j] = ti.n * p.T + tt;
+                        } else if (p.has_cache) {
+                            from_cache[j] = true;
+                            fidx[j] = ti.n * 2 + tt + 2;
+                        }
+                    }
+                }
+            }
+            const int ph = kUp ? unit_phase(u, p) : 0;  // upsampler: its weights
+            const CUtensorMap *bm = shortcut ? mapSB : mapB;
             for (int kc = 0; kc < nkc; ++kc) {
                 if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) {
                     ok = false;
@@ -267,37 +313,10 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                 const uint32_t fb = kPair == 2 ? mapa_shared(fb_local, 0) : fb_local;
                 const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
                 const uint32_t sb = sa + p.a_bytes;
-                for (int j = 0; j < ntap; ++j) {
-                    // wtap: the tap's slice of the weight rows
-                    int wtap = 0, kh = 1, kw = 1, fidx = frames;  // frames: out of range -> zeros
-                    const CUtensorMap *am = mapA;
-                    if (!shortcut && p.taps == 27) {
-                        // (constant divisors on either path: this thread must
-                        // keep ahead of the MMAs)
-                        const int q = seg * p.itb + j;
-                        int kt;
-                        if (kUp) {  // the phase's 2 x 2 taps, current frame only
-                            kt = 2;
-                            kh = tbase.kh + ((q >> 1) & 1);
-                            kw = tbase.kw + (q & 1);
-                            wtap = q & 3;
-                        } else {
-                            const int tap = kt0 * 9 + q;
-                            kt = tap / 9;
-                            kh = (tap / 3) % 3;
-                            kw = tap % 3;
-                            wtap = tap;
-                        }
-                        const int tt = ti.t + kt - 2;
-                        if (!ti.dummy) {
-                            if (tt >= 0) {
-                                fidx = ti.n * p.T + tt;
-                            } else if (p.has_cache) {
-                                am = mapC;
-                                fidx = ti.n * 2 + tt + 2;
-                            }
-                        }
-                    }
+#pragma unroll
+                for (int j = 0; j < kMaxItb; ++j) {
+                    if (j >= ntap) break;
+                    const CUtensorMap *am = from_cache[j] ? mapC : mapA;
                     for (int s = 0; s < nch; ++s) {
                         const int c0 = (kc * nch + s) * p.sw;
                         const int idx = j * nch + s;  // sub-tile of the stage
@@ -307,24 +326,22 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                                 tma_load_2d_pair(da, mapSA, fb, c0, row0);
                             else if (p.taps == 27)
                                 tma_load_im2col_4d_pair(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1,
-                                                        fidx, (uint16_t)kw, (uint16_t)kh);
+                                                        fidx[j], (uint16_t)kw[j], (uint16_t)kh[j]);
                             else
                                 tma_load_2d_pair(da, mapA, fb, c0, row0);
                         } else {
                             if (shortcut)
                                 tma_load_2d(da, mapSA, fb, c0, row0);
                             else if (p.taps == 27)
-                                tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx,
-                                                   (uint16_t)kw, (uint16_t)kh);
+                                tma_load_im2col_4d(da, am, fb, c0, ti.w0 - 1, ti.h0 - 1, fidx[j],
+                                                   (uint16_t)kw[j], (uint16_t)kh[j]);
                             else
                                 tma_load_2d(da, mapA, fb, c0, row0);
                         }
                         // This CTA's rows of every N-piece in one box: the weight
                         // map is viewed as [piece][pair rank][half_n rows][K].
                         const uint32_t db = sb + (uint32_t)idx * p.b_sub_bytes;
-                        const CUtensorMap *bm = shortcut ? mapSB : mapB;
-                        const int bk = shortcut ? c0 : wtap * p.c_in + c0;
-                        const int ph = kUp ? unit_phase(u, p) : 0;  // upsampler: its weights
+                        const int bk = shortcut ? c0 : wtap[j] * p.c_in + c0;
                         if (kPair == 2)
                             tma_load_4d_pair(db, bm, fb, bk, (int)rank * p.bc_row,
                                              (int)rank * p.bc_rank + ph * p.ph_c2,
@@ -345,7 +362,7 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
         // Aborted: let the newest fill of every stage land before the CTA
         // (and its shared memory) goes away.
         volatile int no_abort = 0;
-        const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+        const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
         const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
         for (uint32_t f = fills - n; f < fills; ++f)
             mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
@@ -495,7 +512,7 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         // Aborted: let the newest fill of every stage (halo loads included)
         // land before the CTA and its shared memory go away.
         volatile int no_abort = 0;
-        const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+        const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
         const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
         for (uint32_t f = fills - n; f < fills; ++f)
             mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
@@ -713,7 +730,7 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         commit(bars.accf(a));
     }
     volatile int no_abort = 0;
-    const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+    const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
     if (kPair == 2)
         mma_commit_pair(bars.drain());
     else
@@ -763,7 +780,7 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
     }
     // Every MMA issued above completes before TMEM is released.
     volatile int no_abort = 0;
-    const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+    const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
     if (kPair == 2)
         mma_commit_pair(bars.drain());
     else
@@ -1183,7 +1200,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         bulk_wait_all();
         if (res_pending) {  // aborted with a residual load in flight: let it land
             volatile int no_abort = 0;
-            const WaitCtl dc{kDrainNs, wc.err, &no_abort};
+            const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
             mbar_wait(bars.resf(), res_phase, dc);
         }
     }
@@ -1271,7 +1288,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const WaitCtl wc{p.wait_ns, p.err, abort_flag};
+    const WaitCtl wc{p.wait_ns, p.err, abort_flag, 0u};
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1538,29 +1555,29 @@ struct Plan {
 // Halo tiles (16 x 8 patches, one halo load per temporal tap and channel
 // chunk feeding all nine spatial taps) move ~6x fewer A bytes and 9x fewer A
 // loads than per-tap im2col, but cover H x W in whole patches: chosen when
-// the patches tile the frame exactly.  WANVAE_CONV_HALO=0/1 forces either.
+// the patches tile the frame exactly.  The kernel-variant setting
+// (set_kernel_variant) can force either.
 int halo_choice(const ConvSpec &s) {
     if (s.k != 3) return 0;
-    const char *e = getenv("WANVAE_CONV_HALO");
-    if (e && e[0] && e[1] == 0 && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+    const int v = g_variant[kVarHalo].load(std::memory_order_relaxed);
+    if (v == 0 || v == 1) return v;
     return s.H % 16 == 0 && s.W % 8 == 0;
 }
 
 // CTA pairs halve each CTA's share of the B (weight) operand -- half the
 // shared-memory bytes per stage, so a deeper pipeline, and half the L2->SM
-// traffic for B.  WANVAE_CONV_PAIR=1 selects the single-CTA kernel instead.
+// traffic for B.  The kernel-variant setting can select the single-CTA kernel.
 int pair_choice() {
-    const char *e = getenv("WANVAE_CONV_PAIR");
-    return (e && e[0] == '1' && e[1] == 0) ? 1 : 2;
+    return g_variant[kVarPair].load(std::memory_order_relaxed) == 1 ? 1 : 2;
 }
 
 // Wide halo tiles (16 x 16 patches, two accumulators per CTA) where the
 // patches tile the frame and the layer is narrow enough (make_plan checks
-// c_out and the shortcut).  WANVAE_CONV_WIDE=0/1 forces either.
+// c_out and the shortcut).  The kernel-variant setting can force either.
 int wide_choice(const ConvSpec &s, int halo) {
     if (!halo) return 0;
-    const char *e = getenv("WANVAE_CONV_WIDE");
-    if (e && e[0] && e[1] == 0 && (e[0] == '0' || e[0] == '1')) return e[0] == '1';
+    const int v = g_variant[kVarWide].load(std::memory_order_relaxed);
+    if (v == 0 || v == 1) return v;
     return s.H % 16 == 0 && s.W % 16 == 0;
 }
 
@@ -1847,9 +1864,19 @@ int conv3d_supported(const ConvSpec &s) {
         return -1;
     if (s.c_in > 4096) return -1;
     if (s.sc_in && (s.c_sc < 16 || s.c_sc % 16 || s.c_sc > 4096)) return -1;
+    if (conv3d_narrow_supported(s) == 0) return 0;
     Plan pl;
-    return pick_plan(s, pl, 2) ? 0 : -1;
+    return pick_plan(s, pl, pair_choice()) ? 0 : -1;
 }
+
+void set_kernel_variant(int pair, int halo, int wide, int narrow) {
+    const int v[kNumVar] = {pair, halo, wide, narrow};
+    for (int i = 0; i < kNumVar; ++i)
+        g_variant[i].store(v[i] == 0 || v[i] == 1 || (i == kVarPair && v[i] == 2) ? v[i] : -1,
+                           std::memory_order_relaxed);
+}
+
+int narrow_variant() { return g_variant[kVarNarrow].load(std::memory_order_relaxed); }
 
 bool encode_tiled_bf16(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims,
                        const cuuint64_t *strides, const cuuint32_t *box, int swizzle_bytes) {

@@ -81,6 +81,14 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx);
 int conv3d_narrow_supported(const ConvSpec &s);
 cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx);
 
+// Kernel-variant overrides, process-wide (wanvae_set_kernel_variant): each
+// argument 0 or 1 forces that choice, anything else restores the automatic
+// choice.  pair: 1 = single-CTA kernel, else CTA pairs; halo: halo tiles (1)
+// or im2col tiles (0); wide: 16 x 16 halo patches (1) or 16 x 8 (0); narrow:
+// the GEMM-plus-stencil kernel for c_out <= 3 (1) or the implicit GEMM (0).
+void set_kernel_variant(int pair, int halo, int wide, int narrow);
+int narrow_variant();
+
 // cuTensorMapEncodeTiled for a bf16 tensor of `rank` dimensions (driver
 // entry point looked up once); swizzle_bytes 0, 32, 64 or 128.  False when
 // the entry point is missing or the encoding is rejected.

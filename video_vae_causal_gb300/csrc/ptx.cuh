@@ -13,6 +13,8 @@ namespace wanvae {
 enum : unsigned {
     kDevErrTimeout = 1u,  // a bounded wait gave up
     kDevErrAlign = 2u,    // a TMA store's shared-memory source was misaligned (skipped)
+    kDevErrDrain = 4u,    // after an abort, a wait for the kernel's own in-flight copies or
+                          // MMAs gave up too: they may still land after the CTA has gone
 };
 
 // How long a bounded wait may spin before giving up, and where it reports.
@@ -20,6 +22,7 @@ struct WaitCtl {
     uint64_t limit_ns;      // give up after this many ns of spinning
     unsigned *err;          // device error word (global memory)
     volatile int *abort;    // CTA-wide abort flag (shared memory)
+    unsigned give_up_bits;  // bits raised when the wait gives up (0: kDevErrTimeout)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -123,7 +126,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 >= w.limit_ns) {
             *w.abort = 1;
-            atomicOr(w.err, kDevErrTimeout);
+            atomicOr(w.err, w.give_up_bits ? w.give_up_bits : kDevErrTimeout);
             return false;
         }
     }
@@ -143,7 +146,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
             if (ok || *w.abort) break;
             if (lane == 0 && globaltimer_ns() - t0 >= w.limit_ns) {
                 *w.abort = 1;
-                atomicOr(w.err, kDevErrTimeout);
+                atomicOr(w.err, w.give_up_bits ? w.give_up_bits : kDevErrTimeout);
                 break;
             }
         }

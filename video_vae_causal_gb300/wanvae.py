@@ -13,7 +13,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libwanvae.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT,
+ ERR_UNDRAINED) = range(8)
 BF16, F32 = 0, 1
 
 # Every exported symbol of include/wanvae.h.
@@ -22,7 +23,7 @@ EXPORTS = (
     "wanvae_resblock_workspace_size", "wanvae_resblock_forward",
     "wanvae_resblock_forward_profiled", "wanvae_sync_status", "wanvae_set_wait_limit_ns",
     "wanvae_launch_count", "wanvae_resblock_forward_static", "wanvae_upsample2d_workspace_size",
-    "wanvae_upsample2d_conv",
+    "wanvae_upsample2d_conv", "wanvae_set_kernel_variant",
 )
 
 # Size of the library's own workspace used by resblock_forward_static.
@@ -87,6 +88,8 @@ def load(path=LIB_PATH):
     L.wanvae_sync_status.restype = st
     L.wanvae_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.wanvae_set_wait_limit_ns.restype = None
+    L.wanvae_set_kernel_variant.argtypes = [ci, ci, ci, ci]
+    L.wanvae_set_kernel_variant.restype = None
     L.wanvae_launch_count.argtypes = []
     L.wanvae_launch_count.restype = ctypes.c_uint64
     L.wanvae_resblock_forward_static.argtypes = [ctypes.POINTER(ResblockParams), vp, vp, Dims,
@@ -133,6 +136,11 @@ def launch_count():
 
 def set_wait_limit_ns(ns):
     load().wanvae_set_wait_limit_ns(int(ns))
+
+
+def set_kernel_variant(pair=-1, halo=-1, wide=-1, narrow=-1):
+    """Force kernel variants for later calls (0 or 1 each; -1 = automatic)."""
+    load().wanvae_set_kernel_variant(int(pair), int(halo), int(wide), int(narrow))
 
 
 def sync_status(stream=None):
