@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["tiny", "latent_fullT", "stream_720p", "reduce_384_192",
                              "fullres_96", "conv_in_latent", "post_quant_latent",
-                             "conv_out_fullres", "upsample2d_fullres"],
+                             "conv_out_fullres", "upsample2d_fullres", "time_upsample_latent"],
                     help="fullres_96 (default) is the headline; the others are the remaining "
                          "workloads of the design notes (the conv_* / post_quant_* ones time "
                          "one CausalConv3d call: the decoder's boundary convs)")
@@ -189,6 +189,9 @@ WORKLOAD_TEXT = {
     "upsample2d_fullres": "upsample2d_fullres: nearest 2x upsampling + 3x3 conv of x bf16 "
                           "[1,81,240,416,192] -> [1,81,480,832,96] (the last up block's "
                           "upsampler)",
+    "time_upsample_latent": "time_upsample_latent: nearest 2x upsampling in T + causal 3x1x1 "
+                            "conv of x bf16 [1,21,60,104,384] -> [1,42,60,104,384] (the "
+                            "temporal half of the first up block's upsample3d)",
 }
 
 
@@ -232,7 +235,8 @@ def bench_reference(args):
     import oracle
     from video_vae_causal_gb300 import synth
     name = args.workload
-    if name in synth.CONV_WORKLOADS or name in synth.UPSAMPLE_WORKLOADS:
+    if (name in synth.CONV_WORKLOADS or name in synth.UPSAMPLE_WORKLOADS
+            or name in synth.TIME_UPSAMPLE_WORKLOADS):
         return bench_reference_conv(args)
     dims, ci, co, _ = synth.WORKLOADS[name]
     B, T, H, W = dims
@@ -270,17 +274,23 @@ def bench_reference_conv(args):
     from video_vae_causal_gb300 import synth
     name = args.workload
     up = name in synth.UPSAMPLE_WORKLOADS
+    upt = name in synth.TIME_UPSAMPLE_WORKLOADS
     if up:
         dims, ci, co = synth.UPSAMPLE_WORKLOADS[name]
         B, T, H, W = dims
         x, w, b = synth.make_upsample_inputs((B, min(T, 3), H, W), ci, co, seed=0)
         fn = oracle.upsample2d_conv
+    elif upt:
+        dims, ci, co = synth.TIME_UPSAMPLE_WORKLOADS[name]
+        B, T, H, W = dims
+        x, w, b = synth.make_time_upsample_inputs((B, min(T, 3), H, W), ci, co, seed=0)
+        fn = oracle.time_upsample_conv
     else:
         dims, ci, co, k = synth.CONV_WORKLOADS[name]
         B, T, H, W = dims
         x, w, b = synth.make_conv_inputs((B, min(T, 3), H, W), ci, co, k, seed=0)
         fn = oracle.causal_conv3d
-    per_row = 4 if up else 1  # output voxels per input voxel
+    per_row = 4 if up else (2 if upt else 1)  # output voxels per input voxel
     steps = args.steps if args.steps else 10
     budget = max(1.0, 60.0 / max(1, steps + args.warmup))
     t0 = time.perf_counter()
@@ -297,8 +307,7 @@ def bench_reference_conv(args):
     sample = f"the clip's first {x.shape[1]} frames over {rows} of {H} rows x {W} columns"
     print(json.dumps({
         "impl": "reference",
-        "metric": ("Upsampler output voxels/s" if up else "CausalConv3d voxels/s") +
-                  " (roofline: the bound its arithmetic intensity sets)",
+        "metric": metric_name(up, upt),
         "value": v, "unit": "voxels/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -332,6 +341,12 @@ def time_one(stream, fn):
     return a.elapsed_time(b)
 
 
+def metric_name(up, upt):
+    what = ("Upsampler output voxels/s" if up else
+            "Temporal upsampler output voxels/s" if upt else "CausalConv3d voxels/s")
+    return what + " (roofline: the bound its arithmetic intensity sets)"
+
+
 def bench_conv(args):
     """One CausalConv3d call per step (the decoder's boundary convs): device
     time by CUDA events around the call, end to end with host buffers, the
@@ -352,8 +367,12 @@ def bench_conv(args):
     wanvae.load()
     name = args.workload
     up = name in synth.UPSAMPLE_WORKLOADS
+    upt = name in synth.TIME_UPSAMPLE_WORKLOADS
     if up:
         dims, ci, co = synth.UPSAMPLE_WORKLOADS[name]
+        k = 3
+    elif upt:
+        dims, ci, co = synth.TIME_UPSAMPLE_WORKLOADS[name]
         k = 3
     else:
         dims, ci, co, k = synth.CONV_WORKLOADS[name]
@@ -361,23 +380,30 @@ def bench_conv(args):
         dims = (dims[0], args.frames) + tuple(dims[2:])
     B, T, H, W = dims
     Ho, Wo = (2 * H, 2 * W) if up else (H, W)
-    M = B * T * Ho * Wo                       # output voxels
+    To = 2 * T if upt else T
+    M = B * To * Ho * Wo                      # output voxels
     on_dev = M * max(ci, co) > (1 << 30)
-    make = synth.make_upsample_inputs if up else (
-        lambda d, a, c, seed, device: synth.make_conv_inputs(d, a, c, k, seed=seed, device=device))
+    make = (synth.make_upsample_inputs if up else synth.make_time_upsample_inputs if upt else
+            lambda d, a, c, seed, device: synth.make_conv_inputs(d, a, c, k, seed=seed,
+                                                                 device=device))
     x, w, b = make(dims, ci, co, seed=0, device=dev if on_dev else "cpu")
     x_cpu = None if on_dev else x
     w_cpu, b_cpu = w.cpu(), b.cpu()
     x, w, b = x.to(dev), w.to(dev), b.to(dev)
-    y = torch.empty((B, T, Ho, Wo, co), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((B, To, Ho, Wo, co), dtype=torch.bfloat16, device=dev)
     ws_up = None
     if up:
         n = int(wanvae.load().wanvae_upsample2d_workspace_size(ci, co))
+        ws_up = torch.empty(n, dtype=torch.uint8, device=dev)
+    elif upt:
+        n = int(wanvae.load().wanvae_time_upsample_workspace_size(ci, co))
         ws_up = torch.empty(n, dtype=torch.uint8, device=dev)
 
     def call(xin):
         if up:
             wanvae.upsample2d_conv(xin, w, b, y=y, workspace=ws_up)
+        elif upt:
+            wanvae.time_upsample_conv(xin, w, b, y=y, workspace=ws_up)
         else:
             wanvae.causal_conv3d(xin, w, b, y=y)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -409,7 +435,7 @@ def bench_conv(args):
     if x_cpu is None:
         x_cpu = x.cpu()
     x_host = x_cpu.pin_memory()
-    y_host = torch.empty((B, T, Ho, Wo, co), dtype=torch.bfloat16).pin_memory()
+    y_host = torch.empty((B, To, Ho, Wo, co), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
     E = max(1, min(args.e2e_steps, K))
     for _ in range(2):
@@ -430,8 +456,10 @@ def bench_conv(args):
     peaks = load_peaks()
     # useful work (a padded N is not counted).  The upsampler: the 2 x 2 sub-pixel
     # conv each output voxel reduces to exactly (the 3 x 3 conv of the upsampled
-    # frame would count 9 taps instead of 4: reported beside it, not used)
-    flop = 2.0 * (4 if up else k ** 3) * ci * co * M
+    # frame would count 9 taps instead of 4: reported beside it, not used).  The
+    # temporal upsampler likewise: 2 taps per output voxel, not the 3 of the
+    # 3x1x1 conv over the repeated frames.
+    flop = 2.0 * (4 if up else 2 if upt else k ** 3) * ci * co * M
     nbytes = (ci * 2.0 * B * T * H * W + co * 2.0 * M + w.numel() * 2.0 + co * 4.0)  # x, y once
     tflops = flop / (ms / 1e3) / 1e12
     gbs = nbytes / (ms / 1e3) / 1e9
@@ -440,10 +468,12 @@ def bench_conv(args):
               "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"], "flop_per_launch": flop}
     if up:
         tensor["flop_per_launch_3x3_on_upsampled"] = 2.0 * 9 * ci * co * M
+    if upt:
+        tensor["flop_per_launch_3x1x1_on_upsampled"] = 2.0 * 3 * ci * co * M
     hbm = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
            "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": nbytes}
     main, other = (tensor, hbm) if flop / nbytes >= ridge else (hbm, tensor)
-    narrow = not up and ci >= 32 and ci % 32 == 0 and ci <= 128 and co <= 3 and k == 3
+    narrow = not up and not upt and ci >= 32 and ci % 32 == 0 and ci <= 128 and co <= 3 and k == 3
     kname = "conv3d_narrow" if narrow else "conv3d_tcgen05"
     traffic = None if args.frames else profiled_traffic(
         name, kname, (kname + ".cu", "ptx.cuh"))
@@ -455,8 +485,7 @@ def bench_conv(args):
             dist.destroy_process_group()
         return
     line = {
-        "metric": ("Upsampler output voxels/s" if up else "CausalConv3d voxels/s") +
-                  " (roofline: the bound its arithmetic intensity sets)",
+        "metric": metric_name(up, upt),
         "value": value, "unit": "voxels/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
@@ -471,7 +500,8 @@ def bench_conv(args):
         import oracle
         # The oracle on the first frames of the clip over as many rows as fit ~10 s.
         xs = x_cpu[:, :min(T, 3)]
-        fn = oracle.upsample2d_conv if up else oracle.causal_conv3d
+        fn = (oracle.upsample2d_conv if up else oracle.time_upsample_conv if upt else
+              oracle.causal_conv3d)
         t0 = time.perf_counter()
         fn(xs[:, :, :1], w_cpu, b_cpu)
         t1 = max(time.perf_counter() - t0, 1e-3)
@@ -479,7 +509,7 @@ def bench_conv(args):
         t0 = time.perf_counter()
         fn(xs[:, :, :rows], w_cpu, b_cpu)
         dt = time.perf_counter() - t0
-        vox = xs.shape[0] * xs.shape[1] * rows * W * (4 if up else 1)  # output voxels
+        vox = xs.shape[0] * xs.shape[1] * rows * W * (4 if up else 2 if upt else 1)  # output
         line["cpu_baseline"] = {"value": vox / dt, "unit": "voxels/s",
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": f"the clip's first {xs.shape[1]} frames over {rows} "
@@ -671,7 +701,7 @@ def main():
     if args.impl == "reference":
         bench_reference(args)
     elif args.workload in ("conv_in_latent", "post_quant_latent", "conv_out_fullres",
-                           "upsample2d_fullres"):
+                           "upsample2d_fullres", "time_upsample_latent"):
         bench_conv(args)
     else:
         bench_ours(args)

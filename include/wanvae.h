@@ -157,6 +157,28 @@ wanvae_status wanvae_upsample2d_conv(const void *x, const void *w, const float *
                                      wanvae_dims d, int64_t c_in, int64_t c_out,
                                      void *workspace, size_t ws_bytes, wanvae_stream stream);
 
+/* The temporal half of the decoder's upsample3d ("Sharding of WAN 2.2 VAE",
+ * decoder tree: WanUpBlock(..., upsample3d); the graph's 3x1x1 conv kernels,
+ * "Closing the gap", section 3): every frame repeated twice in T (nearest
+ * neighbour), then a causal conv with a 3x1x1 kernel (two zero frames before
+ * the first) and a bias.  The pages give no more; this is the plainest
+ * reading.  The spatial half is wanvae_upsample2d_conv on this call's output.
+ *   x     : bf16 [B][T][H][W][c_in]
+ *   w     : bf16 [c_out][3][c_in] (tap 2 reads the current upsampled frame)
+ *   bias  : fp32 [c_out] (NULL = zeros)
+ *   y     : bf16 [B][2T][H][W][c_out]
+ *   workspace : device buffer of wanvae_time_upsample_workspace_size(c_in,
+ *           c_out) bytes, 256-byte aligned, for the two frame phases'
+ *           weights: output frame 2t + a is a 2-tap conv of input frames
+ *           t - 1 and t whose taps are bf16 sums of the 3 taps (one more
+ *           rounding of the weights than the plain definition).
+ *   c_in, c_out : multiples of 16 up to 512.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+size_t wanvae_time_upsample_workspace_size(int64_t c_in, int64_t c_out);
+wanvae_status wanvae_time_upsample_conv(const void *x, const void *w, const float *bias,
+                                        void *y, wanvae_dims d, int64_t c_in, int64_t c_out,
+                                        void *workspace, size_t ws_bytes, wanvae_stream stream);
+
 /* Bytes of device workspace wanvae_resblock_forward needs for these sizes
  * (the bf16 conv inputs a1 and a2, 256-byte aligned).  0 on invalid sizes. */
 size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out);

@@ -107,6 +107,20 @@ def test_upsample_argument_errors(lib):
     assert f(A, A + 4, None, Y, d, 32, 16, WS, n, None) == wanvae.ERR_MISALIGNED
 
 
+def test_time_upsample_argument_errors(lib):
+    f = lib.wanvae_time_upsample_conv
+    d = _dims(1, 2, 4, 4)
+    Y, WS = 0x900000, 0x2000000
+    n = lib.wanvae_time_upsample_workspace_size(32, 16)
+    assert n == 2 * 2 * 32 * 16 * 2  # 2 phases x 2 taps
+    assert f(None, A, None, Y, d, 32, 16, WS, n, None) == wanvae.ERR_INVALID_ARG
+    assert f(A, A, None, Y, d, 32, 16, None, n, None) == wanvae.ERR_INVALID_ARG
+    assert f(A, A, None, Y, d, 32, 528, WS, 1 << 30, None) == wanvae.ERR_UNSUPPORTED
+    assert f(A, A, None, Y, d, 40, 16, WS, n, None) == wanvae.ERR_UNSUPPORTED
+    assert f(A, A, None, Y, d, 32, 16, WS, n - 2, None) == wanvae.ERR_WORKSPACE
+    assert f(A, A + 4, None, Y, d, 32, 16, WS, n, None) == wanvae.ERR_MISALIGNED
+
+
 def test_resblock_argument_errors(lib):
     f = lib.wanvae_resblock_forward
     d = _dims(1, 2, 4, 4)

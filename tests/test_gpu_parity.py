@@ -210,6 +210,29 @@ def test_upsample2d_conv(cuda_lib, case, variant):
     compare(to_f64(y), oracle.upsample2d_conv(x, w, b), what=f"upsample2d {case}")
 
 
+# --------------------------------------------------------- temporal upsampler
+TIME_UP_CASES = [
+    # (B, T, H, W, c_in, c_out); output is 2T frames
+    (1, 1, 5, 7, 32, 16),       # one frame: both phases read the causal zero frame
+    (2, 3, 6, 9, 64, 32),       # two clips: frame t - 1 never crosses into the other
+    (1, 4, 8, 16, 96, 48),
+    (1, 2, 9, 13, 384, 384),    # the first up block's 384 channels (one accumulator)
+]
+
+
+@pytest.mark.parametrize("case", TIME_UP_CASES)
+def test_time_upsample_conv(cuda_lib, case, variant):
+    B, T, H, W, ci, co = case
+    x = synth.make_tensor((B, T, H, W, ci), seed=200 + sum(case))
+    bound = 1.0 / np.sqrt(3 * ci)
+    w = synth.make_tensor((co, 3, ci), seed=201 + sum(case), kind="uniform", lo=-bound,
+                          hi=bound)
+    b = synth.make_tensor((co,), seed=202, dtype=torch.float32, kind="uniform", lo=-.1, hi=.1)
+    y = cuda_lib.time_upsample_conv(x.to(DEV), w.to(DEV), b.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.time_upsample_conv(x, w, b), what=f"time upsample {case}")
+
+
 # ------------------------------------------------------------------ block
 BLOCK_CASES = [
     # (B, T, H, W, c_in, c_out)

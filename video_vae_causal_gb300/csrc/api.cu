@@ -232,6 +232,57 @@ wanvae_status wanvae_upsample2d_conv(const void *x, const void *w, const float *
     return from_cuda(e);
 }
 
+size_t wanvae_time_upsample_workspace_size(int64_t c_in, int64_t c_out) {
+    if (c_in < 1 || c_out < 1 || c_in > 4096 || c_out > 4096) return 0;
+    return align256((size_t)2 * 2 * c_in * c_out * 2);  // 2 phases x 2 taps
+}
+
+wanvae_status wanvae_time_upsample_conv(const void *x, const void *w, const float *bias, void *y,
+                                        wanvae_dims d, int64_t c_in, int64_t c_out,
+                                        void *workspace, size_t ws_bytes, wanvae_stream stream) {
+    if (!x || !w || !y || !workspace) return WANVAE_ERR_INVALID_ARG;
+    if (!dims_ok(d) || c_in < 1 || c_out < 1) return WANVAE_ERR_INVALID_ARG;
+    if (c_in % 16 || c_out % 16 || c_in > 512 || c_out > 512) return WANVAE_ERR_UNSUPPORTED;
+    if (misaligned(x) || misaligned(w) || misaligned(y) || misaligned(bias) ||
+        misaligned(workspace))
+        return WANVAE_ERR_MISALIGNED;
+    const size_t need = wanvae_time_upsample_workspace_size(c_in, c_out);
+    if (ws_bytes < need) return WANVAE_ERR_WORKSPACE;
+    const int64_t M = voxels(d);
+    const size_t xb = (size_t)M * c_in * 2, yb = (size_t)M * 2 * c_out * 2;
+    if (overlap(x, xb, y, yb) || overlap(workspace, need, y, yb) ||
+        overlap(workspace, need, x, xb))
+        return WANVAE_ERR_INVALID_ARG;
+
+    ConvSpec s;
+    memset(&s, 0, sizeof(s));
+    s.in = x;
+    s.w = workspace;  // phase weights [2][c_out][2][c_in]
+    s.bias = bias;
+    s.out = y;
+    s.B = (int)d.B;
+    s.T = (int)d.T;
+    s.H = (int)d.H;
+    s.W = (int)d.W;
+    s.c_in = (int)c_in;
+    s.c_out = (int)c_out;
+    s.k = 3;
+    s.epi = kEpiBias;
+    s.up_t = 1;
+    if (conv3d_supported(s)) return WANVAE_ERR_UNSUPPORTED;
+
+    LaunchCtx ctx;
+    const wanvae_status st = make_ctx(ctx, stream);
+    if (st != WANVAE_OK) return st;
+    g_launches++;
+    cudaError_t e = launch_expand_time_up_weights(w, workspace, (int)c_out, (int)c_in, ctx);
+    if (e == cudaSuccess) {
+        g_launches++;
+        e = launch_conv3d(s, ctx);
+    }
+    return from_cuda(e);
+}
+
 size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out) {
     if (!dims_ok(d) || c_in < 1 || c_out < 1 || c_in > 4096 || c_out > 4096) return 0;
     const size_t M = (size_t)voxels(d);

@@ -329,6 +329,7 @@ bool narrow_enabled() { return narrow_variant() != 0; }
 int conv3d_narrow_supported(const ConvSpec &s) {
     if (!narrow_enabled()) return -1;
     if (s.k != 3 || s.c_out < 1 || s.c_out > 3 || s.sc_in || s.epi != kEpiBias) return -1;
+    if (s.up2d || s.up_t) return -1;  // plain convs only
     if (s.c_in < 32 || s.c_in % 32 || s.c_in > 128) return -1;
     return 0;
 }

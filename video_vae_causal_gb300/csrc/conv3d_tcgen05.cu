@@ -80,6 +80,7 @@ struct ConvArgs {
     int segs_per_kt;     // im2col: stages per temporal tap and channel chunk, sp_taps / itb
     int na;              // halo mode: buffers in the A (halo) ring, 2 to 4
     int up_tma;          // upsampler on halo tiles: TMA stores through the phase view of y
+    int up_t;            // temporal upsampler: frame phases, taps t-1 and t at the centre pixel
     int ph_c2, ph_c3;    // upsampler: B box coordinates 2 and 3 advance by phase x these
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
@@ -278,7 +279,10 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                 if (j < ntap && !shortcut && p.taps == 27) {
                     const int q = seg * p.itb + j;
                     int kt;
-                    if (kUp) {  // the phase's 2 x 2 taps, current frame only
+                    if (kUp && p.up_t) {  // frames t - 1 and t, centre pixel
+                        kt = 1 + (q & 1);
+                        wtap[j] = q & 1;
+                    } else if (kUp) {  // the phase's 2 x 2 taps, current frame only
                         kt = 2;
                         kh[j] = tbase.kh + ((q >> 1) & 1);
                         kw[j] = tbase.kw + (q & 1);
@@ -1018,15 +1022,22 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                         }
                     }
                 } else if (kUp) {
-                    // Upsampler: low-res pixel (i, j) of this row is output
-                    // pixel (2i + a, 2j + b) of the unit's phase (a, b).
+                    // Spatial upsampler: low-res pixel (i, j) of this row is
+                    // output pixel (2i + a, 2j + b) of the unit's phase (a, b).
+                    // Temporal upsampler: frame t of batch element n is output
+                    // frame 2t + a of the unit's phase a.
                     if (valid) {
                         const int64_t pos = g - (int64_t)ti.frame * p.HW;  // in the frame
-                        const int64_t i = pos / p.W, j = pos - i * p.W;
                         const int ph = unit_phase(u, p);
-                        const int64_t dst =
-                            (((int64_t)ti.frame * 2 * p.H + 2 * i + (ph >> 1)) * 2 * p.W + 2 * j +
-                             (ph & 1)) * p.c_out + c;
+                        int64_t dst;
+                        if (p.up_t) {
+                            dst = (((int64_t)ti.n * 2 * p.T + 2 * ti.t + ph) * p.HW + pos) *
+                                      p.c_out + c;
+                        } else {
+                            const int64_t i = pos / p.W, j = pos - i * p.W;
+                            dst = (((int64_t)ti.frame * 2 * p.H + 2 * i + (ph >> 1)) * 2 * p.W +
+                                   2 * j + (ph & 1)) * p.c_out + c;
+                        }
                         uint4 *d = reinterpret_cast<uint4 *>(p.out + dst);
 #pragma unroll
                         for (int vv = 0; vv < 4; ++vv)
@@ -1637,7 +1648,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
                            4u * 4u * kBlockM /*norm partial sums*/;
     pl.staged = 0;
     if (s.up2d && pl.nacc != 2) return false;  // its scattered stores use the direct epilogue
-    if (pl.nacc == 1 && s.c_out % 64 == 0) {
+    if (pl.nacc == 1 && s.c_out % 64 == 0 && !s.up_t) {  // (the temporal upsampler: direct)
         const uint32_t sb1 = (kBlockM + b_rows) * (uint32_t)sw * 2u;
         if (3u * ((sb1 + 1023u) & ~1023u) + fixed + stage_tile <= (uint32_t)kSmemBudget)
             pl.staged = 1;
@@ -1732,7 +1743,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     // holds three consecutive taps (same K order as one tap per stage).
     // (The upsampler's four taps per phase: two or four per stage.)
     pl.itb = 1;
-    if (s.k == 3 && !s.sc_in && pl.kc_main == 1 && pl.nsub * sw <= 32) {
+    if (s.k == 3 && !s.sc_in && !s.up_t && pl.kc_main == 1 && pl.nsub * sw <= 32) {
         for (int itb : {s.up2d ? 4 : 3, s.up2d ? 2 : 3}) {
             const uint32_t sbt = (uint32_t)itb * pl.nsub * (kBlockM + b_rows) * sw * 2u;
             if (pl.itb == 1 &&
@@ -1849,7 +1860,7 @@ cudaError_t kernel_facts(ConvKernelFn fn, bool pair, int &max_pairs) {
 // The first plan that fits: the preferred CTA grouping with wide halo tiles,
 // then plain halo tiles, then the same on single CTAs, then im2col.
 bool pick_plan(const ConvSpec &s, Plan &pl, int pair) {
-    const int hc = halo_choice(s), wc = wide_choice(s, hc);
+    const int hc = s.up_t ? 0 : halo_choice(s), wc = wide_choice(s, hc);  // (im2col: centre taps)
     return (wc && make_plan(s, pl, pair, hc, 1)) || make_plan(s, pl, pair, hc, 0) ||
            (wc && make_plan(s, pl, 1, hc, 1)) || make_plan(s, pl, 1, hc, 0) ||
            make_plan(s, pl, 1, 0, 0);
@@ -1898,7 +1909,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     if (!pick_plan(s, pl, pair_choice())) return cudaErrorInvalidValue;
     if (!load_encoders()) return cudaErrorInvalidValue;
     auto pick = [&](int pair) {
-        if (s.up2d)
+        if (s.up2d || s.up_t)
             return pair == 2 ? pick_kernel_up<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
                              : pick_kernel_up<1>(pl.sw / 16, pl.nsub, pl.n_pieces);
         return pair == 2 ? pick_kernel<2>(pl.sw / 16, pl.nsub, pl.n_pieces)
@@ -1946,9 +1957,10 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
                                       s.c_out, pl.pair, pl.sw, pl.nsub, pl.tb, pl.npad,
                                       s.up2d ? 4 : 1);
     else
-        ok = ok && encode_weights(&mB, s.w, (uint64_t)(s.up2d ? 4 : s.k * s.k * s.k) * s.c_in,
+        ok = ok && encode_weights(&mB, s.w,
+                                  (uint64_t)(s.up2d ? 4 : s.up_t ? 2 : s.k * s.k * s.k) * s.c_in,
                                   s.c_out, pl.pair, pl.n_pieces, pl.sw, pl.halo ? pl.nsub : 0,
-                                  pl.npad, s.up2d ? 4 : 1);
+                                  pl.npad, s.up2d ? 4 : s.up_t ? 2 : 1);
     if (s.sc_in) {
         if (pl.halo)
             ok = ok && encode_patch(&mSA, s.sc_in, s.c_sc, s.W, s.H, frames, pl.sw, pl.sw);
@@ -2008,17 +2020,18 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.tiles_per_frame = pl.halo ? ((s.H + 15) / 16) * a.patches_w : (HW + kBlockM - 1) / kBlockM;
     a.num_tiles = a.tiles_per_frame * frames;
     a.frames = frames;
-    a.nphase = s.up2d ? 4 : 1;
+    a.nphase = s.up2d ? 4 : s.up_t ? 2 : 1;
     a.tile_units = (a.num_tiles + pl.pair - 1) / pl.pair;
-    a.wtap0 = s.up2d ? 18 : 0;
-    a.sp_taps = s.up2d ? 4 : 9;
-    a.sp_w = s.up2d ? 2 : 3;
+    a.wtap0 = s.up2d ? 18 : s.up_t ? 9 : 0;  // (temporal upsampler: taps kt = 1, 2)
+    a.sp_taps = s.up2d ? 4 : s.up_t ? 1 : 9;
+    a.sp_w = s.up2d ? 2 : s.up_t ? 1 : 3;
+    a.up_t = s.up_t;
     a.segs_per_kt = a.sp_taps / (pl.halo ? 1 : pl.itb);  // (as a.itb)
     // which B box coordinate a phase moves: the rank dimension of the 3-tap
     // map (its pieces are one), else the piece dimension
     const bool taps_map = pl.halo && pl.tb > 1;
     a.ph_c2 = s.up2d && taps_map ? pl.pair : 0;
-    a.ph_c3 = s.up2d && !taps_map ? pl.n_pieces : 0;
+    a.ph_c3 = (s.up2d || s.up_t) && !taps_map ? pl.n_pieces : 0;
     a.stages = pl.stages;
     a.a_sub_bytes = pl.a_sub;
     a.b_sub_bytes = pl.b_sub;

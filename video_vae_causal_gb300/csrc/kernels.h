@@ -33,6 +33,11 @@ cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int6
 cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
                                        const LaunchCtx &ctx);
 
+// Phase weights of the temporal upsampler conv: w [Co][3][Ci] ->
+// w2 [2 phases][Co][2][Ci] (bf16), see rmsnorm_silu.cu.
+cudaError_t launch_expand_time_up_weights(const void *w, void *w2, int Co, int Ci,
+                                          const LaunchCtx &ctx);
+
 // Epilogue of the implicit-GEMM conv.
 enum EpiMode : int {
     kEpiBias = 0,      // out = acc + bias (+ bias2)
@@ -65,6 +70,12 @@ struct ConvSpec {
     // frame's taps only), out is [B][T][2H][2W][c_out]; k = 3, no cache, bias
     // epilogue.
     int up2d;
+    // Temporal upsampler conv (upsample3d's temporal half): nearest 2x in T
+    // then a causal 3x1x1 conv, as two frame phases over the input frames:
+    // output frame 2t + a is a 2-tap conv of input frames t - 1 and t.  w holds
+    // the phase weights [2][c_out][2][c_in]; out is [B][2T][H][W][c_out];
+    // k = 3, no cache, bias epilogue.
+    int up_t;
 };
 
 // Host-side validation of a ConvSpec the library can run (channel counts,

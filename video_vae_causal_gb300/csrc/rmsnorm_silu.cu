@@ -225,7 +225,43 @@ __global__ void expand_up2d_weights_kernel(const __nv_bfloat16 *__restrict__ w,
     }
 }
 
+// Phase weights of the temporal upsampler conv.  Nearest 2x in T then a
+// causal 3-tap conv gives output frame 2t + a as a conv over input frames
+// t - 1 and t: tap kt of the upsampled sequence reads upsampled frame
+// 2t + a + kt - 2, i.e. input frame t - 1 + ((a + kt) >> 1).  So phase a's tap
+// e in {0, 1} (frame t - 1 + e) is the sum of the taps kt with
+// (a + kt) >> 1 == e: w0 + w1 and w2 for a = 0, w0 and w1 + w2 for a = 1.
+// w [Co][3][Ci] -> w2 [2 = a][Co][2 = e][Ci], fp32 sums rounded to bf16.
+__global__ void expand_time_up_weights_kernel(const __nv_bfloat16 *__restrict__ w,
+                                              __nv_bfloat16 *__restrict__ w2, int Co, int Ci) {
+    const int64_t total = (int64_t)2 * Co * 2 * Ci;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % Ci);
+        int64_t r = idx / Ci;
+        const int e = (int)(r & 1);
+        r >>= 1;
+        const int o = (int)(r % Co);
+        const int a = (int)(r / Co);
+        float acc = 0.f;
+        for (int kt = 0; kt < 3; ++kt)
+            if (((a + kt) >> 1) == e) acc += __bfloat162float(w[((int64_t)o * 3 + kt) * Ci + c]);
+        w2[idx] = __float2bfloat16_rn(acc);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_expand_time_up_weights(const void *w, void *w2, int Co, int Ci,
+                                          const LaunchCtx &ctx) {
+    const int64_t total = (int64_t)2 * Co * 2 * Ci;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)ctx.num_sms * 8) blocks = (int64_t)ctx.num_sms * 8;
+    if (blocks < 1) blocks = 1;
+    expand_time_up_weights_kernel<<<(unsigned)blocks, 256, 0, ctx.stream>>>(
+        static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2), Co, Ci);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
                                        const LaunchCtx &ctx) {

@@ -39,6 +39,12 @@ UPSAMPLE_WORKLOADS = {
     "upsample2d_fullres": ((1, 81, 240, 416), 192, 96),
 }
 
+# The temporal half of the decoder's upsample3d (nearest 2x in T, then a causal
+# 3x1x1 conv), as in the first up block: (name, (B, T, H, W), c_in, c_out).
+TIME_UPSAMPLE_WORKLOADS = {
+    "time_upsample_latent": ((1, 21, 60, 104), 384, 384),
+}
+
 
 def _uniform(g, shape, lo, hi, device):
     return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
@@ -85,6 +91,20 @@ def make_conv_inputs(dims, c_in, c_out, k, seed=0, device="cpu"):
                     dtype=torch.float32).to(torch.bfloat16)
     bound = 1.0 / math.sqrt(k * k * k * c_in)
     w = _uniform(g, (c_out, k, k, k, c_in), -bound, bound, device).to(torch.bfloat16)
+    b = _uniform(g, (c_out,), -0.1, 0.1, device)
+    return x, w, b
+
+
+def make_time_upsample_inputs(dims, c_in, c_out, seed=0, device="cpu"):
+    """x [B,T,H,W,c_in] bf16 ~ N(0,1), w [c_out,3,c_in] bf16 ~ U(+-1/sqrt(3 c_in)),
+    bias fp32 ~ U(-0.1, 0.1), drawn in that order from one seeded generator."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, T, H, W = dims
+    x = torch.randn((B, T, H, W, c_in), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    bound = 1.0 / math.sqrt(3 * c_in)
+    w = _uniform(g, (c_out, 3, c_in), -bound, bound, device).to(torch.bfloat16)
     b = _uniform(g, (c_out,), -0.1, 0.1, device)
     return x, w, b
 

@@ -23,7 +23,8 @@ EXPORTS = (
     "wanvae_resblock_workspace_size", "wanvae_resblock_forward",
     "wanvae_resblock_forward_profiled", "wanvae_sync_status", "wanvae_set_wait_limit_ns",
     "wanvae_launch_count", "wanvae_resblock_forward_static", "wanvae_upsample2d_workspace_size",
-    "wanvae_upsample2d_conv", "wanvae_set_kernel_variant",
+    "wanvae_upsample2d_conv", "wanvae_set_kernel_variant", "wanvae_time_upsample_workspace_size",
+    "wanvae_time_upsample_conv",
 )
 
 # Size of the library's own workspace used by resblock_forward_static.
@@ -99,6 +100,11 @@ def load(path=LIB_PATH):
     L.wanvae_upsample2d_workspace_size.restype = ctypes.c_size_t
     L.wanvae_upsample2d_conv.argtypes = [vp, vp, vp, vp, Dims, i64, i64, vp, ctypes.c_size_t, vp]
     L.wanvae_upsample2d_conv.restype = st
+    L.wanvae_time_upsample_workspace_size.argtypes = [i64, i64]
+    L.wanvae_time_upsample_workspace_size.restype = ctypes.c_size_t
+    L.wanvae_time_upsample_conv.argtypes = [vp, vp, vp, vp, Dims, i64, i64, vp, ctypes.c_size_t,
+                                            vp]
+    L.wanvae_time_upsample_conv.restype = st
     _lib = L
     return L
 
@@ -186,6 +192,24 @@ def upsample2d_conv(x, w, bias=None, y=None, workspace=None, stream=None):
     st = L.wanvae_upsample2d_conv(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), _dims(x.shape), c_in,
                                   c_out, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "wanvae_upsample2d_conv")
+    return y
+
+
+def time_upsample_conv(x, w, bias=None, y=None, workspace=None, stream=None):
+    """Nearest 2x upsampling in T, then a causal 3x1x1 conv with bias (the
+    temporal half of upsample3d).  x [B,T,H,W,c_in] bf16, w [c_out,3,c_in]
+    bf16 -> y [B,2T,H,W,c_out]."""
+    B, T, H, W, c_in = x.shape
+    c_out = w.shape[0]
+    if y is None:
+        y = torch.empty((B, 2 * T, H, W, c_out), dtype=torch.bfloat16, device=x.device)
+    L = load()
+    if workspace is None:
+        n = int(L.wanvae_time_upsample_workspace_size(c_in, c_out))
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = L.wanvae_time_upsample_conv(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), _dims(x.shape), c_in,
+                                     c_out, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "wanvae_time_upsample_conv")
     return y
 
 
