@@ -179,6 +179,23 @@ wanvae_status wanvae_time_upsample_conv(const void *x, const void *w, const floa
                                         void *y, wanvae_dims d, int64_t c_in, int64_t c_out,
                                         void *workspace, size_t ws_bytes, wanvae_stream stream);
 
+/* The decoder's whole upsample3d as read from the pages: the temporal half
+ * (wanvae_time_upsample_conv, c_in -> c_mid) and then the spatial upsampler
+ * (wanvae_upsample2d_conv, c_mid -> c_out) on every frame of its output.
+ *   x : bf16 [B][T][H][W][c_in];  y : bf16 [B][2T][2H][2W][c_out]
+ *   w_t : bf16 [c_mid][3][c_in], b_t : fp32 [c_mid] or NULL
+ *   w_s : bf16 [c_out][3][3][c_mid], b_s : fp32 [c_out] or NULL
+ *   workspace : wanvae_upsample3d_workspace_size(d, c_in, c_mid, c_out) bytes,
+ *           256-byte aligned (the [B][2T][H][W][c_mid] intermediate and both
+ *           calls' weight workspaces).
+ * Errors: those of the two calls; WORKSPACE if ws_bytes is short. */
+size_t wanvae_upsample3d_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_mid,
+                                        int64_t c_out);
+wanvae_status wanvae_upsample3d(const void *x, const void *w_t, const float *b_t, const void *w_s,
+                                const float *b_s, void *y, wanvae_dims d, int64_t c_in,
+                                int64_t c_mid, int64_t c_out, void *workspace, size_t ws_bytes,
+                                wanvae_stream stream);
+
 /* Bytes of device workspace wanvae_resblock_forward needs for these sizes
  * (the bf16 conv inputs a1 and a2, 256-byte aligned).  0 on invalid sizes. */
 size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out);

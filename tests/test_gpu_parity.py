@@ -233,6 +233,21 @@ def test_time_upsample_conv(cuda_lib, case, variant):
     compare(to_f64(y), oracle.time_upsample_conv(x, w, b), what=f"time upsample {case}")
 
 
+def test_upsample3d(cuda_lib):
+    """The composite (time then space) against the oracle's upsample3d."""
+    B, T, H, W, ci, cm, co = 1, 2, 6, 9, 64, 64, 32
+    x = synth.make_tensor((B, T, H, W, ci), seed=400)
+    bt_ = 1.0 / np.sqrt(3 * ci)
+    w_t = synth.make_tensor((cm, 3, ci), seed=401, kind="uniform", lo=-bt_, hi=bt_)
+    b_t = synth.make_tensor((cm,), seed=402, dtype=torch.float32, kind="uniform", lo=-.1, hi=.1)
+    bs_ = 1.0 / np.sqrt(9 * cm)
+    w_s = synth.make_tensor((co, 3, 3, cm), seed=403, kind="uniform", lo=-bs_, hi=bs_)
+    b_s = synth.make_tensor((co,), seed=404, dtype=torch.float32, kind="uniform", lo=-.1, hi=.1)
+    y = cuda_lib.upsample3d(x.to(DEV), w_t.to(DEV), b_t.to(DEV), w_s.to(DEV), b_s.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.upsample3d(x, w_t, b_t, w_s, b_s), what="upsample3d")
+
+
 # ------------------------------------------------------------------ block
 BLOCK_CASES = [
     # (B, T, H, W, c_in, c_out)

@@ -24,7 +24,7 @@ EXPORTS = (
     "wanvae_resblock_forward_profiled", "wanvae_sync_status", "wanvae_set_wait_limit_ns",
     "wanvae_launch_count", "wanvae_resblock_forward_static", "wanvae_upsample2d_workspace_size",
     "wanvae_upsample2d_conv", "wanvae_set_kernel_variant", "wanvae_time_upsample_workspace_size",
-    "wanvae_time_upsample_conv",
+    "wanvae_time_upsample_conv", "wanvae_upsample3d_workspace_size", "wanvae_upsample3d",
 )
 
 # Size of the library's own workspace used by resblock_forward_static.
@@ -105,6 +105,11 @@ def load(path=LIB_PATH):
     L.wanvae_time_upsample_conv.argtypes = [vp, vp, vp, vp, Dims, i64, i64, vp, ctypes.c_size_t,
                                             vp]
     L.wanvae_time_upsample_conv.restype = st
+    L.wanvae_upsample3d_workspace_size.argtypes = [Dims, i64, i64, i64]
+    L.wanvae_upsample3d_workspace_size.restype = ctypes.c_size_t
+    L.wanvae_upsample3d.argtypes = [vp, vp, vp, vp, vp, vp, Dims, i64, i64, i64, vp,
+                                    ctypes.c_size_t, vp]
+    L.wanvae_upsample3d.restype = st
     _lib = L
     return L
 
@@ -210,6 +215,24 @@ def time_upsample_conv(x, w, bias=None, y=None, workspace=None, stream=None):
     st = L.wanvae_time_upsample_conv(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), _dims(x.shape), c_in,
                                      c_out, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "wanvae_time_upsample_conv")
+    return y
+
+
+def upsample3d(x, w_t, b_t, w_s, b_s, y=None, workspace=None, stream=None):
+    """upsample3d: the temporal half (w_t [c_mid,3,c_in]) then the spatial
+    upsampler (w_s [c_out,3,3,c_mid]).  x [B,T,H,W,c_in] -> [B,2T,2H,2W,c_out]."""
+    B, T, H, W, c_in = x.shape
+    c_mid, c_out = w_t.shape[0], w_s.shape[0]
+    if y is None:
+        y = torch.empty((B, 2 * T, 2 * H, 2 * W, c_out), dtype=torch.bfloat16, device=x.device)
+    L = load()
+    if workspace is None:
+        n = int(L.wanvae_upsample3d_workspace_size(_dims(x.shape), c_in, c_mid, c_out))
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = L.wanvae_upsample3d(_ptr(x), _ptr(w_t), _ptr(b_t), _ptr(w_s), _ptr(b_s), _ptr(y),
+                             _dims(x.shape), c_in, c_mid, c_out, _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    _check(st, "wanvae_upsample3d")
     return y
 
 
