@@ -52,7 +52,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["tiny", "latent_fullT", "stream_720p", "reduce_384_192",
                              "fullres_96", "conv_in_latent", "post_quant_latent",
-                             "conv_out_fullres", "upsample2d_fullres", "time_upsample_latent"],
+                             "conv_out_fullres", "upsample2d_fullres", "time_upsample_latent",
+                             "mid_attention_latent"],
                     help="fullres_96 (default) is the headline; the others are the remaining "
                          "workloads of the design notes (the conv_* / post_quant_* ones time "
                          "one CausalConv3d call: the decoder's boundary convs)")
@@ -192,6 +193,9 @@ WORKLOAD_TEXT = {
     "time_upsample_latent": "time_upsample_latent: nearest 2x upsampling in T + causal 3x1x1 "
                             "conv of x bf16 [1,21,60,104,384] -> [1,42,60,104,384] (the "
                             "temporal half of the first up block's upsample3d)",
+    "mid_attention_latent": "mid_attention_latent: the mid-block's per-frame spatial "
+                            "self-attention over x bf16 [1,21,60,104,384] (6240 positions per "
+                            "frame, one head of 384, 1x1 q/k/v/out projections, residual)",
 }
 
 
@@ -238,6 +242,8 @@ def bench_reference(args):
     if (name in synth.CONV_WORKLOADS or name in synth.UPSAMPLE_WORKLOADS
             or name in synth.TIME_UPSAMPLE_WORKLOADS):
         return bench_reference_conv(args)
+    if name in synth.ATTENTION_WORKLOADS:
+        return bench_reference_attention(args)
     dims, ci, co, _ = synth.WORKLOADS[name]
     B, T, H, W = dims
     # The oracle only needs the few rows it runs on: draw the clip's first
@@ -345,6 +351,135 @@ def metric_name(up, upt):
     what = ("Upsampler output voxels/s" if up else
             "Temporal upsampler output voxels/s" if upt else "CausalConv3d voxels/s")
     return what + " (roofline: the bound its arithmetic intensity sets)"
+
+
+def bench_reference_attention(args):
+    """The oracle's attention, as it stands, on the host cores: each step one
+    frame of the workload (all its queries against all its keys)."""
+    import oracle
+    from video_vae_causal_gb300 import synth
+    name = args.workload
+    dims, C = synth.ATTENTION_WORKLOADS[name]
+    B, T, H, W = dims
+    x, g, wqkv, bqkv, wo, bo = synth.make_attention_inputs((1, 1, H, W), C, seed=0)
+    steps = args.steps if args.steps else 3
+    vals = []
+    for i in range(args.warmup + steps):
+        t0 = time.perf_counter()
+        oracle.frame_attention(x, g, wqkv, bqkv, wo, bo)
+        if i >= args.warmup:
+            vals.append(H * W / (time.perf_counter() - t0))
+    v = statistics.median(vals)
+    print(json.dumps({
+        "impl": "reference", "metric": ATTN_METRIC, "value": v, "unit": "voxels/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(name, B, T, H, W, C, C, 1),
+        "cpu_baseline": {"value": v, "unit": "voxels/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"one {H}x{W} frame per step"},
+        "e2e": {"value": v, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+ATTN_METRIC = "Attention block voxels/s (roofline: the attention core's TFLOP/s)"
+
+
+def bench_attention(args):
+    """One attention-block call per step: device time by CUDA events around
+    the call, the core's FLOPs (4 N^2 C per frame) against the bf16 peak, end
+    to end with host buffers, and the oracle on one frame."""
+    import torch
+
+    from video_vae_causal_gb300 import synth, wanvae
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    if ws > 1:
+        raise RuntimeError("the attention workload runs on one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wanvae.load()
+    name = args.workload
+    dims, C = synth.ATTENTION_WORKLOADS[name]
+    if args.frames:
+        dims = (dims[0], args.frames) + tuple(dims[2:])
+    B, T, H, W = dims
+    N, F, M = H * W, B * T, B * T * H * W
+    x, g, wqkv, bqkv, wo, bo = synth.make_attention_inputs(dims, C, seed=0)
+    x_cpu = x
+    x, g, wqkv, bqkv, wo, bo = (t.to(dev) for t in (x, g, wqkv, bqkv, wo, bo))
+    y = torch.empty_like(x)
+    nws = int(wanvae.load().wanvae_frame_attention_workspace_size(wanvae._dims(x.shape), C))
+    wsb = torch.empty(nws, dtype=torch.uint8, device=dev)
+
+    def call(xin):
+        wanvae.frame_attention(xin, g, wqkv, bqkv, wo, bo, y=y, workspace=wsb)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call(x)
+    torch.cuda.synchronize(dev)
+    K = default_steps(args, time_one(stream, lambda: call(x)))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    n0 = wanvae.launch_count()
+    with ClockSampler(local) as clk:
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            call(x)
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+    launches = wanvae.launch_count() - n0
+    wanvae.sync_status()
+    ms = sum(a.elapsed_time(z) for a, z in evs) / K
+    value = M / (ms / 1e3)
+    x_host = x_cpu.pin_memory()
+    y_host = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    E = max(1, min(args.e2e_steps, K))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        x_dev.copy_(x_host, non_blocking=True)
+        call(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_value = M * E / (e0.elapsed_time(e1) / 1e3)
+    peaks = load_peaks()
+    flop_core = 4.0 * F * N * N * C                # Q K^T and P V
+    flop_proj = 2.0 * 4 * M * C * C                # q, k, v and output projections
+    tflops = (flop_core + flop_proj) / (ms / 1e3) / 1e12
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": "voxels/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(name, B, T, H, W, C, C, 1),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                     "flop_per_launch": flop_core + flop_proj, "kernel": "whole block",
+                     "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst"},
+        "e2e": {"value": e2e_value, "unit": "voxels/s", "h2d_bytes_per_step": x.numel() * 2,
+                "d2h_bytes_per_step": y.numel() * 2, "steps": E},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        xs = x_cpu[:1, :1]
+        t0 = time.perf_counter()
+        oracle.frame_attention(xs, g.cpu(), wqkv.cpu(), bqkv.cpu(), wo.cpu(), bo.cpu())
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": N / dt, "unit": "voxels/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"one {H}x{W} frame: {N} voxels in {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+
+
 
 
 def bench_conv(args):
@@ -703,6 +838,8 @@ def main():
     elif args.workload in ("conv_in_latent", "post_quant_latent", "conv_out_fullres",
                            "upsample2d_fullres", "time_upsample_latent"):
         bench_conv(args)
+    elif args.workload == "mid_attention_latent":
+        bench_attention(args)
     else:
         bench_ours(args)
 

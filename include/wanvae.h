@@ -195,6 +195,25 @@ wanvae_status wanvae_upsample3d(const void *x, const void *w_t, const float *b_t
                                 const float *b_s, void *y, wanvae_dims d, int64_t c_in,
                                 int64_t c_mid, int64_t c_out, void *workspace, size_t ws_bytes,
                                 wanvae_stream stream);
+/* The decoder's mid-block attention ("Closing the gap: Wan 2.2 14B VAE
+ * decoder", section 5: a spatial self-attention within each frame; the
+ * sequence is the H x W grid and each (batch, frame) is an independent
+ * problem).  The pages give no more; the plainest reading is computed:
+ *   y = x + Wo (softmax(q k^T / sqrt(C)) v) + bo,  [q; k; v] = Wqkv n + bqkv,
+ *   n = RMS_norm(x) (as in the ResidualBlock, no SiLU), one head of width C.
+ *   x, y  : bf16 [B][T][H][W][C] (y may not alias x)
+ *   gamma : fp32 [C];  wqkv : bf16 [3C][C] (rows q, k, v);  bqkv : fp32 [3C]
+ *           or NULL;  wo : bf16 [C][C];  bo : fp32 [C] or NULL;  eps > 0
+ *   workspace : device buffer of wanvae_frame_attention_workspace_size(d, C)
+ *           bytes, 256-byte aligned (the normed input, q, k, v, V transposed
+ *           and the attention output).
+ *   C : 128, 256 or 384.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+size_t wanvae_frame_attention_workspace_size(wanvae_dims d, int64_t c);
+wanvae_status wanvae_frame_attention(const void *x, const float *gamma, const void *wqkv,
+                                     const float *bqkv, const void *wo, const float *bo, void *y,
+                                     wanvae_dims d, int64_t c, float eps, void *workspace,
+                                     size_t ws_bytes, wanvae_stream stream);
 
 /* Bytes of device workspace wanvae_resblock_forward needs for these sizes
  * (the bf16 conv inputs a1 and a2, 256-byte aligned).  0 on invalid sizes. */

@@ -119,6 +119,17 @@ def test_time_upsample_argument_errors(lib):
     assert f(A, A, None, Y, d, 40, 16, WS, n, None) == wanvae.ERR_UNSUPPORTED
     assert f(A, A, None, Y, d, 32, 16, WS, n - 2, None) == wanvae.ERR_WORKSPACE
     assert f(A, A + 4, None, Y, d, 32, 16, WS, n, None) == wanvae.ERR_MISALIGNED
+def test_frame_attention_argument_errors(lib):
+    f = lib.wanvae_frame_attention
+    d = _dims(1, 2, 4, 4)
+    Y, WS = 0x900000, 0x2000000
+    n = lib.wanvae_frame_attention_workspace_size(d, 128)
+    assert n > 0
+    assert f(None, A, A, None, A, None, Y, d, 128, 1e-12, WS, n, None) == wanvae.ERR_INVALID_ARG
+    assert f(A, A, A, None, A, None, Y, d, 128, 0.0, WS, n, None) == wanvae.ERR_INVALID_ARG
+    assert f(A, A, A, None, A, None, Y, d, 192, 1e-12, WS, 1 << 30, None) == wanvae.ERR_UNSUPPORTED
+    assert f(A, A, A, None, A, None, Y, d, 128, 1e-12, WS, n - 2, None) == wanvae.ERR_WORKSPACE
+    assert f(A, A + 4, A, None, A, None, Y, d, 128, 1e-12, WS, n, None) == wanvae.ERR_MISALIGNED
 
 
 def test_resblock_argument_errors(lib):

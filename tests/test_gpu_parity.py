@@ -246,6 +246,33 @@ def test_upsample3d(cuda_lib):
     y = cuda_lib.upsample3d(x.to(DEV), w_t.to(DEV), b_t.to(DEV), w_s.to(DEV), b_s.to(DEV))
     cuda_lib.sync_status()
     compare(to_f64(y), oracle.upsample3d(x, w_t, b_t, w_s, b_s), what="upsample3d")
+# ------------------------------------------------------- mid-block attention
+ATTN_CASES = [
+    # (B, T, H, W, C): N = H*W positions per frame
+    (1, 2, 4, 8, 128),          # one partial key block, one query tile
+    (2, 1, 12, 16, 256),        # two clips, N = 192: a ragged second block
+    (1, 2, 10, 13, 384),        # N = 130: two query tiles, the second of 2 rows
+    (1, 1, 20, 30, 384),        # N = 600: five key blocks
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES)
+def test_frame_attention(cuda_lib, case):
+    B, T, H, W, C = case
+    s = sum(case)
+    x = synth.make_tensor((B, T, H, W, C), seed=300 + s)
+    g = synth.make_tensor((C,), seed=301, dtype=torch.float32, kind="uniform", lo=0.5, hi=1.5)
+    bw = 1.0 / np.sqrt(C)
+    wqkv = synth.make_tensor((3 * C, C), seed=302 + s, kind="uniform", lo=-bw, hi=bw)
+    bqkv = synth.make_tensor((3 * C,), seed=303, dtype=torch.float32, kind="uniform",
+                             lo=-.1, hi=.1)
+    wo = synth.make_tensor((C, C), seed=304 + s, kind="uniform", lo=-bw, hi=bw)
+    bo = synth.make_tensor((C,), seed=305, dtype=torch.float32, kind="uniform", lo=-.1, hi=.1)
+    y = cuda_lib.frame_attention(x.to(DEV), g.to(DEV), wqkv.to(DEV), bqkv.to(DEV), wo.to(DEV),
+                                 bo.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.frame_attention(x, g, wqkv, bqkv, wo, bo),
+            what=f"attention {case}")
 
 
 # ------------------------------------------------------------------ block

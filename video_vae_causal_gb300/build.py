@@ -15,7 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libwanvae.so")
-SOURCES = ["api.cu", "rmsnorm_silu.cu", "conv3d_tcgen05.cu", "conv3d_narrow.cu"]
+SOURCES = ["api.cu", "rmsnorm_silu.cu", "conv3d_tcgen05.cu", "conv3d_narrow.cu",
+           "attn_tcgen05.cu"]
 DEPS = SOURCES + ["ptx.cuh", "kernels.h", "exports.map"]
 HEADER = os.path.join(ROOT, "include", "wanvae.h")
 

@@ -2,6 +2,7 @@
 // per-device error word, and the composition of the ResidualBlock
 // ("Sharding of WAN 2.2 VAE", ResidualBlock listing: norm1, SiLU, conv A,
 // norm2, SiLU, conv B, shortcut, residual add) out of the kernels.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -270,6 +271,65 @@ wanvae_status wanvae_time_upsample_conv(const void *x, const void *w, const floa
     s.epi = kEpiBias;
     s.up_t = 1;
     if (conv3d_supported(s)) return WANVAE_ERR_UNSUPPORTED;
+// Workspace of the attention block: the normed input, q, k, v and the
+// attention output ([M][C] bf16 each) and V transposed ([B*T][C][ldn]).
+size_t wanvae_frame_attention_workspace_size(wanvae_dims d, int64_t c) {
+    if (!dims_ok(d) || c < 1 || c > 4096) return 0;
+    const size_t M = (size_t)voxels(d), F = (size_t)(d.B * d.T);
+    const size_t ldn = (size_t)frame_attention_ldn((int)(d.H * d.W));
+    return 5 * align256(M * c * 2) + align256(F * c * ldn * 2);
+}
+
+wanvae_status wanvae_frame_attention(const void *x, const float *gamma, const void *wqkv,
+                                     const float *bqkv, const void *wo, const float *bo, void *y,
+                                     wanvae_dims d, int64_t c, float eps, void *workspace,
+                                     size_t ws_bytes, wanvae_stream stream) {
+    if (!x || !gamma || !wqkv || !wo || !y || !workspace) return WANVAE_ERR_INVALID_ARG;
+    if (!dims_ok(d) || c < 1 || !(eps > 0.f)) return WANVAE_ERR_INVALID_ARG;
+    if (c != 128 && c != 256 && c != 384) return WANVAE_ERR_UNSUPPORTED;
+    if (d.H * d.W > (1 << 24)) return WANVAE_ERR_UNSUPPORTED;
+    if (misaligned(x) || misaligned(gamma) || misaligned(wqkv) || misaligned(bqkv) ||
+        misaligned(wo) || misaligned(bo) || misaligned(y) || misaligned(workspace))
+        return WANVAE_ERR_MISALIGNED;
+    const size_t need = wanvae_frame_attention_workspace_size(d, c);
+    if (ws_bytes < need) return WANVAE_ERR_WORKSPACE;
+    const int64_t M = voxels(d);
+    const size_t xb = (size_t)M * c * 2;
+    if (overlap(x, xb, y, xb) || overlap(workspace, need, x, xb) ||
+        overlap(workspace, need, y, xb))
+        return WANVAE_ERR_INVALID_ARG;
+    const int F = (int)(d.B * d.T), N = (int)(d.H * d.W), C = (int)c;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t slab = align256((size_t)M * c * 2);
+    void *nx = ws, *q = ws + slab, *k = ws + 2 * slab, *v = ws + 3 * slab, *o = ws + 4 * slab;
+    void *vt = ws + 5 * slab;
+
+    // the four 1x1 projections on the conv kernel: q, k, v of the normed
+    // input (bias), and the output projection of o with the input added
+    auto spec = [&](const void *in, const void *w, const float *b, void *out, const void *res) {
+        ConvSpec s;
+        memset(&s, 0, sizeof(s));
+        s.in = in;
+        s.w = w;
+        s.bias = b;
+        s.out = out;
+        s.resid = res;
+        s.B = (int)d.B;
+        s.T = (int)d.T;
+        s.H = (int)d.H;
+        s.W = (int)d.W;
+        s.c_in = C;
+        s.c_out = C;
+        s.k = 1;
+        s.epi = res ? kEpiResidual : kEpiBias;
+        return s;
+    };
+    const __nv_bfloat16 *wq = static_cast<const __nv_bfloat16 *>(wqkv);
+    const ConvSpec sq = spec(nx, wq, bqkv, q, nullptr);
+    const ConvSpec sk = spec(nx, wq + (size_t)C * C, bqkv ? bqkv + C : nullptr, k, nullptr);
+    const ConvSpec sv = spec(nx, wq + (size_t)2 * C * C, bqkv ? bqkv + 2 * C : nullptr, v, nullptr);
+    const ConvSpec so = spec(o, wo, bo, y, x);
+    if (conv3d_supported(sq) || conv3d_supported(so)) return WANVAE_ERR_UNSUPPORTED;
 
     LaunchCtx ctx;
     const wanvae_status st = make_ctx(ctx, stream);
@@ -313,6 +373,17 @@ wanvae_status wanvae_upsample3d(const void *x, const void *w_t, const float *b_t
     d2.T = 2 * d.T;
     return wanvae_upsample2d_conv(ws, w_s, b_s, y, d2, c_mid, c_out, ws + mid + wt,
                                   ws_bytes - mid - wt, stream);
+}
+
+    g_launches += 7;
+    cudaError_t e = launch_rmsnorm(x, nx, gamma, M, C, eps, ctx);
+    if (e == cudaSuccess) e = launch_conv3d(sq, ctx);
+    if (e == cudaSuccess) e = launch_conv3d(sk, ctx);
+    if (e == cudaSuccess) e = launch_conv3d(sv, ctx);
+    if (e == cudaSuccess) e = launch_transpose_v(v, vt, F, N, C, ctx);
+    if (e == cudaSuccess) e = launch_attention_core(q, k, vt, o, F, N, C, ctx);
+    if (e == cudaSuccess) e = launch_conv3d(so, ctx);
+    return from_cuda(e);
 }
 
 size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out) {

@@ -23,6 +23,18 @@ struct LaunchCtx {
 cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool is_f32,
                                 int64_t n, int C, float eps, const LaunchCtx &ctx);
 
+// RMS_norm alone (no activation), bf16 in and out: the attention block's norm.
+cudaError_t launch_rmsnorm(const void *x, void *y, const float *gamma, int64_t n, int C,
+                           float eps, const LaunchCtx &ctx);
+
+// The attention core (attn_tcgen05.cu): out = softmax(q k^T / sqrt(D)) v per
+// frame, q, k, out bf16 [F][N][D], vt bf16 [F][D][frame_attention_ldn(N)]
+// (V transposed by launch_transpose_v); D = 128, 256 or 384.
+int frame_attention_ldn(int N);
+cudaError_t launch_transpose_v(const void *v, void *vt, int F, int N, int D, const LaunchCtx &ctx);
+cudaError_t launch_attention_core(const void *q, const void *k, const void *vt, void *out, int F,
+                                  int N, int D, const LaunchCtx &ctx);
+
 // cache[b] <- last two frames of concat(cache[b], src[b]) along T, for bf16
 // tensors of frame_bytes bytes per frame (a multiple of 16).
 cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,

@@ -26,6 +26,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // -87 the denominator overflows and the result is the limit 0).
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// The pass's activation: SiLU, or none (the attention block's norm).
+template <bool kSilu>
+__device__ __forceinline__ float act(float z) {
+    return kSilu ? silu(z) : z;
+}
+
 // One group of L lanes owns one voxel; each lane holds VPT 16-byte vectors
 // of it (vector j of the voxel lives in lane j % L, slot j / L), so every
 // warp-wide load covers 32 consecutive 16-byte vectors of (32 / L) voxels.
@@ -33,7 +39,7 @@ __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __e
 // loads before the first reduction, so U * VPT loads per lane are in flight
 // (the pass is bound by DRAM latency x bytes in flight).  The channel sum of
 // squares is reduced with xor-shuffles inside the group.
-template <bool F32, int VPT, int U>
+template <bool F32, int VPT, int U, bool kSilu>
 __global__ void __launch_bounds__(256)
 rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                     const float *__restrict__ gamma, int64_t n, int C, int L, float eps,
@@ -95,20 +101,20 @@ rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                 uint4 o;
                 if (F32) {
                     const float4 g = __ldg(g4);
-                    o.x = __float_as_uint(silu(__uint_as_float(b.x) * scale * g.x));
-                    o.y = __float_as_uint(silu(__uint_as_float(b.y) * scale * g.y));
-                    o.z = __float_as_uint(silu(__uint_as_float(b.z) * scale * g.z));
-                    o.w = __float_as_uint(silu(__uint_as_float(b.w) * scale * g.w));
+                    o.x = __float_as_uint(act<kSilu>(__uint_as_float(b.x) * scale * g.x));
+                    o.y = __float_as_uint(act<kSilu>(__uint_as_float(b.y) * scale * g.y));
+                    o.z = __float_as_uint(act<kSilu>(__uint_as_float(b.z) * scale * g.z));
+                    o.w = __float_as_uint(act<kSilu>(__uint_as_float(b.w) * scale * g.w));
                 } else {
                     const float4 ga = __ldg(g4), gb = __ldg(g4 + 1);
-                    o.x = pack_bf16x2(silu(bf16lo(b.x) * scale * ga.x),
-                                      silu(bf16hi(b.x) * scale * ga.y));
-                    o.y = pack_bf16x2(silu(bf16lo(b.y) * scale * ga.z),
-                                      silu(bf16hi(b.y) * scale * ga.w));
-                    o.z = pack_bf16x2(silu(bf16lo(b.z) * scale * gb.x),
-                                      silu(bf16hi(b.z) * scale * gb.y));
-                    o.w = pack_bf16x2(silu(bf16lo(b.w) * scale * gb.z),
-                                      silu(bf16hi(b.w) * scale * gb.w));
+                    o.x = pack_bf16x2(act<kSilu>(bf16lo(b.x) * scale * ga.x),
+                                      act<kSilu>(bf16hi(b.x) * scale * ga.y));
+                    o.y = pack_bf16x2(act<kSilu>(bf16lo(b.y) * scale * ga.z),
+                                      act<kSilu>(bf16hi(b.y) * scale * ga.w));
+                    o.z = pack_bf16x2(act<kSilu>(bf16lo(b.z) * scale * gb.x),
+                                      act<kSilu>(bf16hi(b.z) * scale * gb.y));
+                    o.w = pack_bf16x2(act<kSilu>(bf16lo(b.w) * scale * gb.z),
+                                      act<kSilu>(bf16hi(b.w) * scale * gb.w));
                 }
                 y[v * V + j] = o;
             }
@@ -116,7 +122,7 @@ rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
     }
 }
 
-template <bool F32>
+template <bool F32, bool kSilu = true>
 cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n, int C, float eps,
                           const LaunchCtx &ctx) {
     constexpr int E = F32 ? 4 : 8;
@@ -134,7 +140,7 @@ cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n,
     // instantiation's registers allow, looked up once per instantiation.
 #define WANVAE_NORM_CASE(K)                                                              \
     case K: {                                                                            \
-        auto *kern = rmsnorm_silu_kernel<F32, K, (K <= 4 ? 2 : 1)>;                      \
+        auto *kern = rmsnorm_silu_kernel<F32, K, (K <= 4 ? 2 : 1), kSilu>;               \
         static int per_sm = 0;                                                           \
         if (per_sm == 0 &&                                                               \
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) !=  \
@@ -271,6 +277,11 @@ cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
     expand_up2d_weights_kernel<<<(unsigned)blocks, 256, 0, ctx.stream>>>(
         static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2), Co, Ci);
     return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void *x, void *y, const float *gamma, int64_t n, int C,
+                           float eps, const LaunchCtx &ctx) {
+    return dispatch_norm<false, false>(x, y, gamma, n, C, eps, ctx);
 }
 
 cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool is_f32,

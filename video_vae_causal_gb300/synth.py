@@ -107,6 +107,28 @@ def make_time_upsample_inputs(dims, c_in, c_out, seed=0, device="cpu"):
     w = _uniform(g, (c_out, 3, c_in), -bound, bound, device).to(torch.bfloat16)
     b = _uniform(g, (c_out,), -0.1, 0.1, device)
     return x, w, b
+# The mid-block attention at the latent size: (name, (B, T, H, W), C).
+ATTENTION_WORKLOADS = {
+    "mid_attention_latent": ((1, 21, 60, 104), 384),
+}
+
+
+def make_attention_inputs(dims, C, seed=0, device="cpu"):
+    """x [B,T,H,W,C] bf16 ~ N(0,1), gamma fp32 ~ U(0.5,1.5), wqkv [3C,C] and
+    wo [C,C] bf16 ~ U(+-1/sqrt(C)), biases fp32 ~ U(-0.1,0.1), drawn in the
+    order x, gamma, wqkv, bqkv, wo, bo from one seeded generator."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, T, H, W = dims
+    x = torch.randn((B, T, H, W, C), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    gamma = _uniform(g, (C,), 0.5, 1.5, device)
+    bound = 1.0 / math.sqrt(C)
+    wqkv = _uniform(g, (3 * C, C), -bound, bound, device).to(torch.bfloat16)
+    bqkv = _uniform(g, (3 * C,), -0.1, 0.1, device)
+    wo = _uniform(g, (C, C), -bound, bound, device).to(torch.bfloat16)
+    bo = _uniform(g, (C,), -0.1, 0.1, device)
+    return x, gamma, wqkv, bqkv, wo, bo
 
 
 def make_upsample_inputs(dims, c_in, c_out, seed=0, device="cpu"):

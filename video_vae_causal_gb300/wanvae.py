@@ -25,6 +25,7 @@ EXPORTS = (
     "wanvae_launch_count", "wanvae_resblock_forward_static", "wanvae_upsample2d_workspace_size",
     "wanvae_upsample2d_conv", "wanvae_set_kernel_variant", "wanvae_time_upsample_workspace_size",
     "wanvae_time_upsample_conv", "wanvae_upsample3d_workspace_size", "wanvae_upsample3d",
+    "wanvae_frame_attention_workspace_size", "wanvae_frame_attention",
 )
 
 # Size of the library's own workspace used by resblock_forward_static.
@@ -110,6 +111,11 @@ def load(path=LIB_PATH):
     L.wanvae_upsample3d.argtypes = [vp, vp, vp, vp, vp, vp, Dims, i64, i64, i64, vp,
                                     ctypes.c_size_t, vp]
     L.wanvae_upsample3d.restype = st
+    L.wanvae_frame_attention_workspace_size.argtypes = [Dims, i64]
+    L.wanvae_frame_attention_workspace_size.restype = ctypes.c_size_t
+    L.wanvae_frame_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, Dims, i64, ctypes.c_float, vp,
+                                         ctypes.c_size_t, vp]
+    L.wanvae_frame_attention.restype = st
     _lib = L
     return L
 
@@ -233,6 +239,22 @@ def upsample3d(x, w_t, b_t, w_s, b_s, y=None, workspace=None, stream=None):
                              _dims(x.shape), c_in, c_mid, c_out, _ptr(workspace),
                              workspace.numel(), _stream(stream))
     _check(st, "wanvae_upsample3d")
+def frame_attention(x, gamma, wqkv, bqkv=None, wo=None, bo=None, y=None, workspace=None,
+                    eps=1e-12, stream=None):
+    """The mid-block attention: y = x + Wo softmax(q k^T / sqrt(C)) v + bo per
+    frame, [q; k; v] = Wqkv RMS_norm(x) + bqkv.  x [B,T,H,W,C] bf16, gamma fp32
+    [C], wqkv bf16 [3C,C], bqkv fp32 [3C], wo bf16 [C,C], bo fp32 [C]."""
+    B, T, H, W, C = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    L = load()
+    if workspace is None:
+        n = int(L.wanvae_frame_attention_workspace_size(_dims(x.shape), C))
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = L.wanvae_frame_attention(_ptr(x), _ptr(gamma), _ptr(wqkv), _ptr(bqkv), _ptr(wo),
+                                  _ptr(bo), _ptr(y), _dims(x.shape), C, eps, _ptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    _check(st, "wanvae_frame_attention")
     return y
 
 
