@@ -275,6 +275,53 @@ def test_frame_attention(cuda_lib, case):
             what=f"attention {case}")
 
 
+def _attn_inputs(B, T, H, W, C, seed):
+    x = synth.make_tensor((B, T, H, W, C), seed=seed)
+    g = synth.make_tensor((C,), seed=seed + 1, dtype=torch.float32, kind="uniform", lo=0.5,
+                          hi=1.5)
+    bw = 1.0 / np.sqrt(C)
+    wqkv = synth.make_tensor((3 * C, C), seed=seed + 2, kind="uniform", lo=-bw, hi=bw)
+    bqkv = synth.make_tensor((3 * C,), seed=seed + 3, dtype=torch.float32, kind="uniform",
+                             lo=-.1, hi=.1)
+    wo = synth.make_tensor((C, C), seed=seed + 4, kind="uniform", lo=-bw, hi=bw)
+    bo = synth.make_tensor((C,), seed=seed + 5, dtype=torch.float32, kind="uniform", lo=-.1,
+                           hi=.1)
+    return x, g, wqkv, bqkv, wo, bo
+
+
+def test_frame_attention_uniform_when_q_k_vanish(cuda_lib):
+    """Zero q and k projections: every score is 0, so each query's output is
+    the mean of v over its frame (closed form: x + bo + Wo mean(v)), across
+    several key blocks and a ragged last one."""
+    x, g, wqkv, bqkv, wo, bo = _attn_inputs(1, 2, 12, 25, 128, seed=310)
+    C = 128
+    wqkv[:2 * C] = 0
+    bqkv[:2 * C] = 0
+    y = cuda_lib.frame_attention(x.to(DEV), g.to(DEV), wqkv.to(DEV), bqkv.to(DEV), wo.to(DEV),
+                                 bo.to(DEV))
+    cuda_lib.sync_status()
+    ref = oracle.frame_attention(x, g, wqkv, bqkv, wo, bo)
+    compare(to_f64(y), ref, what="attention uniform")
+    # the closed form itself, per frame
+    xf = to_f64(x).reshape(2, -1, C)
+    n = xf / np.maximum(np.linalg.norm(xf, axis=2, keepdims=True), 1e-12) * np.sqrt(C) * \
+        to_f64(g)
+    v = n @ to_f64(wqkv[2 * C:]).T + to_f64(bqkv[2 * C:])
+    closed = xf + to_f64(bo) + v.mean(axis=1, keepdims=True) @ to_f64(wo).T
+    compare(to_f64(y).reshape(2, -1, C), closed, what="attention uniform closed form")
+
+
+def test_frame_attention_single_position(cuda_lib):
+    """One position per frame: its only key gets all the weight, so
+    y = x + bo + Wo v (a 1 x 1 frame: one ragged query tile and key block)."""
+    x, g, wqkv, bqkv, wo, bo = _attn_inputs(2, 3, 1, 1, 256, seed=320)
+    y = cuda_lib.frame_attention(x.to(DEV), g.to(DEV), wqkv.to(DEV), bqkv.to(DEV), wo.to(DEV),
+                                 bo.to(DEV))
+    cuda_lib.sync_status()
+    compare(to_f64(y), oracle.frame_attention(x, g, wqkv, bqkv, wo, bo),
+            what="attention one position")
+
+
 # ------------------------------------------------------------------ block
 BLOCK_CASES = [
     # (B, T, H, W, c_in, c_out)

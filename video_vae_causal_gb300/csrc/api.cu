@@ -271,6 +271,51 @@ wanvae_status wanvae_time_upsample_conv(const void *x, const void *w, const floa
     s.epi = kEpiBias;
     s.up_t = 1;
     if (conv3d_supported(s)) return WANVAE_ERR_UNSUPPORTED;
+
+    LaunchCtx ctx;
+    const wanvae_status st = make_ctx(ctx, stream);
+    if (st != WANVAE_OK) return st;
+    g_launches++;
+    cudaError_t e = launch_expand_time_up_weights(w, workspace, (int)c_out, (int)c_in, ctx);
+    if (e == cudaSuccess) {
+        g_launches++;
+        e = launch_conv3d(s, ctx);
+    }
+    return from_cuda(e);
+}
+
+// upsample3d: the temporal half into a [B][2T][H][W][c_mid] slab of the
+// workspace, then the spatial upsampler; the two weight sets after it.
+size_t wanvae_upsample3d_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_mid,
+                                        int64_t c_out) {
+    if (!dims_ok(d) || c_in < 1 || c_mid < 1 || c_out < 1 || c_in > 4096 || c_mid > 4096 ||
+        c_out > 4096)
+        return 0;
+    return align256((size_t)voxels(d) * 2 * c_mid * 2) +
+           wanvae_time_upsample_workspace_size(c_in, c_mid) +
+           wanvae_upsample2d_workspace_size(c_mid, c_out);
+}
+
+wanvae_status wanvae_upsample3d(const void *x, const void *w_t, const float *b_t, const void *w_s,
+                                const float *b_s, void *y, wanvae_dims d, int64_t c_in,
+                                int64_t c_mid, int64_t c_out, void *workspace, size_t ws_bytes,
+                                wanvae_stream stream) {
+    if (!workspace) return WANVAE_ERR_INVALID_ARG;
+    const size_t need = wanvae_upsample3d_workspace_size(d, c_in, c_mid, c_out);
+    if (need == 0) return WANVAE_ERR_INVALID_ARG;
+    if (ws_bytes < need) return WANVAE_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t mid = align256((size_t)voxels(d) * 2 * c_mid * 2);
+    const size_t wt = wanvae_time_upsample_workspace_size(c_in, c_mid);
+    wanvae_status st = wanvae_time_upsample_conv(x, w_t, b_t, ws, d, c_in, c_mid, ws + mid, wt,
+                                                 stream);
+    if (st != WANVAE_OK) return st;
+    wanvae_dims d2 = d;
+    d2.T = 2 * d.T;
+    return wanvae_upsample2d_conv(ws, w_s, b_s, y, d2, c_mid, c_out, ws + mid + wt,
+                                  ws_bytes - mid - wt, stream);
+}
+
 // Workspace of the attention block: the normed input, q, k, v and the
 // attention output ([M][C] bf16 each) and V transposed ([B*T][C][ldn]).
 size_t wanvae_frame_attention_workspace_size(wanvae_dims d, int64_t c) {
@@ -334,47 +379,6 @@ wanvae_status wanvae_frame_attention(const void *x, const float *gamma, const vo
     LaunchCtx ctx;
     const wanvae_status st = make_ctx(ctx, stream);
     if (st != WANVAE_OK) return st;
-    g_launches++;
-    cudaError_t e = launch_expand_time_up_weights(w, workspace, (int)c_out, (int)c_in, ctx);
-    if (e == cudaSuccess) {
-        g_launches++;
-        e = launch_conv3d(s, ctx);
-    }
-    return from_cuda(e);
-}
-
-// upsample3d: the temporal half into a [B][2T][H][W][c_mid] slab of the
-// workspace, then the spatial upsampler; the two weight sets after it.
-size_t wanvae_upsample3d_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_mid,
-                                        int64_t c_out) {
-    if (!dims_ok(d) || c_in < 1 || c_mid < 1 || c_out < 1 || c_in > 4096 || c_mid > 4096 ||
-        c_out > 4096)
-        return 0;
-    return align256((size_t)voxels(d) * 2 * c_mid * 2) +
-           wanvae_time_upsample_workspace_size(c_in, c_mid) +
-           wanvae_upsample2d_workspace_size(c_mid, c_out);
-}
-
-wanvae_status wanvae_upsample3d(const void *x, const void *w_t, const float *b_t, const void *w_s,
-                                const float *b_s, void *y, wanvae_dims d, int64_t c_in,
-                                int64_t c_mid, int64_t c_out, void *workspace, size_t ws_bytes,
-                                wanvae_stream stream) {
-    if (!workspace) return WANVAE_ERR_INVALID_ARG;
-    const size_t need = wanvae_upsample3d_workspace_size(d, c_in, c_mid, c_out);
-    if (need == 0) return WANVAE_ERR_INVALID_ARG;
-    if (ws_bytes < need) return WANVAE_ERR_WORKSPACE;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const size_t mid = align256((size_t)voxels(d) * 2 * c_mid * 2);
-    const size_t wt = wanvae_time_upsample_workspace_size(c_in, c_mid);
-    wanvae_status st = wanvae_time_upsample_conv(x, w_t, b_t, ws, d, c_in, c_mid, ws + mid, wt,
-                                                 stream);
-    if (st != WANVAE_OK) return st;
-    wanvae_dims d2 = d;
-    d2.T = 2 * d.T;
-    return wanvae_upsample2d_conv(ws, w_s, b_s, y, d2, c_mid, c_out, ws + mid + wt,
-                                  ws_bytes - mid - wt, stream);
-}
-
     g_launches += 7;
     cudaError_t e = launch_rmsnorm(x, nx, gamma, M, C, eps, ctx);
     if (e == cudaSuccess) e = launch_conv3d(sq, ctx);

@@ -29,6 +29,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -158,7 +160,7 @@ __device__ void attn_producer(const CUtensorMap *mQ, const CUtensorMap *mK,
     if (!ok) {
         // Aborted: let every copy in flight land before shared memory goes away.
         volatile int no_abort = 0;
-        const WaitCtl dc{kADrainNs, wc.err, &no_abort};
+        const WaitCtl dc{kADrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
         const uint32_t n = fills < (uint32_t)kAStages ? fills : (uint32_t)kAStages;
         for (uint32_t f = fills - n; f < fills; ++f)
             mbar_wait<false>(bars.full((int)(f % kAStages)), (f / kAStages) & 1u, dc);
@@ -247,7 +249,7 @@ __device__ void attn_mma(const AttnArgs &p, uint32_t sbase, uint32_t tmem, const
     }
     // Every MMA issued above completes before TMEM is released.
     volatile int no_abort = 0;
-    const WaitCtl dc{kADrainNs, wc.err, &no_abort};
+    const WaitCtl dc{kADrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
     mma_commit(bars.drain());
     mbar_wait<false>(bars.drain(), 0u, dc);
 }
@@ -399,7 +401,7 @@ attn_tcgen05_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtl wc{p.wait_ns, p.err, abort_flag};
+    const WaitCtl wc{p.wait_ns, p.err, abort_flag, 0u};
     const int items = p.F * p.q_tiles;
     if (warp == 0) {
         if (lane == 0)
@@ -484,13 +486,19 @@ cudaError_t launch_attention_core(const void *q, const void *k, const void *vt, 
     a.err = ctx.err;
     a.wait_ns = ctx.wait_ns;
     const size_t smem = 1024 + a.off_bars + 8 * kANumBars + 16;
-    static bool attr_set = false;  // (one opt-in per process: every launch asks for <= 227 KB)
-    if (!attr_set) {
+    // The shared-memory opt-in, once per device (every launch asks for <= 227 KB).
+    constexpr int kMaxDev = 64;
+    static std::atomic<bool> attr_set[kMaxDev];
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(attn_tcgen05_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     const int items = F * a.q_tiles;
