@@ -16,8 +16,10 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libwanvae.so")
 SOURCES = ["api.cu", "rmsnorm_silu.cu", "conv3d_tcgen05.cu", "conv3d_narrow.cu",
-           "attn_tcgen05.cu"]
-DEPS = SOURCES + ["ptx.cuh", "kernels.h", "exports.map"]
+           "attn_tcgen05.cu", "conv3d_kernels_p1_n1.cu", "conv3d_kernels_p1_n2.cu",
+           "conv3d_kernels_p2_n1.cu", "conv3d_kernels_p2_n2.cu", "conv3d_kernels_misc.cu"]
+DEPS = SOURCES + ["ptx.cuh", "kernels.h", "exports.map", "conv3d_tcgen05.cuh",
+                  "conv3d_kernels.inc"]
 HEADER = os.path.join(ROOT, "include", "wanvae.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -58,7 +60,8 @@ def build(force=False, verbose=False, extra_flags=()):
                 print(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
+    # largest translation units first, all of them in parallel
+    with cf.ThreadPoolExecutor(min(len(SOURCES), max(2, os.cpu_count() or 2))) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs,

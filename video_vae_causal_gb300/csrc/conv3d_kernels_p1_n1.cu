@@ -1,0 +1,4 @@
+// Instantiations of the conv kernel for CTA grouping 1 and 1 N piece(s).
+#define WANVAE_PAIR 1
+#define WANVAE_NP 1
+#include "conv3d_kernels.inc"

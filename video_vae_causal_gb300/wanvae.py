@@ -239,6 +239,9 @@ def upsample3d(x, w_t, b_t, w_s, b_s, y=None, workspace=None, stream=None):
                              _dims(x.shape), c_in, c_mid, c_out, _ptr(workspace),
                              workspace.numel(), _stream(stream))
     _check(st, "wanvae_upsample3d")
+    return y
+
+
 def frame_attention(x, gamma, wqkv, bqkv=None, wo=None, bo=None, y=None, workspace=None,
                     eps=1e-12, stream=None):
     """The mid-block attention: y = x + Wo softmax(q k^T / sqrt(C)) v + bo per
