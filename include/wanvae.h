@@ -246,6 +246,37 @@ wanvae_status wanvae_resblock_forward_profiled(const wanvae_resblock_params *p,
                                                void *workspace, size_t ws_bytes,
                                                void *const *events, wanvae_stream stream);
 
+/* Bytes of device workspace wanvae_resblock_forward_host needs: two chunks of
+ * x and of y (chunk_T frames each), the two feat_caches, and the block
+ * workspace of one chunk.  0 on invalid sizes. */
+size_t wanvae_resblock_forward_host_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out,
+                                                   int64_t chunk_T);
+
+/* The whole-clip ResidualBlock forward for a clip held in HOST memory.  The
+ * clip runs as consecutive chunks of chunk_T frames carried by the
+ * feat_cache ("Sharding of WAN 2.2 VAE", "Why depth sharding is not
+ * beneficial": frame-wise decode with a cache of the previous frames), which
+ * gives exactly the full-T result, and the chunks are pipelined over three
+ * streams: chunk i+1 is copied in on `copy_in` while chunk i computes on
+ * `compute` and chunk i-1 is copied out on `copy_out`.
+ *   x_host : bf16 [B][T][H][W][c_in], y_host : bf16 [B][T][H][W][c_out], host
+ *            memory (page-locked for the copies to overlap; pageable memory
+ *            gives the same result without the overlap).
+ *   chunk_T : frames per chunk, 1 <= chunk_T (the last chunk may be shorter).
+ *   workspace : device buffer of wanvae_resblock_forward_host_workspace_size()
+ *            bytes, 256-byte aligned; contents on entry are ignored.
+ *   compute, copy_in, copy_out : CUDA streams (may coincide: then nothing
+ *            overlaps).  The call returns once everything is enqueued; y_host
+ *            is complete when copy_out has drained (synchronise it).  Work
+ *            enqueued on copy_in / copy_out before this call is not waited for.
+ * Kernels and numerics: those of wanvae_resblock_forward on each chunk.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+wanvae_status wanvae_resblock_forward_host(const wanvae_resblock_params *p, const void *x_host,
+                                           void *y_host, wanvae_dims d, int64_t chunk_T,
+                                           void *workspace, size_t ws_bytes,
+                                           wanvae_stream compute, wanvae_stream copy_in,
+                                           wanvae_stream copy_out);
+
 /* Size of the library's own device workspace used by
  * wanvae_resblock_forward_static: 32 MiB, enough for one frame-by-frame call
  * (T = 1) of a 384-channel block on a 90 x 160 latent frame. */

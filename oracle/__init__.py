@@ -115,7 +115,12 @@ def upsample2d_conv(x, w, bias):
 def time_upsample_conv(x, w, bias):
     """Temporal half of upsample3d: every frame repeated twice in T, then a
     causal 3x1x1 conv (two zero frames before the first) with bias.
-    x [B,T,H,W,Ci], w [Co,3,Ci] (tap 2 = current frame) -> [B,2T,H,W,Co]."""
+    x [B,T,H,W,Ci], w [Co,3,Ci] (tap 2 = current frame) -> [B,2T,H,W,Co].
+
+    An unconfirmed reading: the pages name the upsample3d block and 3x1x1
+    conv kernels and nothing more.  A design whose 3x1x1 conv maps C to 2C
+    channels and interleaves the two halves as two output frames is another
+    reading the pages do not rule out; it is not what this function computes."""
     x, w, bias = _f64(x), _f64(w), _f64(bias)
     B, T, H, W, Ci = x.shape
     Co = w.shape[0]

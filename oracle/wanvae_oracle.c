@@ -392,7 +392,9 @@ API int oracle_upsample2d_conv(const double *in, const double *w, const double *
  * gap", conv3d blocking).  The pages give no more, so the plain reading of
  * "upsample + conv": every frame is repeated twice in T (nearest neighbour),
  * then a causal conv with a 3x1x1 kernel -- two zero frames before the first,
- * like every CausalConv3d of the decoder -- and a bias, C_in -> C_out.
+ * like every CausalConv3d of the decoder -- and a bias, C_in -> C_out.  This
+ * reading is unconfirmed: a 3x1x1 conv to twice the channels whose halves
+ * become two output frames would also fit the pages' few words.
  *   in [B][T][H][W][Ci], w [Co][3][Ci] (tap 2 reads the current upsampled
  *   frame, tap 0 the one two before it), bias [Co] or NULL,
  *   out [B][2T][H][W][Co]. */

@@ -400,6 +400,29 @@ def test_resblock_causal_on_gpu(cuda_lib):
     assert torch.equal(y[:, :3], y2[:, :3])
 
 
+# ------------------------------------------------------------------ host buffers, pipelined
+@pytest.mark.parametrize("case,chunk", [((1, 7, 16, 24, 64, 64), 3),     # ragged last chunk
+                                        ((2, 5, 9, 10, 64, 32), 2),      # two clips, 1x1x1 shortcut
+                                        ((1, 4, 16, 16, 96, 96), 1),     # frame by frame
+                                        ((1, 3, 10, 12, 384, 384), 8)])  # one chunk
+def test_resblock_forward_host_equals_fullT(cuda_lib, case, chunk):
+    """The clip in host memory, chunked in T over the feat_cache and pipelined
+    over three streams, gives the full-T result bit for bit."""
+    B, T, H, W, ci, co = case
+    x, p = block_inputs(case, seed=17)
+    pd = dev(p)
+    full = cuda_lib.resblock_forward(x.to(DEV), pd)
+    x_host = x.pin_memory()
+    y_host = torch.full((B, T, H, W, co), 7.0, dtype=torch.bfloat16).pin_memory()
+    n = cuda_lib.resblock_forward_host_workspace_size((B, T, H, W), ci, co, chunk)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    streams = (torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream())
+    cuda_lib.resblock_forward_host(x_host, pd, y_host, chunk, ws, streams)
+    streams[2].synchronize()
+    cuda_lib.sync_status()
+    assert torch.equal(y_host, full.cpu())
+
+
 # ------------------------------------------------------------------ closed form at x = 0
 @pytest.mark.parametrize("ci,co", [(96, 96), (384, 384), (64, 32)])
 def test_resblock_zero_input_closed_form(cuda_lib, ci, co):

@@ -396,10 +396,11 @@ size_t wanvae_resblock_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out
     return align256(M * c_in * 2) + align256(M * c_out * 2);
 }
 
+// check_only: validate every argument and return before enqueuing anything.
 static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *x, void *y,
                                    wanvae_dims d, const wanvae_resblock_cache *cache,
                                    void *workspace, size_t ws_bytes, void *const *events,
-                                   wanvae_stream stream) {
+                                   wanvae_stream stream, bool check_only = false) {
     if (!p || !x || !y) return WANVAE_ERR_INVALID_ARG;
     if (!p->gamma1 || !p->gamma2 || !p->wA || !p->wB) return WANVAE_ERR_INVALID_ARG;
     if (!dims_ok(d) || p->c_in < 1 || p->c_out < 1) return WANVAE_ERR_INVALID_ARG;
@@ -473,6 +474,7 @@ static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *
         sB.resid = x;
     }
     if (conv3d_supported(sA) || conv3d_supported(sB)) return WANVAE_ERR_UNSUPPORTED;
+    if (check_only) return WANVAE_OK;
 
     LaunchCtx ctx;
     const wanvae_status st = make_ctx(ctx, stream);
@@ -523,6 +525,119 @@ wanvae_status wanvae_resblock_forward_profiled(const wanvae_resblock_params *p, 
     if (!events || !events[0] || !events[1] || !events[2] || !events[3])
         return WANVAE_ERR_INVALID_ARG;
     return resblock_impl(p, x, y, d, cache, workspace, ws_bytes, events, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Whole-clip forward from host memory, chunked in T and pipelined over three
+// streams.  Workspace: x chunks [2], y chunks [2], cache A, cache B, then the
+// block workspace of one chunk.
+namespace {
+struct HostPlan {
+    int64_t chunk;
+    size_t xc, yc, ca, cb, blk, total;
+};
+bool host_plan(wanvae_dims d, int64_t c_in, int64_t c_out, int64_t chunk_T, HostPlan &hp) {
+    if (!dims_ok(d) || c_in < 1 || c_out < 1 || c_in > 4096 || c_out > 4096 || chunk_T < 1)
+        return false;
+    hp.chunk = chunk_T < d.T ? chunk_T : d.T;
+    const size_t fr = (size_t)d.B * hp.chunk * d.H * d.W;  // voxels of one chunk
+    hp.xc = align256(fr * c_in * 2);
+    hp.yc = align256(fr * c_out * 2);
+    hp.ca = align256((size_t)d.B * 2 * d.H * d.W * c_in * 2);
+    hp.cb = align256((size_t)d.B * 2 * d.H * d.W * c_out * 2);
+    wanvae_dims dc = d;
+    dc.T = hp.chunk;
+    hp.blk = wanvae_resblock_workspace_size(dc, c_in, c_out);
+    if (!hp.blk) return false;
+    hp.total = 2 * hp.xc + 2 * hp.yc + hp.ca + hp.cb + hp.blk;
+    return true;
+}
+}  // namespace
+
+size_t wanvae_resblock_forward_host_workspace_size(wanvae_dims d, int64_t c_in, int64_t c_out,
+                                                   int64_t chunk_T) {
+    HostPlan hp;
+    return host_plan(d, c_in, c_out, chunk_T, hp) ? hp.total : 0;
+}
+
+wanvae_status wanvae_resblock_forward_host(const wanvae_resblock_params *p, const void *x_host,
+                                           void *y_host, wanvae_dims d, int64_t chunk_T,
+                                           void *workspace, size_t ws_bytes,
+                                           wanvae_stream compute, wanvae_stream copy_in,
+                                           wanvae_stream copy_out) {
+    if (!p || !x_host || !y_host) return WANVAE_ERR_INVALID_ARG;
+    HostPlan hp;
+    if (!host_plan(d, p->c_in, p->c_out, chunk_T, hp)) return WANVAE_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < hp.total) return WANVAE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return WANVAE_ERR_MISALIGNED;
+    const int64_t M = voxels(d);
+    const size_t xbytes = (size_t)M * p->c_in * 2, ybytes = (size_t)M * p->c_out * 2;
+    if (overlap(x_host, xbytes, y_host, ybytes)) return WANVAE_ERR_INVALID_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *xb[2] = {ws, ws + hp.xc};
+    uint8_t *yb[2] = {ws + 2 * hp.xc, ws + 2 * hp.xc + hp.yc};
+    uint8_t *ca = ws + 2 * hp.xc + 2 * hp.yc;
+    uint8_t *cb = ca + hp.ca;
+    uint8_t *blk = cb + hp.cb;
+    wanvae_resblock_cache cache{ca, cb};
+    // Every argument the chunk calls will see, checked once before anything
+    // is enqueued (the last chunk only differs in T).
+    {
+        wanvae_dims dc = d;
+        dc.T = hp.chunk;
+        const wanvae_status st =
+            resblock_impl(p, xb[0], yb[0], dc, &cache, blk, hp.blk, nullptr, nullptr, true);
+        if (st != WANVAE_OK) return st;
+    }
+    const cudaStream_t sc = reinterpret_cast<cudaStream_t>(compute);
+    const cudaStream_t si = reinterpret_cast<cudaStream_t>(copy_in);
+    const cudaStream_t so = reinterpret_cast<cudaStream_t>(copy_out);
+    // x_ready[s]: chunk in slot s copied in; x_free[s]: its compute done;
+    // y_ready[s]: its output written; y_free[s]: its output copied out.
+    cudaEvent_t ev[8] = {};
+    for (auto &e : ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            for (auto &f : ev)
+                if (f) cudaEventDestroy(f);
+            return WANVAE_ERR_CUDA;
+        }
+    cudaEvent_t *x_ready = ev, *x_free = ev + 2, *y_ready = ev + 4, *y_free = ev + 6;
+    cudaError_t e = cudaMemsetAsync(ca, 0, hp.ca, sc);  // a new clip: empty caches
+    if (e == cudaSuccess) e = cudaMemsetAsync(cb, 0, hp.cb, sc);
+    const size_t fx = (size_t)d.H * d.W * p->c_in * 2, fy = (size_t)d.H * d.W * p->c_out * 2;
+    wanvae_status st = WANVAE_OK;
+    int64_t i = 0;
+    for (int64_t t0 = 0; e == cudaSuccess && st == WANVAE_OK && t0 < d.T; t0 += hp.chunk, ++i) {
+        const int s = (int)(i & 1);
+        const int64_t n = d.T - t0 < hp.chunk ? d.T - t0 : hp.chunk;
+        // copy in: the slot is free once the compute of chunk i-2 is done
+        if (i >= 2) e = cudaStreamWaitEvent(si, x_free[s], 0);
+        for (int64_t b = 0; e == cudaSuccess && b < d.B; ++b)
+            e = cudaMemcpyAsync(xb[s] + (size_t)b * n * fx,
+                                static_cast<const uint8_t *>(x_host) + ((size_t)b * d.T + t0) * fx,
+                                (size_t)n * fx, cudaMemcpyHostToDevice, si);
+        if (e == cudaSuccess) e = cudaEventRecord(x_ready[s], si);
+        // compute: after its input landed and the y slot was copied out
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, x_ready[s], 0);
+        if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(sc, y_free[s], 0);
+        if (e != cudaSuccess) break;
+        wanvae_dims dc = d;
+        dc.T = n;
+        st = resblock_impl(p, xb[s], yb[s], dc, &cache, blk, hp.blk, nullptr, compute, false);
+        if (st != WANVAE_OK) break;
+        e = cudaEventRecord(x_free[s], sc);
+        if (e == cudaSuccess) e = cudaEventRecord(y_ready[s], sc);
+        // copy out
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(so, y_ready[s], 0);
+        for (int64_t b = 0; e == cudaSuccess && b < d.B; ++b)
+            e = cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + ((size_t)b * d.T + t0) * fy,
+                                yb[s] + (size_t)b * n * fy, (size_t)n * fy,
+                                cudaMemcpyDeviceToHost, so);
+        if (e == cudaSuccess) e = cudaEventRecord(y_free[s], so);
+    }
+    for (auto &f : ev) cudaEventDestroy(f);  // released once the work above completes
+    if (st != WANVAE_OK) return st;
+    return from_cuda(e);
 }
 
 wanvae_status wanvae_sync_status(wanvae_stream stream) {

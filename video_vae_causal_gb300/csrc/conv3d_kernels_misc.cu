@@ -26,6 +26,9 @@ ConvKernelFn conv_kernel_up(int pair, int kk, int nsub, int np) {
     if (kk == 4 && nsub == 1 && np == 1)
         return pair == 2 ? conv3d_tcgen05_kernel<2, 4, 1, 1, true>
                          : conv3d_tcgen05_kernel<1, 4, 1, 1, true>;
+    if (kk == 4 && nsub == 1 && np == 2)  // the temporal upsampler at 384 channels
+        return pair == 2 ? conv3d_tcgen05_kernel<2, 4, 1, 2, true>
+                         : conv3d_tcgen05_kernel<1, 4, 1, 2, true>;
     return pair == 2 ? conv3d_tcgen05_kernel<2, 0, 0, 0, true>
                      : conv3d_tcgen05_kernel<1, 0, 0, 0, true>;
 }

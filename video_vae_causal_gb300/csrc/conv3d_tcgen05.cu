@@ -326,7 +326,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
                            4u * 4u * kBlockM /*norm partial sums*/;
     pl.staged = 0;
     if (s.up2d && pl.nacc != 2) return false;  // its scattered stores use the direct epilogue
-    if (pl.nacc == 1 && s.c_out % 64 == 0 && !s.up_t) {  // (the temporal upsampler: direct)
+    if (pl.nacc == 1 && s.c_out % 64 == 0) {
         const uint32_t sb1 = (kBlockM + b_rows) * (uint32_t)sw * 2u;
         if (3u * ((sb1 + 1023u) & ~1023u) + fixed + stage_tile <= (uint32_t)kSmemBudget)
             pl.staged = 1;
@@ -614,7 +614,8 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
             if (s.epi == kEpiResidual)
                 ok = ok && encode_patch(&mR, s.resid, s.c_out, s.W, s.H, frames, 64, 64);
         } else {
-            ok = ok && encode_frames(&mY, s.out, s.c_out, HW, frames);
+            // (the temporal upsampler writes 2T frames: frame 2t + phase)
+            ok = ok && encode_frames(&mY, s.out, s.c_out, HW, frames * (s.up_t ? 2 : 1));
             if (s.epi == kEpiResidual) ok = ok && encode_frames(&mR, s.resid, s.c_out, HW, frames);
         }
     }

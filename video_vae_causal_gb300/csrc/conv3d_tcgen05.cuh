@@ -1189,6 +1189,10 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         fence_proxy_async_smem();  // the tile in `buf` is visible to the TMA stores below
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
         if (issuer) {
+            // output frame: the tile's own, or for the temporal upsampler frame
+            // 2t + a of the unit's phase a
+            const int out_frame =
+                p.up_t ? (ti.n * 2 * p.T + 2 * ti.t + unit_phase(u, p)) : ti.frame;
             if (!ti.dummy) {
                 for (int b = 0; b < nblk; ++b) {
                     if (p.halo)
@@ -1196,7 +1200,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
                                      ti.h0, ti.frame);
                     else
                         tma_store_3d(mapY, buf_s + (uint32_t)b * (kBlockM * 128u), b * 64,
-                                     ti.pos, ti.frame);
+                                     ti.pos, out_frame);
                 }
                 bulk_commit();
             }

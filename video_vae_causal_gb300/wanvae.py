@@ -26,6 +26,7 @@ EXPORTS = (
     "wanvae_upsample2d_conv", "wanvae_set_kernel_variant", "wanvae_time_upsample_workspace_size",
     "wanvae_time_upsample_conv", "wanvae_upsample3d_workspace_size", "wanvae_upsample3d",
     "wanvae_frame_attention_workspace_size", "wanvae_frame_attention",
+    "wanvae_resblock_forward_host_workspace_size", "wanvae_resblock_forward_host",
 )
 
 # Size of the library's own workspace used by resblock_forward_static.
@@ -90,6 +91,11 @@ def load(path=LIB_PATH):
     L.wanvae_sync_status.restype = st
     L.wanvae_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.wanvae_set_wait_limit_ns.restype = None
+    L.wanvae_resblock_forward_host_workspace_size.argtypes = [Dims, i64, i64, i64]
+    L.wanvae_resblock_forward_host_workspace_size.restype = ctypes.c_size_t
+    L.wanvae_resblock_forward_host.argtypes = [ctypes.POINTER(ResblockParams), vp, vp, Dims, i64,
+                                               vp, ctypes.c_size_t, vp, vp, vp]
+    L.wanvae_resblock_forward_host.restype = st
     L.wanvae_set_kernel_variant.argtypes = [ci, ci, ci, ci]
     L.wanvae_set_kernel_variant.restype = None
     L.wanvae_launch_count.argtypes = []
@@ -314,6 +320,29 @@ def resblock_forward(x, params, y=None, cache=None, workspace=None, stream=None,
     _check(st, "wanvae_resblock_forward")
     del keep_alive
     return y
+
+
+def resblock_forward_host_workspace_size(dims, c_in, c_out, chunk_frames):
+    return int(load().wanvae_resblock_forward_host_workspace_size(_dims(dims), c_in, c_out,
+                                                                   chunk_frames))
+
+
+def resblock_forward_host(x_host, params, y_host, chunk_frames, workspace, streams):
+    """Whole-clip ResidualBlock forward of a clip in host memory (x_host, y_host:
+    CPU bf16 tensors, pinned for the copies to overlap), as chunks of
+    chunk_frames frames carried by the feat_cache and pipelined over
+    streams = (compute, copy_in, copy_out).  Returns once enqueued; y_host is
+    complete when streams[2] has drained."""
+    keep_alive = params
+    if isinstance(params, dict):
+        params = make_params(params)
+    sc, si, so = (ctypes.c_void_p(s.cuda_stream) for s in streams)
+    st = load().wanvae_resblock_forward_host(ctypes.byref(params), _ptr(x_host), _ptr(y_host),
+                                             _dims(x_host.shape), int(chunk_frames),
+                                             _ptr(workspace), workspace.numel(), sc, si, so)
+    _check(st, "wanvae_resblock_forward_host")
+    del keep_alive
+    return y_host
 
 
 def resblock_forward_static(x, params, y, cache=None, stream=None):
