@@ -365,6 +365,7 @@ __device__ void attn_softmax(const AttnArgs &p, uint8_t *pbuf, uint32_t tmem, co
 __global__ void __launch_bounds__(kAThreads, 1)
 attn_tcgen05_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mVt, const AttnArgs p) {
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -402,6 +403,7 @@ attn_tcgen05_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{p.wait_ns, p.err, abort_flag, 0u};
+    griddep_wait();  // q, k and V^T written by the previous kernels are visible
     const int items = p.F * p.q_tiles;
     if (warp == 0) {
         if (lane == 0)
@@ -424,6 +426,8 @@ attn_tcgen05_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 __global__ void __launch_bounds__(256)
 transpose_v_kernel(const __nv_bfloat16 *__restrict__ v, __nv_bfloat16 *__restrict__ vt, int N,
                    int D, int ldn) {
+    griddep_launch_dependents();
+    griddep_wait();
     __shared__ __nv_bfloat16 tile[32][33];
     const int f = blockIdx.z;
     const int n0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
@@ -448,10 +452,9 @@ int frame_attention_ldn(int N) { return (N + 7) / 8 * 8; }
 cudaError_t launch_transpose_v(const void *v, void *vt, int F, int N, int D,
                                const LaunchCtx &ctx) {
     const dim3 grid((unsigned)((N + 31) / 32), (unsigned)((D + 31) / 32), (unsigned)F);
-    transpose_v_kernel<<<grid, 256, 0, ctx.stream>>>(static_cast<const __nv_bfloat16 *>(v),
-                                                     static_cast<__nv_bfloat16 *>(vt), N, D,
-                                                     frame_attention_ldn(N));
-    return cudaGetLastError();
+    return launch_pdl(transpose_v_kernel, grid, dim3(256), 0, ctx,
+                      static_cast<const __nv_bfloat16 *>(v), static_cast<__nv_bfloat16 *>(vt), N, D,
+                      frame_attention_ldn(N));
 }
 
 cudaError_t launch_attention_core(const void *q, const void *k, const void *vt, void *out, int F,
@@ -503,8 +506,8 @@ cudaError_t launch_attention_core(const void *q, const void *k, const void *vt, 
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     const int items = F * a.q_tiles;
     const int grid = items < ctx.num_sms ? items : ctx.num_sms;
-    attn_tcgen05_kernel<<<grid, kAThreads, smem, ctx.stream>>>(mQ, mK, mV, a);
-    return cudaGetLastError();
+    return launch_pdl(attn_tcgen05_kernel, dim3((unsigned)grid), dim3(kAThreads), smem, ctx, mQ,
+                      mK, mV, a);
 }
 
 }  // namespace wanvae

@@ -82,6 +82,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX64,
                      const __grid_constant__ CUtensorMap mapC32,
                      const __grid_constant__ CUtensorMap mapW64,
                      const __grid_constant__ CUtensorMap mapW32, const NarrowArgs p) {
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -112,6 +113,7 @@ conv3d_narrow_kernel(const __grid_constant__ CUtensorMap mapX64,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{p.wait_ns, p.err, abort_flag, 0u};
+    griddep_wait();  // the previous kernel's outputs are visible from here on
 
     // The whole B operand (27 c_out rows, rows up to npad read as zeros) once.
     if (tid == 0) {
@@ -316,8 +318,8 @@ cudaError_t launch_narrow(const NarrowArgs &a, const CUtensorMap *m, uint32_t sm
         opted[dev].store(smem, std::memory_order_release);
     }
     const int grid = a.num_items < ctx.num_sms ? a.num_items : ctx.num_sms;
-    kern<<<grid, kThreadsN, smem, ctx.stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreadsN), smem, ctx, m[0], m[1], m[2],
+                      m[3], m[4], m[5], a);
 }
 
 // The kernel-variant setting (set_kernel_variant) can route narrow layers to

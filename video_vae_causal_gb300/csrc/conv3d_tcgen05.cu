@@ -698,22 +698,27 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.wait_ns = ctx.wait_ns;
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    // programmatic dependent launch: the prologue (barriers, TMEM, descriptor
+    // prefetch) overlaps the previous kernel's tail; the kernel waits for it
+    // before its first global read
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
     if (pl.pair == 1) {
         const int units = a.tile_units * a.nphase;
         const int grid = units < ctx.num_sms ? units : ctx.num_sms;
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
-        cfg.numAttrs = 0;
+        cfg.numAttrs = 1;
     } else {
         const int units = a.tile_units * a.nphase;
         const int pairs = units < max_pairs ? units : max_pairs;
         cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
     }
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;

@@ -1219,8 +1219,10 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
     }
 }
 
+// (kThreads threads and one CTA per SM: 200 registers a thread fit the
+// register file and leave the issue loops without spills)
 template <int kPair, int KK, int NSUB, int NP, bool kUp>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(200)
 conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapC,
                       const __grid_constant__ CUtensorMap mapB,
@@ -1228,6 +1230,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapSB,
                       const __grid_constant__ CUtensorMap mapY,
                       const __grid_constant__ CUtensorMap mapR, const ConvArgs p) {
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1288,6 +1291,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
             tmem_relinquish();
         }
     }
+    griddep_wait();  // the previous kernel's outputs (and anything before it) are visible
     for (int i = threadIdx.x; i < p.c_out; i += kThreads) {
         float b = p.bias ? p.bias[i] : 0.f;
         if (p.bias2) b += p.bias2[i];

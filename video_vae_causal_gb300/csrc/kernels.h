@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace wanvae {
 
 // Per-launch context every kernel needs: the device error word and the
@@ -17,6 +19,24 @@ struct LaunchCtx {
     uint64_t wait_ns;   // bound of every device-side wait
     int num_sms;
 };
+
+// Launch `kern` on ctx.stream with programmatic dependent launch allowed (the
+// kernel must call griddep_wait before reading what earlier work wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       const LaunchCtx &ctx, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // SiLU(RMS_norm(x)) over C channels of n voxels; is_f32 selects fp32 in/out
 // (else bf16).  Returns a cudaError_t.

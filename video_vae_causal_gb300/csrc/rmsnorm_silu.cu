@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace wanvae {
 namespace {
@@ -44,6 +45,8 @@ __global__ void __launch_bounds__(256)
 rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                     const float *__restrict__ gamma, int64_t n, int C, int L, float eps,
                     float sqrt_c) {
+    griddep_launch_dependents();
+    griddep_wait();
     constexpr int E = F32 ? 4 : 8;  // channels per 16-byte vector
     const int V = C / E;            // vectors per voxel
     const int lane = threadIdx.x & 31;
@@ -148,8 +151,10 @@ cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n,
             per_sm = 2;                                                                  \
         if (per_sm < 1) per_sm = 1;                                                      \
         const int64_t cap = (int64_t)ctx.num_sms * per_sm;                               \
-        kern<<<(unsigned)(blocks < cap ? blocks : cap), threads, 0, ctx.stream>>>(        \
-            xi, yo, gamma, n, C, L, eps, sqrt_c);                                        \
+        const cudaError_t le = launch_pdl(kern, dim3((unsigned)(blocks < cap ? blocks : cap)), \
+                                          dim3(threads), 0, ctx, xi, yo, gamma, n, C, L, eps,   \
+                                          sqrt_c);                                              \
+        if (le != cudaSuccess) return le;                                                \
         break;                                                                           \
     }
     switch (vpt) {
@@ -182,6 +187,8 @@ cudaError_t dispatch_norm(const void *x, void *y, const float *gamma, int64_t n,
 // the same thread, so the in-place shift has no race).
 __global__ void cache_update_kernel(uint4 *__restrict__ cache, const uint4 *__restrict__ src,
                                     int B, int T, int64_t fv) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t total = (int64_t)B * fv;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -209,6 +216,8 @@ __global__ void cache_update_kernel(uint4 *__restrict__ cache, const uint4 *__re
 // w [Co][3][3][Ci] -> w2 [4 = 2a + b][Co][2][2][Ci], fp32 sums rounded to bf16.
 __global__ void expand_up2d_weights_kernel(const __nv_bfloat16 *__restrict__ w,
                                            __nv_bfloat16 *__restrict__ w2, int Co, int Ci) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t total = (int64_t)4 * Co * 4 * Ci;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -240,6 +249,8 @@ __global__ void expand_up2d_weights_kernel(const __nv_bfloat16 *__restrict__ w,
 // w [Co][3][Ci] -> w2 [2 = a][Co][2 = e][Ci], fp32 sums rounded to bf16.
 __global__ void expand_time_up_weights_kernel(const __nv_bfloat16 *__restrict__ w,
                                               __nv_bfloat16 *__restrict__ w2, int Co, int Ci) {
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t total = (int64_t)2 * Co * 2 * Ci;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -264,9 +275,9 @@ cudaError_t launch_expand_time_up_weights(const void *w, void *w2, int Co, int C
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)ctx.num_sms * 8) blocks = (int64_t)ctx.num_sms * 8;
     if (blocks < 1) blocks = 1;
-    expand_time_up_weights_kernel<<<(unsigned)blocks, 256, 0, ctx.stream>>>(
-        static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2), Co, Ci);
-    return cudaGetLastError();
+    return launch_pdl(expand_time_up_weights_kernel, dim3((unsigned)blocks), dim3(256), 0, ctx,
+                      static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2),
+                      Co, Ci);
 }
 
 cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
@@ -274,9 +285,9 @@ cudaError_t launch_expand_up2d_weights(const void *w, void *w2, int Co, int Ci,
     const int64_t total = (int64_t)4 * Co * 4 * Ci;
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)ctx.num_sms * 8) blocks = (int64_t)ctx.num_sms * 8;
-    expand_up2d_weights_kernel<<<(unsigned)blocks, 256, 0, ctx.stream>>>(
-        static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2), Co, Ci);
-    return cudaGetLastError();
+    return launch_pdl(expand_up2d_weights_kernel, dim3((unsigned)blocks), dim3(256), 0, ctx,
+                      static_cast<const __nv_bfloat16 *>(w), static_cast<__nv_bfloat16 *>(w2),
+                      Co, Ci);
 }
 
 cudaError_t launch_rmsnorm(const void *x, void *y, const float *gamma, int64_t n, int C,
@@ -297,9 +308,8 @@ cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int6
     int64_t blocks = ((int64_t)B * fv + threads - 1) / threads;
     const int64_t cap = (int64_t)ctx.num_sms * 8;
     if (blocks > cap) blocks = cap;
-    cache_update_kernel<<<(unsigned)blocks, threads, 0, ctx.stream>>>(
-        static_cast<uint4 *>(cache), static_cast<const uint4 *>(src), B, T, fv);
-    return cudaGetLastError();
+    return launch_pdl(cache_update_kernel, dim3((unsigned)blocks), dim3(threads), 0, ctx,
+                      static_cast<uint4 *>(cache), static_cast<const uint4 *>(src), B, T, fv);
 }
 
 }  // namespace wanvae
