@@ -1219,10 +1219,10 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
     }
 }
 
-// (kThreads threads and one CTA per SM: 200 registers a thread fit the
-// register file and leave the issue loops without spills)
+// (kThreads = 10 warps, one CTA per SM: three warps share a sub-partition's
+// 16K registers, so at most 168 registers a thread)
 template <int kPair, int KK, int NSUB, int NP, bool kUp>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
 conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapC,
                       const __grid_constant__ CUtensorMap mapB,
