@@ -325,13 +325,17 @@ void wanvae_set_wait_limit_ns(uint64_t ns);
  * no effect on results beyond the summation order of fp32 partial sums).
  * Each argument 0 or 1 forces a choice for later calls; -1 (or any other
  * value) restores the automatic, shape-driven choice:
- *   pair   : 1 = single-CTA conv kernel (cta_group::1) instead of CTA pairs
- *   halo   : 1 = halo tiles, 0 = per-tap im2col tiles (k = 3 convs)
- *   wide   : 1 = 16 x 16 halo patches where they apply, 0 = 16 x 8
- *   narrow : 1 = the GEMM-plus-stencil kernel for c_out <= 3, 0 = the
- *            implicit GEMM for those layers too
+ *   pair      : 1 = single-CTA conv kernel (cta_group::1) instead of CTA pairs
+ *   halo      : 1 = halo tiles, 0 = per-tap im2col tiles (k = 3 convs)
+ *   wide      : 1 = 16 x 16 halo patches where they apply, 0 = 16 x 8
+ *   narrow    : 1 = the GEMM-plus-stencil kernel for c_out <= 3, 0 = the
+ *               implicit GEMM for those layers too
+ *   fuse_norm : 0 = the ResidualBlock's RMS_norm1 + SiLU always as a pass of
+ *               its own; else fused into conv A's halo loads where the plan
+ *               allows (halo tiles, c_in in one chunk of at most 128 channels;
+ *               the values are bit for bit those of the separate pass)
  * A forced choice that cannot run a given shape falls back to one that can. */
-void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow);
+void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow, int fuse_norm);
 
 /* Number of kernels this library has enqueued since load (host counter). */
 uint64_t wanvae_launch_count(void);

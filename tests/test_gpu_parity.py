@@ -400,6 +400,48 @@ def test_resblock_causal_on_gpu(cuda_lib):
     assert torch.equal(y[:, :3], y2[:, :3])
 
 
+# ------------------------------------------------------------------ norm1 fused into conv A
+FUSE_CASES = [
+    # (B, T, H, W, c): one chunk holds all c channels, halo tiles
+    (1, 2, 16, 16, 32),         # the smallest: 32-channel planes, one 16 x 16 patch
+    (1, 4, 32, 32, 96),         # the full-resolution block's 96 channels
+    (2, 3, 17, 24, 64),         # 64-channel swizzled rows, ragged patches, two clips
+    (1, 3, 16, 24, 48),         # three 16-channel sub-tiles
+    (1, 2, 16, 16, 128),        # two 64-channel regions
+]
+
+
+@pytest.mark.parametrize("case", FUSE_CASES)
+@pytest.mark.parametrize("mode", ["pair-wide", "pair-halo", "single-halo"])
+def test_fused_norm_equals_separate_pass(cuda_lib, case, mode):
+    """RMS_norm1 + SiLU applied in conv A's halo loads gives the block output
+    of the separate norm pass bit for bit (same arithmetic), full-T and frame
+    by frame over the feat_cache, and matches the oracle."""
+    B, T, H, W, C = case
+    pair, tiles = mode.split("-")
+    x, p = synth.make_resblock_inputs((B, T, H, W), C, C, seed=31)
+    xd, pd = x.to(DEV), dev(p)
+    outs = {}
+    try:
+        for fuse in (0, 1):
+            cuda_lib.set_kernel_variant(pair=1 if pair == "single" else -1, halo=1,
+                                        wide=1 if tiles == "wide" else 0, fuse_norm=fuse)
+            full = cuda_lib.resblock_forward(xd, pd)
+            cA = torch.zeros((B, 2, H, W, C), dtype=torch.bfloat16, device=DEV)
+            cB = torch.zeros((B, 2, H, W, C), dtype=torch.bfloat16, device=DEV)
+            frames = [cuda_lib.resblock_forward(xd[:, t:t + 1].contiguous(), pd, cache=(cA, cB))
+                      for t in range(T)]
+            cuda_lib.sync_status()
+            outs[fuse] = (full, torch.cat(frames, dim=1), cA.clone())
+    finally:
+        cuda_lib.set_kernel_variant()
+    assert torch.equal(outs[1][0], outs[0][0]), "fused full-T differs from the separate pass"
+    assert torch.equal(outs[1][1], outs[1][0]), "fused streaming differs from fused full-T"
+    assert torch.equal(outs[1][2], outs[0][2]), "fused feat_cache differs"
+    compare(to_f64(outs[1][0]), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
+            what=f"fused {case} {mode}")
+
+
 # ------------------------------------------------------------------ host buffers, pipelined
 @pytest.mark.parametrize("case,chunk", [((1, 7, 16, 24, 64, 64), 3),     # ragged last chunk
                                         ((2, 5, 9, 10, 64, 32), 2),      # two clips, 1x1x1 shortcut

@@ -17,9 +17,10 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libwanvae.so")
 SOURCES = ["api.cu", "rmsnorm_silu.cu", "conv3d_tcgen05.cu", "conv3d_narrow.cu",
            "attn_tcgen05.cu", "conv3d_kernels_p1_n1.cu", "conv3d_kernels_p1_n2.cu",
-           "conv3d_kernels_p2_n1.cu", "conv3d_kernels_p2_n2.cu", "conv3d_kernels_misc.cu"]
+           "conv3d_kernels_p2_n1.cu", "conv3d_kernels_p2_n2.cu", "conv3d_kernels_misc.cu",
+           "conv3d_kernels_fuse.cu"]
 DEPS = SOURCES + ["ptx.cuh", "kernels.h", "exports.map", "conv3d_tcgen05.cuh",
-                  "conv3d_kernels.inc"]
+                  "conv3d_kernels.inc", "norm_act.cuh"]
 HEADER = os.path.join(ROOT, "include", "wanvae.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

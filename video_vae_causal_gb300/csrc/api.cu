@@ -112,8 +112,8 @@ void wanvae_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
 
 uint64_t wanvae_launch_count(void) { return g_launches.load(); }
 
-void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow) {
-    set_kernel_variant(pair, halo, wide, narrow);
+void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow, int fuse_norm) {
+    set_kernel_variant(pair, halo, wide, narrow, fuse_norm);
 }
 
 wanvae_status wanvae_rmsnorm_silu(const void *x, void *y, const float *gamma, wanvae_dtype dt,
@@ -474,6 +474,17 @@ static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *
         sB.resid = x;
     }
     if (conv3d_supported(sA) || conv3d_supported(sB)) return WANVAE_ERR_UNSUPPORTED;
+    // RMS_norm1 + SiLU fused into conv A's halo loads where its plan allows
+    // ("Closing the gap", section 4: the norm and the activation in one pass;
+    // here that pass is conv A's own input path), else a pass of its own.
+    {
+        ConvSpec sf = sA;
+        sf.in = x;
+        sf.norm_in = 1;
+        sf.gamma_in = p->gamma1;
+        if (conv3d_fuses_norm(sf)) sA = sf;
+    }
+    const bool fused = sA.norm_in != 0;
     if (check_only) return WANVAE_OK;
 
     LaunchCtx ctx;
@@ -485,7 +496,7 @@ static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *
     };
     const int64_t frA = d.H * d.W * p->c_in * 2, frB = d.H * d.W * p->c_out * 2;
     cudaError_t e = rec(0);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && !fused) {
         g_launches++;
         e = launch_rmsnorm_silu(x, a1, p->gamma1, false, M, (int)p->c_in, p->eps, ctx);
     }
@@ -496,7 +507,9 @@ static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *
     }
     if (e == cudaSuccess && cache) {
         g_launches++;
-        e = launch_cache_update(cache->convA_in, a1, (int)d.B, (int)d.T, frA, ctx);
+        e = fused ? launch_cache_update_norm(cache->convA_in, x, p->gamma1, (int)d.B, (int)d.T,
+                                             d.H * d.W, (int)p->c_in, p->eps, ctx)
+                  : launch_cache_update(cache->convA_in, a1, (int)d.B, (int)d.T, frA, ctx);
     }
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess) {

@@ -12,6 +12,7 @@
 
 #include "conv3d_tcgen05.cuh"
 #include "kernels.h"
+#include "norm_act.cuh"
 
 namespace wanvae {
 namespace {
@@ -19,8 +20,8 @@ namespace {
 using namespace conv;
 
 // Kernel-variant overrides (set_kernel_variant): -1 = chosen per call.
-enum { kVarPair = 0, kVarHalo = 1, kVarWide = 2, kVarNarrow = 3, kNumVar = 4 };
-std::atomic<int> g_variant[kNumVar] = {{-1}, {-1}, {-1}, {-1}};
+enum { kVarPair = 0, kVarHalo = 1, kVarWide = 2, kVarNarrow = 3, kVarFuse = 4, kNumVar = 5 };
+std::atomic<int> g_variant[kNumVar] = {{-1}, {-1}, {-1}, {-1}, {-1}};
 
 // ------------------------------------------------------------------ host
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -239,6 +240,7 @@ struct Plan {
     int acc_stride;
     uint32_t off_a, a_stride, a_tx;
     int na;  // halo mode: A ring buffers
+    int fuse;  // the input norm fused into the halo loads (conv3d_transform warps)
 };
 
 // Halo tiles (16 x 8 patches, one halo load per temporal tap and channel
@@ -392,11 +394,21 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.off_stage = off;
         if (pl.staged) off += stage_tile;
         pl.off_bars = off;
-        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
+        pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 14);
         pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
         pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                         (s.up2d ? 128u : 0u) /*staging alignment for TMA stores*/ +
                         (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
+        // The input norm can ride on the halo loads when one chunk holds every
+        // channel of a pixel (its norm is then complete in one halo), with no
+        // shortcut segment and two accumulators (four epilogue warps keep up).
+        {
+            const int L = nact_lanes(s.c_in), vpt = (s.c_in / 8) / L;
+            pl.fuse = s.norm_in && s.k == 3 && !s.up2d && !s.up_t && !s.sc_in &&
+                      pl.kc_main == 1 && pl.nsub * sw == s.c_in && pl.nacc == 2 &&
+                      !pl.staged && vpt <= kMaxNormVpt &&
+                      g_variant[kVarFuse].load(std::memory_order_relaxed) != 0;
+        }
         if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
         return pl.smem_bytes <= (uint32_t)kSmemBudget;
     }
@@ -406,6 +418,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.na = 2;
     pl.tb = 1;
     pl.nsub = 1;
+    pl.fuse = 0;
     for (int d = 4; d >= 1; --d) {
         if (d * sw > 128 || g_main % d || g_sc % d) continue;
         const uint32_t sb = (uint32_t)d * (kBlockM + b_rows) * sw * 2;
@@ -443,7 +456,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.off_stage = off;
     if (pl.staged) off += stage_tile;
     pl.off_bars = off;
-    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 10);
+    pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 14);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
     pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                     (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
@@ -521,8 +534,14 @@ int conv3d_supported(const ConvSpec &s) {
     return pick_plan(s, pl, pair_choice()) ? 0 : -1;
 }
 
-void set_kernel_variant(int pair, int halo, int wide, int narrow) {
-    const int v[kNumVar] = {pair, halo, wide, narrow};
+bool conv3d_fuses_norm(const ConvSpec &s) {
+    if (!s.norm_in || conv3d_narrow_supported(s) == 0) return false;
+    Plan pl;
+    return pick_plan(s, pl, pair_choice()) && pl.fuse;
+}
+
+void set_kernel_variant(int pair, int halo, int wide, int narrow, int fuse) {
+    const int v[kNumVar] = {pair, halo, wide, narrow, fuse};
     for (int i = 0; i < kNumVar; ++i)
         g_variant[i].store(v[i] == 0 || v[i] == 1 || (i == kVarPair && v[i] == 2) ? v[i] : -1,
                            std::memory_order_relaxed);
@@ -548,9 +567,11 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     if (conv3d_narrow_supported(s) == 0) return launch_conv3d_narrow(s, ctx);
     Plan pl;
     if (!pick_plan(s, pl, pair_choice())) return cudaErrorInvalidValue;
+    if (s.norm_in && !pl.fuse) return cudaErrorInvalidValue;  // (callers ask conv3d_fuses_norm)
     if (!load_encoders()) return cudaErrorInvalidValue;
     auto pick = [&](int pair) {
         if (s.up2d || s.up_t) return conv_kernel_up(pair, pl.sw / 16, pl.nsub, pl.n_pieces);
+        if (pl.fuse) return conv_kernel_fuse(pair, pl.sw / 16, pl.nsub, pl.n_pieces);
         return conv_kernel_plain(pair, pl.sw / 16, pl.nsub, pl.n_pieces);
     };
     ConvKernelFn fn = pick(pl.pair);
@@ -558,7 +579,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     cudaError_t fe = kernel_facts(fn, pl.pair == 2, max_pairs);
     if (fe != cudaSuccess) return fe;
     if (pl.pair == 2 && max_pairs < 1) {
-        if (!pick_plan(s, pl, 1)) return cudaErrorInvalidValue;
+        if (!pick_plan(s, pl, 1) || (s.norm_in && !pl.fuse)) return cudaErrorInvalidValue;
         fn = pick(1);
         fe = kernel_facts(fn, false, max_pairs);
         if (fe != cudaSuccess) return fe;
@@ -696,6 +717,16 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.out = static_cast<__nv_bfloat16 *>(s.out);
     a.err = ctx.err;
     a.wait_ns = ctx.wait_ns;
+    a.fuse = pl.fuse;
+    a.epi_warps = pl.fuse ? 4 : kEpiWarps;
+    if (pl.fuse) {
+        a.nl_L = nact_lanes(s.c_in);
+        a.nl_vpt = (s.c_in / 8) / a.nl_L;
+        a.sqrt_c_in = sqrtf((float)s.c_in);
+        a.gamma_in = s.gamma_in;
+        a.x_in = static_cast<const __nv_bfloat16 *>(s.in);
+        a.cache_in = static_cast<const __nv_bfloat16 *>(s.cache);
+    }
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];

@@ -43,6 +43,7 @@
 #include <type_traits>
 
 #include "kernels.h"
+#include "norm_act.cuh"
 #include "ptx.cuh"
 
 namespace wanvae {
@@ -54,6 +55,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 rows x 32 bf16 channels
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kMaxItb = 4;  // im2col: most taps per stage (the upsampler's 2 x 2)
+constexpr int kMaxNormVpt = 4;  // fused input norm: most 16-byte vectors a lane holds
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // cleanup waits after an abort
 
 
@@ -79,6 +81,12 @@ struct ConvArgs {
     int na;              // halo mode: buffers in the A (halo) ring, 2 to 4
     int up_tma;          // upsampler on halo tiles: TMA stores through the phase view of y
     int up_t;            // temporal upsampler: frame phases, taps t-1 and t at the centre pixel
+    int fuse;            // input norm fused: warps 2 + epi_warps .. 9 build every halo
+    int epi_warps;       // epilogue warps: 8 (two per TMEM lane quarter), 4 when fused
+    int nl_L, nl_vpt;    // fused norm: lanes per pixel, 16-byte vectors per lane
+    float sqrt_c_in;     // fused norm: sqrt(c_in)
+    const float *gamma_in;
+    const __nv_bfloat16 *x_in, *cache_in;  // fused: raw input x and the cache (normalised)
     int ph_c2, ph_c3;    // upsampler: B box coordinates 2 and 3 advance by phase x these
     int stages;
     uint32_t a_sub_bytes, b_sub_bytes, a_bytes, stage_bytes, stage_tx;
@@ -213,6 +221,8 @@ struct Bars {
     __device__ uint32_t drain() const { return base + 8u * (2 * stages + 4); }
     __device__ uint32_t resf() const { return base + 8u * (2 * stages + 5); }
     __device__ uint32_t emptya(int i) const { return base + 8u * (2 * stages + 6 + i); }
+    // fused norm in a CTA pair: the peer's halo in A buffer i is written
+    __device__ uint32_t peer(int i) const { return base + 8u * (2 * stages + 10 + i); }
 };
 
 // The MMA issuer's view of the `full` ring.  Every barrier access by the
@@ -414,7 +424,7 @@ __device__ __forceinline__ void load4(uint32_t dst, const CUtensorMap *m, uint32
 // spatial taps each (B ring); the halo completes on the barrier of the first
 // of those stages, so the MMA issuer waits once per stage.  Then the shortcut
 // segment's chunks (x patch into the A ring + its weights, one stage each).
-template <int kPair, bool kUp>
+template <int kPair, bool kUp, bool kFuse>
 __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *mapC,
                                    const CUtensorMap *mapB, const CUtensorMap *mapSA,
                                    const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
@@ -427,11 +437,17 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
     uint32_t phase = 0, pha = 0, fills = 0;
     bool ok = true;
     // Next B stage, armed for `tx` bytes per CTA (both CTAs' loads complete
-    // on the leader's barrier).
-    auto next_stage = [&](uint32_t tx, uint32_t &dst, uint32_t &fb) -> bool {
+    // on the leader's barrier).  With the input norm fused a stage completes
+    // on two arrivals: a halo's first stage gets its second from the
+    // transform warps once the pair's halos are written, the others get both
+    // from here.
+    auto next_stage = [&](uint32_t tx, bool second, uint32_t &dst, uint32_t &fb) -> bool {
         if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) return false;
         const uint32_t fl = bars.full(stage);
-        if (rank == 0) mbar_arrive_expect_tx(fl, tx * kPair);
+        if (rank == 0) {
+            mbar_arrive_expect_tx(fl, tx * kPair);
+            if (second) mbar_arrive(fl);
+        }
         fb = kPair == 2 ? mapa_shared(fl, 0) : fl;
         dst = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
         ++fills;
@@ -466,18 +482,24 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
                 }
             }
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
-                uint32_t da;
-                if (!next_abuf(da)) {
+                uint32_t da = 0;
+                if (kFuse) {  // the transform warps fill the A buffer
+                    if (++ia == p.na) {
+                        ia = 0;
+                        pha ^= 1u;
+                    }
+                } else if (!next_abuf(da)) {
                     ok = false;
                     break;
                 }
                 for (int g = 0; g < groups; ++g) {
                     uint32_t db, fb;
-                    if (!next_stage(p.stage_tx + (g == 0 ? p.a_tx : 0u), db, fb)) {
+                    if (!next_stage(p.stage_tx + (g == 0 && !kFuse ? p.a_tx : 0u),
+                                    kFuse && g > 0, db, fb)) {
                         ok = false;
                         break;
                     }
-                    if (g == 0) {
+                    if (g == 0 && !kFuse) {
                         if (p.halo_rows) {
                             for (int s = 0; s < p.nsub; ++s)  // one region per sw channels
                                 load4<kPair>(da + (uint32_t)s * p.sub_stride, am, fb,
@@ -500,7 +522,7 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         const uint32_t sub_a = (uint32_t)kBlockM * p.sw * 2u;
         for (int cc = 0; ok && cc < p.kc_short; ++cc) {
             uint32_t da, db, fb;
-            if (!next_abuf(da) || !next_stage(p.nsub * (sub_a + p.b_sub_bytes), db, fb)) {
+            if (!next_abuf(da) || !next_stage(p.nsub * (sub_a + p.b_sub_bytes), kFuse, db, fb)) {
                 ok = false;
                 break;
             }
@@ -518,6 +540,135 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
         for (uint32_t f = fills - n; f < fills; ++f)
             mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
+    }
+}
+
+// Shared-memory address of the 16-byte vector j (channels 8j .. 8j + 7) of
+// halo pixel `pix` in an A buffer: one 128-byte swizzled row per pixel and
+// 64-channel region (the layout TMA's 128-byte swizzle writes), or 8-channel
+// planes of 16 bytes per pixel.
+__device__ __forceinline__ uint32_t halo_vec_addr(const ConvArgs &p, uint32_t abuf, int pix,
+                                                  int j) {
+    if (p.halo_rows)
+        return abuf + (uint32_t)(j >> 3) * p.sub_stride + (uint32_t)pix * 128u +
+               ((uint32_t)((j & 7) ^ (pix & 7)) << 4);
+    return abuf + (uint32_t)j * p.plane_bytes + (uint32_t)pix * 16u;
+}
+
+// The input norm fused into the halo loads (warps 2 + epi_warps .. 9, four
+// warps).  For every halo of the unit sequence, in the producer's order, they
+// read the pixels from global memory and write what the MMAs multiply into the
+// A buffer: SiLU(RMS_norm(x)) for frames of the clip (every channel of a
+// pixel is in the one chunk, so the norm is complete), the cache's frames as
+// they are (the cache holds normalised frames), zeros outside the frame or
+// the clip.  L lanes share a pixel as in the standalone norm pass, with the
+// same arithmetic, so the values are bit for bit that pass's.  Then the
+// halo's first weight stage gets its second arrival -- from the leader CTA,
+// after the peer CTA reported its halo written and once the stage's previous
+// phase has completed.
+template <int kPair>
+__device__ void conv_transform(const ConvArgs &p, uint32_t sbase, const Bars &bars,
+                               const WaitCtl &wc, int unit0, int unit_stride, int num_units,
+                               uint32_t rank) {
+    const int tw = (threadIdx.x >> 5) - 2 - p.epi_warps;  // 0 .. 3
+    const int lane = threadIdx.x & 31;
+    const int L = p.nl_L, vpt = p.nl_vpt;
+    const int sub = lane & (L - 1), grp = lane / L, gpw = 32 / L;
+    const int npix = (int)kHaloH * p.halo_w;
+    const bool leader = tw == 0 && lane == 0;
+    const int groups = p.sp_taps / p.tb;
+    const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma_in);
+    int stage = 0, ia = 0;
+    uint32_t phase = 0, pha = 0, peer_par = 0;
+    bool ok = true;
+    for (int u = unit0; ok && u < num_units; u += unit_stride) {
+        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
+        const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
+        for (int kt = kt0; ok && kt < 3; ++kt) {
+            const int tt = ti.t + kt - 2;
+            const __nv_bfloat16 *src = nullptr;  // null: zeros
+            bool norm = false;
+            if (!ti.dummy) {
+                if (tt >= 0) {
+                    src = p.x_in + (size_t)(ti.n * p.T + tt) * p.HW * p.c_in;
+                    norm = true;
+                } else if (p.has_cache) {
+                    src = p.cache_in + (size_t)(ti.n * 2 + tt + 2) * p.HW * p.c_in;
+                }
+            }
+            const int slot = ia;
+            const uint32_t slot_par = pha;
+            if (++ia == p.na) {
+                ia = 0;
+                pha ^= 1u;
+            }
+            const int s0 = stage;
+            const uint32_t ph0 = phase;
+            for (int g = 0; g < groups; ++g)
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            // the A buffer is free once the MMAs of its previous halo are done
+            ok = mbar_wait_warp<kPair == 2>(bars.emptya(slot), slot_par ^ 1u, wc);
+            if (bar_any(2, 128, !ok)) {
+                ok = false;
+                break;
+            }
+            const uint32_t abuf = sbase + p.off_a + (uint32_t)slot * p.a_stride;
+            for (int pb = tw * gpw; pb < npix; pb += 4 * gpw) {  // warp-uniform bound
+                const int pix = pb + grp;
+                const bool valid = pix < npix;
+                const int hy = pix / p.halo_w, hx = pix - hy * p.halo_w;
+                const int h = ti.h0 - 1 + hy, w = ti.w0 - 1 + hx;
+                const bool in = valid && src && h >= 0 && h < p.H && w >= 0 && w < p.W;
+                const uint4 *pv = in ? reinterpret_cast<const uint4 *>(
+                                           src + ((size_t)h * p.W + w) * p.c_in)
+                                     : nullptr;
+                uint4 v[kMaxNormVpt];
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < kMaxNormVpt; ++i) {
+                    if (i < vpt) {
+                        v[i] = in ? __ldg(pv + sub + i * L) : make_uint4(0u, 0u, 0u, 0u);
+                        if (norm) ss = nact_sumsq8(v[i], ss);
+                    }
+                }
+                if (norm) ss = nact_group_sum(ss, L);  // (norm is uniform over the warp)
+                const float scale = nact_scale(ss, p.sqrt_c_in, p.eps);
+#pragma unroll
+                for (int i = 0; i < kMaxNormVpt; ++i) {
+                    if (i < vpt && valid) {
+                        const int j = sub + i * L;
+                        const uint4 o = (norm && in)
+                                            ? nact_apply8<true>(v[i], scale, __ldg(g4 + 2 * j),
+                                                                __ldg(g4 + 2 * j + 1))
+                                            : v[i];
+                        const uint32_t a = halo_vec_addr(p, abuf, pix, j);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                                     : "memory");
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the tensor core reads the halo (async proxy)
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (leader) {
+                if (kPair == 2 && rank == 1) {
+                    mbar_arrive_cluster(mapa_shared(bars.peer(slot), 0));
+                } else {
+                    bool w = true;
+                    if (kPair == 2) {
+                        w = mbar_wait<true>(bars.peer(slot), (peer_par >> slot) & 1u, wc);
+                        peer_par ^= 1u << slot;
+                    }
+                    // this arrival belongs to the stage's phase ph0: the one
+                    // before must have completed
+                    if (w) w = mbar_wait<kPair == 2>(bars.full(s0), ph0 ^ 1u, wc);
+                    if (w) mbar_arrive_cluster(bars.full(s0));
+                }
+            }
+        }
     }
 }
 
@@ -874,7 +1025,9 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
     const int q = warp & 3;           // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2; // 0 or 1: which column half
     const int row = q * 32 + lane;
-    const int c_split = ((p.c_out / 2) + 15) / 16 * 16;
+    // eight epilogue warps: two per lane quarter, each half the columns;
+    // four: one per lane quarter, all of them
+    const int c_split = p.epi_warps == 8 ? ((p.c_out / 2) + 15) / 16 * 16 : p.c_out;
     const int c_begin = half ? c_split : 0, c_end = half ? p.c_out : c_split;
     int it = 0;
     uint32_t nst = 0;  // staging half of this warp's next TMA store (upsampler)
@@ -885,7 +1038,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         if (p.epi == kEpiNormSilu) {
             // The norm's halves meet at a named barrier below, so all epilogue
             // warps take the same decision: stop if any of them gave up.
-            if (bar_any(1, 32 * kEpiWarps, !got)) break;
+            if (bar_any(1, 32 * p.epi_warps, !got)) break;
         } else if (!got) {
             break;
         }
@@ -932,9 +1085,13 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                     }
                 }
             }
-            part[half * kBlockM + row] = ss;
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-            const float tot = part[row] + part[kBlockM + row];
+            // (four epilogue warps: each thread has summed the whole row)
+            float tot = ss;
+            if (p.epi_warps == 8) {
+                part[half * kBlockM + row] = ss;
+                asm volatile("bar.sync 1, %0;" ::"r"(32 * p.epi_warps) : "memory");
+                tot = part[row] + part[kBlockM + row];
+            }
             const float scale = p.sqrt_c / fmaxf(sqrtf(tot), p.eps);
             for (int c = c_begin; c < c_end; c += 32) {
                 uint32_t r[32];
@@ -1080,7 +1237,9 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
-    const int c_split = ((p.c_out / 2) + 15) / 16 * 16;
+    // eight epilogue warps: two per lane quarter, each half the columns;
+    // four: one per lane quarter, all of them
+    const int c_split = p.epi_warps == 8 ? ((p.c_out / 2) + 15) / 16 * 16 : p.c_out;
     const int c_begin = half ? c_split : 0, c_end = half ? p.c_out : c_split;
     const bool issuer = warp == 2 && lane == 0;
     const bool resid = p.epi == kEpiResidual;
@@ -1115,7 +1274,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
             res_phase ^= 1u;
             if (issuer) res_pending = false;
         }
-        if (bar_any(1, 32 * kEpiWarps, !got)) break;  // same decision in every epilogue warp
+        if (bar_any(1, 32 * p.epi_warps, !got)) break;  // same decision in every epilogue warp
         tc_fence_after();
         const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
         uint8_t *rowp = buf + row * 128;  // row `row` of block 0
@@ -1156,7 +1315,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         }
         if (norm) s_part[half * kBlockM + row] = ss;
         tc_fence_before();
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * p.epi_warps) : "memory");
         if (lane == 0) {
             // TMEM read out: the MMA warp may start the next tile now.
             if (kPair == 2)
@@ -1187,7 +1346,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
             }
         }
         fence_proxy_async_smem();  // the tile in `buf` is visible to the TMA stores below
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * p.epi_warps) : "memory");
         if (issuer) {
             // output frame: the tile's own, or for the temporal upsampler frame
             // 2t + a of the unit's phase a
@@ -1221,7 +1380,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
 
 // (kThreads = 10 warps, one CTA per SM: three warps share a sub-partition's
 // 16K registers, so at most 168 registers a thread)
-template <int kPair, int KK, int NSUB, int NP, bool kUp>
+template <int kPair, int KK, int NSUB, int NP, bool kUp, bool kFuse = false>
 __global__ void __launch_bounds__(kThreads, 1)
 conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapC,
@@ -1256,16 +1415,18 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(bars.full(s), 1);
+            mbar_init(bars.full(s), kFuse ? 2 : 1);  // (fused: the weights' and the halo's)
             mbar_init(bars.empty(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bars.accf(a), 1);
-            mbar_init(bars.acce(a), kEpiWarps * kPair);
+            mbar_init(bars.acce(a), p.epi_warps * kPair);
         }
         mbar_init(bars.drain(), 1);
         mbar_init(bars.resf(), 1);
         for (int i = 0; i < 4; ++i) mbar_init(bars.emptya(i), 1);
+        if (kFuse)
+            for (int i = 0; i < 4; ++i) mbar_init(bars.peer(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1310,8 +1471,9 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     if (warp == 0) {
         if (lane == 0) {
             if (p.halo)
-                conv_producer_halo<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
-                                          unit0, unit_stride, num_units, rank);
+                conv_producer_halo<kPair, kUp, kFuse>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p,
+                                                      sbase, bars, wc, unit0, unit_stride,
+                                                      num_units, rank);
             else
                 conv_producer<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
                                      unit0, unit_stride, num_units, rank);
@@ -1325,6 +1487,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                 conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
                                               num_units);
         }
+    } else if (kFuse && warp >= 2 + p.epi_warps) {
+        conv_transform<kPair>(p, sbase, bars, wc, unit0, unit_stride, num_units, rank);
     } else {
         if (p.staged)
             conv_epilogue_staged<kPair>(p, tmem_base, s_bias, s_gamma, s_part,
@@ -1362,6 +1526,7 @@ typedef void (*ConvKernelFn)(const CUtensorMap, const CUtensorMap, const CUtenso
 // upsamplers' instantiations.
 ConvKernelFn conv_kernel_plain(int pair, int kk, int nsub, int np);
 ConvKernelFn conv_kernel_up(int pair, int kk, int nsub, int np);
+ConvKernelFn conv_kernel_fuse(int pair, int kk, int nsub, int np);
 
 }  // namespace conv
 }  // namespace wanvae

@@ -108,7 +108,26 @@ struct ConvSpec {
     // the phase weights [2][c_out][2][c_in]; out is [B][2T][H][W][c_out];
     // k = 3, no cache, bias epilogue.
     int up_t;
+    // Fused input norm (the block's conv A): the conv reads the raw block
+    // input x as `in` and applies SiLU(RMS_norm(x; gamma_in, eps)) to every
+    // halo pixel on its way to shared memory, so a1 is never written out.
+    // `cache` then holds normalised frames, as without fusion.  Honoured only
+    // where conv3d_fuses_norm() says the plan allows it.
+    int norm_in;
+    const float *gamma_in;  // [c_in]
 };
+
+// Whether launch_conv3d runs `s` (with norm_in set) with the input norm fused
+// into the conv: halo tiles whose one channel chunk holds all c_in channels
+// (c_in <= 128), no shortcut segment, double-buffered accumulators.
+bool conv3d_fuses_norm(const ConvSpec &s);
+
+// feat_cache update for a fused conv: cache[b] <- the last two frames of
+// concat(cache[b], SiLU(RMS_norm(src[b]; gamma, eps))), src bf16
+// [B][T][HW][C]; the same arithmetic and lane grouping as the standalone
+// norm pass (bit-identical frames).
+cudaError_t launch_cache_update_norm(void *cache, const void *src, const float *gamma, int B,
+                                     int T, int64_t HW, int C, float eps, const LaunchCtx &ctx);
 
 // Host-side validation of a ConvSpec the library can run (channel counts,
 // sizes); returns 0 if supported.
@@ -128,8 +147,9 @@ cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx);
 // argument 0 or 1 forces that choice, anything else restores the automatic
 // choice.  pair: 1 = single-CTA kernel, else CTA pairs; halo: halo tiles (1)
 // or im2col tiles (0); wide: 16 x 16 halo patches (1) or 16 x 8 (0); narrow:
-// the GEMM-plus-stencil kernel for c_out <= 3 (1) or the implicit GEMM (0).
-void set_kernel_variant(int pair, int halo, int wide, int narrow);
+// the GEMM-plus-stencil kernel for c_out <= 3 (1) or the implicit GEMM (0);
+// fuse: 0 = never fuse the block's input norm into conv A, else where possible.
+void set_kernel_variant(int pair, int halo, int wide, int narrow, int fuse);
 int narrow_variant();
 
 // cuTensorMapEncodeTiled for a bf16 tensor of `rank` dimensions (driver

@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "norm_act.cuh"
 #include "ptx.cuh"
 
 namespace wanvae {
@@ -78,24 +79,25 @@ rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                     float c = __uint_as_float(buf[u][i].z), d = __uint_as_float(buf[u][i].w);
                     ss[u] += a * a + b * b + c * c + d * d;
                 } else {
-                    const uint32_t w4[4] = {buf[u][i].x, buf[u][i].y, buf[u][i].z, buf[u][i].w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float a = bf16lo(w4[k]), b = bf16hi(w4[k]);
-                        ss[u] += a * a + b * b;
-                    }
+                    ss[u] = nact_sumsq8(buf[u][i], ss[u]);
                 }
             }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            for (int off = L >> 1; off > 0; off >>= 1)
-                ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
+        for (int u = 0; u < U; ++u) {
+            if (F32) {
+                for (int off = L >> 1; off > 0; off >>= 1)
+                    ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], off);
+            } else {
+                ss[u] = nact_group_sum(ss[u], L);
+            }
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t v = v0 + u * gpw + grp;
             if (v >= n) continue;
-            const float scale = sqrt_c / fmaxf(sqrtf(ss[u]), eps);
+            const float scale = F32 ? sqrt_c / fmaxf(sqrtf(ss[u]), eps)
+                                    : nact_scale(ss[u], sqrt_c, eps);
 #pragma unroll
             for (int i = 0; i < VPT; ++i) {
                 const int j = sub + i * L;
@@ -109,15 +111,7 @@ rmsnorm_silu_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ y,
                     o.z = __float_as_uint(act<kSilu>(__uint_as_float(b.z) * scale * g.z));
                     o.w = __float_as_uint(act<kSilu>(__uint_as_float(b.w) * scale * g.w));
                 } else {
-                    const float4 ga = __ldg(g4), gb = __ldg(g4 + 1);
-                    o.x = pack_bf16x2(act<kSilu>(bf16lo(b.x) * scale * ga.x),
-                                      act<kSilu>(bf16hi(b.x) * scale * ga.y));
-                    o.y = pack_bf16x2(act<kSilu>(bf16lo(b.y) * scale * ga.z),
-                                      act<kSilu>(bf16hi(b.y) * scale * ga.w));
-                    o.z = pack_bf16x2(act<kSilu>(bf16lo(b.z) * scale * gb.x),
-                                      act<kSilu>(bf16hi(b.z) * scale * gb.y));
-                    o.w = pack_bf16x2(act<kSilu>(bf16lo(b.w) * scale * gb.z),
-                                      act<kSilu>(bf16hi(b.w) * scale * gb.w));
+                    o = nact_apply8<kSilu>(b, scale, __ldg(g4), __ldg(g4 + 1));
                 }
                 y[v * V + j] = o;
             }
@@ -202,6 +196,59 @@ __global__ void cache_update_kernel(uint4 *__restrict__ cache, const uint4 *__re
             const uint4 keep = c[fv];
             c[0] = keep;
             c[fv] = s[0];
+        }
+    }
+}
+
+// feat_cache update of a conv whose input norm is fused (its input a1 =
+// SiLU(RMS_norm(x)) is never written out): cache[b] <- the last two frames of
+// concat(cache[b], a1(src[b])).  A group of L lanes owns a pixel, lane `sub`
+// its vectors sub, sub + L, ..., the grouping and arithmetic of the
+// standalone pass, so the frames are bit for bit those that pass (and the
+// conv's fused transform) produce.  T == 1: frame 1 moves to frame 0 and a1 of
+// src's frame becomes frame 1; each lane copies its own vectors of a pixel
+// before it overwrites them, so the in-place shift has no race.
+template <int VPT>
+__global__ void __launch_bounds__(256)
+cache_update_norm_kernel(uint4 *__restrict__ cache, const uint4 *__restrict__ src,
+                         const float *__restrict__ gamma, int B, int T, int64_t HW, int C, int L,
+                         float eps, float sqrt_c) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int V = C / 8;  // 16-byte vectors per pixel
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & (L - 1), grp = lane / L, gpw = 32 / L;
+    const int64_t warp_id = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t npix = (int64_t)B * HW;
+    const float4 *g4 = reinterpret_cast<const float4 *>(gamma);
+    for (int64_t p0 = warp_id * gpw; p0 < npix; p0 += nwarps * gpw) {  // warp-uniform
+        const int64_t pix = p0 + grp;
+        const bool valid = pix < npix;
+        const int64_t b = valid ? pix / HW : 0, q = valid ? pix - b * HW : 0;
+        uint4 *c0 = cache + ((b * 2 + 0) * HW + q) * V;
+        uint4 *c1 = cache + ((b * 2 + 1) * HW + q) * V;
+        // frames of src that become cache frames: T >= 2: T-2 -> 0 and T-1 -> 1
+        for (int f = (T >= 2 ? 0 : 1); f < 2; ++f) {
+            const int tsrc = T - 2 + f;
+            const uint4 *ps = src + ((b * T + tsrc) * HW + q) * V;
+            uint4 v[VPT];
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                v[i] = valid ? __ldg(ps + sub + i * L) : make_uint4(0u, 0u, 0u, 0u);
+                ss = nact_sumsq8(v[i], ss);
+            }
+            ss = nact_group_sum(ss, L);
+            const float scale = nact_scale(ss, sqrt_c, eps);
+            if (!valid) continue;
+            uint4 *dst = f == 0 ? c0 : c1;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int j = sub + i * L;
+                if (T == 1) c0[j] = c1[j];  // (f == 1 only: move frame 1 first)
+                dst[j] = nact_apply8<true>(v[i], scale, __ldg(g4 + 2 * j), __ldg(g4 + 2 * j + 1));
+            }
         }
     }
 }
@@ -299,6 +346,30 @@ cudaError_t launch_rmsnorm_silu(const void *x, void *y, const float *gamma, bool
                                 int64_t n, int C, float eps, const LaunchCtx &ctx) {
     return is_f32 ? dispatch_norm<true>(x, y, gamma, n, C, eps, ctx)
                   : dispatch_norm<false>(x, y, gamma, n, C, eps, ctx);
+}
+
+cudaError_t launch_cache_update_norm(void *cache, const void *src, const float *gamma, int B,
+                                     int T, int64_t HW, int C, float eps, const LaunchCtx &ctx) {
+    const int L = nact_lanes(C), vpt = (C / 8) / L;
+    const int threads = 256;
+    int64_t blocks = ((int64_t)B * HW * L + threads - 1) / threads;
+    const int64_t cap = (int64_t)ctx.num_sms * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    auto *c = static_cast<uint4 *>(cache);
+    auto *x = static_cast<const uint4 *>(src);
+    const float sc = sqrtf((float)C);
+    switch (vpt) {
+        case 1: return launch_pdl(cache_update_norm_kernel<1>, dim3((unsigned)blocks),
+                                  dim3(threads), 0, ctx, c, x, gamma, B, T, HW, C, L, eps, sc);
+        case 2: return launch_pdl(cache_update_norm_kernel<2>, dim3((unsigned)blocks),
+                                  dim3(threads), 0, ctx, c, x, gamma, B, T, HW, C, L, eps, sc);
+        case 3: return launch_pdl(cache_update_norm_kernel<3>, dim3((unsigned)blocks),
+                                  dim3(threads), 0, ctx, c, x, gamma, B, T, HW, C, L, eps, sc);
+        case 4: return launch_pdl(cache_update_norm_kernel<4>, dim3((unsigned)blocks),
+                                  dim3(threads), 0, ctx, c, x, gamma, B, T, HW, C, L, eps, sc);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,

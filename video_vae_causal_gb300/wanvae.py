@@ -96,7 +96,7 @@ def load(path=LIB_PATH):
     L.wanvae_resblock_forward_host.argtypes = [ctypes.POINTER(ResblockParams), vp, vp, Dims, i64,
                                                vp, ctypes.c_size_t, vp, vp, vp]
     L.wanvae_resblock_forward_host.restype = st
-    L.wanvae_set_kernel_variant.argtypes = [ci, ci, ci, ci]
+    L.wanvae_set_kernel_variant.argtypes = [ci, ci, ci, ci, ci]
     L.wanvae_set_kernel_variant.restype = None
     L.wanvae_launch_count.argtypes = []
     L.wanvae_launch_count.restype = ctypes.c_uint64
@@ -161,9 +161,10 @@ def set_wait_limit_ns(ns):
     load().wanvae_set_wait_limit_ns(int(ns))
 
 
-def set_kernel_variant(pair=-1, halo=-1, wide=-1, narrow=-1):
+def set_kernel_variant(pair=-1, halo=-1, wide=-1, narrow=-1, fuse_norm=-1):
     """Force kernel variants for later calls (0 or 1 each; -1 = automatic)."""
-    load().wanvae_set_kernel_variant(int(pair), int(halo), int(wide), int(narrow))
+    load().wanvae_set_kernel_variant(int(pair), int(halo), int(wide), int(narrow),
+                                     int(fuse_norm))
 
 
 def sync_status(stream=None):
