@@ -435,11 +435,13 @@ def test_fused_norm_equals_separate_pass(cuda_lib, case, mode):
             outs[fuse] = (full, torch.cat(frames, dim=1), cA.clone())
     finally:
         cuda_lib.set_kernel_variant()
-    assert torch.equal(outs[1][0], outs[0][0]), "fused full-T differs from the separate pass"
+    ref = oracle.resblock_forward(x, oracle.Params.from_dict(p))
+    compare(to_f64(outs[1][0]), ref, what=f"fused {case} {mode}")
+    compare(to_f64(outs[0][0]), ref, what=f"separate {case} {mode}")
+    d = (outs[1][0].float() - outs[0][0].float()).abs().max().item()
+    assert torch.equal(outs[1][0], outs[0][0]), f"fused full-T differs from the separate pass by {d}"
     assert torch.equal(outs[1][1], outs[1][0]), "fused streaming differs from fused full-T"
     assert torch.equal(outs[1][2], outs[0][2]), "fused feat_cache differs"
-    compare(to_f64(outs[1][0]), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
-            what=f"fused {case} {mode}")
 
 
 # ------------------------------------------------------------------ host buffers, pipelined

@@ -1071,26 +1071,36 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 }
             }
         } else if (p.epi == kEpiNormSilu) {
-            // RMS_norm over all c_out channels of this voxel, then SiLU.
-            float ss = 0.f;
-            for (int c = c_begin; c < c_end; c += 32) {
-                uint32_t r[32];
-                const int n = c_end - c >= 32 ? 32 : 16;
-                tmem_ld_cols(tb + (uint32_t)c, n, r);
+            // RMS_norm over all c_out channels of this voxel, then SiLU.  The
+            // sum of squares is taken over two column halves and then added,
+            // whether two warps share the row (eight epilogue warps) or one
+            // warp has all of it (four): the same value either way.
+            const int c_half = ((p.c_out / 2) + 15) / 16 * 16;
+            float ssh[2] = {0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (i < n) {
-                        const float v = __uint_as_float(r[i]) + s_bias[c + i];
-                        ss += v * v;
+            for (int hh = 0; hh < 2; ++hh) {
+                const int cb = hh ? c_half : 0, ce = hh ? p.c_out : c_half;
+                if (p.epi_warps == 8 && hh != half) continue;
+                float ss = 0.f;
+                for (int c = cb; c < ce; c += 32) {
+                    uint32_t r[32];
+                    const int n = ce - c >= 32 ? 32 : 16;
+                    tmem_ld_cols(tb + (uint32_t)c, n, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if (i < n) {
+                            const float v = __fadd_rn(__uint_as_float(r[i]), s_bias[c + i]);
+                            ss = __fmaf_rn(v, v, ss);
+                        }
                     }
                 }
+                ssh[hh] = ss;
             }
-            // (four epilogue warps: each thread has summed the whole row)
-            float tot = ss;
+            float tot = __fadd_rn(ssh[0], ssh[1]);
             if (p.epi_warps == 8) {
-                part[half * kBlockM + row] = ss;
+                part[half * kBlockM + row] = ssh[half];
                 asm volatile("bar.sync 1, %0;" ::"r"(32 * p.epi_warps) : "memory");
-                tot = part[row] + part[kBlockM + row];
+                tot = __fadd_rn(part[row], part[kBlockM + row]);
             }
             const float scale = p.sqrt_c / fmaxf(sqrtf(tot), p.eps);
             for (int c = c_begin; c < c_end; c += 32) {
