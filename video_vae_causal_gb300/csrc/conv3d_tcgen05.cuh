@@ -567,9 +567,11 @@ __device__ __forceinline__ uint32_t halo_vec_addr(const ConvArgs &p, uint32_t ab
 // after the peer CTA reported its halo written and once the stage's previous
 // phase has completed.
 template <int kPair>
-__device__ void conv_transform(const ConvArgs &p, uint32_t sbase, const Bars &bars,
+__device__ void conv_transform(const CUtensorMap *mapA, const CUtensorMap *mapC,
+                               const ConvArgs &p, uint32_t sbase, const Bars &bars,
                                const WaitCtl &wc, int unit0, int unit_stride, int num_units,
                                uint32_t rank) {
+    constexpr int NB = 3;  // pixel iterations whose loads are in flight together
     const int tw = (threadIdx.x >> 5) - 2 - p.epi_warps;  // 0 .. 3
     const int lane = threadIdx.x & 31;
     const int L = p.nl_L, vpt = p.nl_vpt;
@@ -578,22 +580,56 @@ __device__ void conv_transform(const ConvArgs &p, uint32_t sbase, const Bars &ba
     const bool leader = tw == 0 && lane == 0;
     const int groups = p.sp_taps / p.tb;
     const float4 *g4 = reinterpret_cast<const float4 *>(p.gamma_in);
+    // Source of the halo of unit u at temporal tap kt: frame index fidx of x
+    // (norm) or of the cache, or none (zeros).
+    struct Src {
+        int fidx;
+        bool cache, any;
+    };
+    auto source = [&](const TileInfo &t2, int kt) -> Src {
+        const int tt = t2.t + kt - 2;
+        if (t2.dummy) return Src{0, false, false};
+        if (tt >= 0) return Src{t2.n * p.T + tt, false, true};
+        if (p.has_cache) return Src{t2.n * 2 + tt + 2, true, true};
+        return Src{0, false, false};
+    };
+    // L2 prefetch of a halo box (the loads below then hit L2, not DRAM)
+    auto prefetch = [&](const TileInfo &t2, const Src &sr) {
+        if (!sr.any) return;
+        const CUtensorMap *m = sr.cache ? mapC : mapA;
+        if (p.halo_rows) {
+            for (int sidx = 0; sidx < p.nsub; ++sidx)
+                tma_prefetch_l2_4d(m, sidx * p.sw, t2.w0 - 1, t2.h0 - 1, sr.fidx);
+        } else {
+            tma_prefetch_l2_5d(m, 0, t2.w0 - 1, t2.h0 - 1, 0, sr.fidx);
+        }
+    };
     int stage = 0, ia = 0;
     uint32_t phase = 0, pha = 0, peer_par = 0;
     bool ok = true;
+    if (leader && unit0 < num_units) {  // the first halo
+        const int u = unit0, kt = unit_first_kt<kPair>(unit_tile(u, p), p);
+        const TileInfo t2 = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
+        prefetch(t2, source(t2, kt));
+    }
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
         const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         for (int kt = kt0; ok && kt < 3; ++kt) {
-            const int tt = ti.t + kt - 2;
-            const __nv_bfloat16 *src = nullptr;  // null: zeros
-            bool norm = false;
-            if (!ti.dummy) {
-                if (tt >= 0) {
-                    src = p.x_in + (size_t)(ti.n * p.T + tt) * p.HW * p.c_in;
-                    norm = true;
-                } else if (p.has_cache) {
-                    src = p.cache_in + (size_t)(ti.n * 2 + tt + 2) * p.HW * p.c_in;
+            const Src sr = source(ti, kt);
+            const __nv_bfloat16 *src =
+                !sr.any ? nullptr
+                        : (sr.cache ? p.cache_in : p.x_in) + (size_t)sr.fidx * p.HW * p.c_in;
+            const bool norm = sr.any && !sr.cache;
+            if (leader) {  // the next halo, into L2 while this one is built
+                int un = u, ktn = kt + 1;
+                if (ktn == 3) {
+                    un = u + unit_stride;
+                    ktn = un < num_units ? unit_first_kt<kPair>(unit_tile(un, p), p) : 0;
+                }
+                if (un < num_units) {
+                    const TileInfo tn = tile_info(unit_tile(un, p) * kPair + (int)rank, p);
+                    prefetch(tn, source(tn, ktn));
                 }
             }
             const int slot = ia;
@@ -616,38 +652,45 @@ __device__ void conv_transform(const ConvArgs &p, uint32_t sbase, const Bars &ba
                 break;
             }
             const uint32_t abuf = sbase + p.off_a + (uint32_t)slot * p.a_stride;
-            for (int pb = tw * gpw; pb < npix; pb += 4 * gpw) {  // warp-uniform bound
-                const int pix = pb + grp;
-                const bool valid = pix < npix;
-                const int hy = pix / p.halo_w, hx = pix - hy * p.halo_w;
-                const int h = ti.h0 - 1 + hy, w = ti.w0 - 1 + hx;
-                const bool in = valid && src && h >= 0 && h < p.H && w >= 0 && w < p.W;
-                const uint4 *pv = in ? reinterpret_cast<const uint4 *>(
-                                           src + ((size_t)h * p.W + w) * p.c_in)
-                                     : nullptr;
-                uint4 v[kMaxNormVpt];
-                float ss = 0.f;
+            for (int pb = tw * gpw; pb < npix; pb += 4 * gpw * NB) {  // warp-uniform bound
+                uint4 v[NB][kMaxNormVpt];
+                bool in[NB];
 #pragma unroll
-                for (int i = 0; i < kMaxNormVpt; ++i) {
-                    if (i < vpt) {
-                        v[i] = in ? __ldg(pv + sub + i * L) : make_uint4(0u, 0u, 0u, 0u);
-                        if (norm) ss = nact_sumsq8(v[i], ss);
-                    }
+                for (int b = 0; b < NB; ++b) {  // every load of NB iterations first
+                    const int pix = pb + b * 4 * gpw + grp;
+                    const int hy = pix / p.halo_w, hx = pix - hy * p.halo_w;
+                    const int h = ti.h0 - 1 + hy, w = ti.w0 - 1 + hx;
+                    in[b] = pix < npix && src && h >= 0 && h < p.H && w >= 0 && w < p.W;
+                    const uint4 *pv = reinterpret_cast<const uint4 *>(
+                        src + ((size_t)(in[b] ? h : 0) * p.W + (in[b] ? w : 0)) * p.c_in);
+#pragma unroll
+                    for (int i = 0; i < kMaxNormVpt; ++i)
+                        if (i < vpt)
+                            v[b][i] = in[b] ? __ldg(pv + sub + i * L) : make_uint4(0u, 0u, 0u, 0u);
                 }
-                if (norm) ss = nact_group_sum(ss, L);  // (norm is uniform over the warp)
-                const float scale = nact_scale(ss, p.sqrt_c_in, p.eps);
 #pragma unroll
-                for (int i = 0; i < kMaxNormVpt; ++i) {
-                    if (i < vpt && valid) {
-                        const int j = sub + i * L;
-                        const uint4 o = (norm && in)
-                                            ? nact_apply8<true>(v[i], scale, __ldg(g4 + 2 * j),
-                                                                __ldg(g4 + 2 * j + 1))
-                                            : v[i];
-                        const uint32_t a = halo_vec_addr(p, abuf, pix, j);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                                     "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                                     : "memory");
+                for (int b = 0; b < NB; ++b) {
+                    const int pix = pb + b * 4 * gpw + grp;
+                    float ss = 0.f;
+#pragma unroll
+                    for (int i = 0; i < kMaxNormVpt; ++i)
+                        if (i < vpt && norm) ss = nact_sumsq8(v[b][i], ss);
+                    if (norm) ss = nact_group_sum(ss, L);  // (norm is uniform over the warp)
+                    const float scale = nact_scale(ss, p.sqrt_c_in, p.eps);
+#pragma unroll
+                    for (int i = 0; i < kMaxNormVpt; ++i) {
+                        if (i < vpt && pix < npix) {
+                            const int j = sub + i * L;
+                            const uint4 o = (norm && in[b])
+                                                ? nact_apply8<true>(v[b][i], scale,
+                                                                    __ldg(g4 + 2 * j),
+                                                                    __ldg(g4 + 2 * j + 1))
+                                                : v[b][i];
+                            const uint32_t a = halo_vec_addr(p, abuf, pix, j);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                         "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                                         : "memory");
+                        }
                     }
                 }
             }
@@ -1498,7 +1541,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                                               num_units);
         }
     } else if (kFuse && warp >= 2 + p.epi_warps) {
-        conv_transform<kPair>(p, sbase, bars, wc, unit0, unit_stride, num_units, rank);
+        conv_transform<kPair>(&mapA, &mapC, p, sbase, bars, wc, unit0, unit_stride, num_units,
+                              rank);
     } else {
         if (p.staged)
             conv_epilogue_staged<kPair>(p, tmem_base, s_bias, s_gamma, s_part,

@@ -183,6 +183,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// L2 prefetch of a tiled box (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *m, int c0, int c1, int c2,
+                                                   int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_5d(const CUtensorMap *m, int c0, int c1, int c2,
+                                                   int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
 // 4-D im2col load over an NHWC tensor map: pixelsPerColumn pixels walked in
 // (W, H, N) order from base pixel (w, h, n) inside the map's bounding box,
 // each read at (pixel + (off_w, off_h)), channelsPerPixel channels from c.
