@@ -330,10 +330,11 @@ void wanvae_set_wait_limit_ns(uint64_t ns);
  *   wide      : 1 = 16 x 16 halo patches where they apply, 0 = 16 x 8
  *   narrow    : 1 = the GEMM-plus-stencil kernel for c_out <= 3, 0 = the
  *               implicit GEMM for those layers too
- *   fuse_norm : 0 = the ResidualBlock's RMS_norm1 + SiLU always as a pass of
- *               its own; else fused into conv A's halo loads where the plan
- *               allows (halo tiles, c_in in one chunk of at most 128 channels;
- *               the values are bit for bit those of the separate pass)
+ *   fuse_norm : 1 = the ResidualBlock's RMS_norm1 + SiLU fused into conv A's
+ *               halo loads where the plan allows (halo tiles, c_in in one
+ *               chunk of 16, 32, 48, 64, 96 or 128 channels; the values are
+ *               bit for bit those of the separate pass, the time is longer);
+ *               else (the default) a pass of its own
  * A forced choice that cannot run a given shape falls back to one that can. */
 void wanvae_set_kernel_variant(int pair, int halo, int wide, int narrow, int fuse_norm);
 

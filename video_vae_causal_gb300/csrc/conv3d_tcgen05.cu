@@ -402,12 +402,15 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         // The input norm can ride on the halo loads when one chunk holds every
         // channel of a pixel (its norm is then complete in one halo), with no
         // shortcut segment and two accumulators (four epilogue warps keep up).
+        // Only on request (set_kernel_variant): measured slower than the
+        // separate pass, since every input voxel is normalised once per
+        // temporal tap and halo it falls in (about 3.8 times) by four warps.
         {
             const int L = nact_lanes(s.c_in), vpt = (s.c_in / 8) / L;
             pl.fuse = s.norm_in && s.k == 3 && !s.up2d && !s.up_t && !s.sc_in &&
                       pl.kc_main == 1 && pl.nsub * sw == s.c_in && pl.nacc == 2 &&
                       !pl.staged && vpt <= kMaxNormVpt &&
-                      g_variant[kVarFuse].load(std::memory_order_relaxed) != 0;
+                      g_variant[kVarFuse].load(std::memory_order_relaxed) == 1;
         }
         if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
         return pl.smem_bytes <= (uint32_t)kSmemBudget;

@@ -148,7 +148,7 @@ cudaError_t launch_conv3d_narrow(const ConvSpec &s, const LaunchCtx &ctx);
 // choice.  pair: 1 = single-CTA kernel, else CTA pairs; halo: halo tiles (1)
 // or im2col tiles (0); wide: 16 x 16 halo patches (1) or 16 x 8 (0); narrow:
 // the GEMM-plus-stencil kernel for c_out <= 3 (1) or the implicit GEMM (0);
-// fuse: 0 = never fuse the block's input norm into conv A, else where possible.
+// fuse: 1 = fuse the block's input norm into conv A where possible, else never.
 void set_kernel_variant(int pair, int halo, int wide, int narrow, int fuse);
 int narrow_variant();
 
