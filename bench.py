@@ -79,7 +79,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def conv_source_sha(files=("conv3d_tcgen05.cu", "ptx.cuh")):
+CONV_SOURCES = ("conv3d_tcgen05.cu", "conv3d_tcgen05.cuh", "ptx.cuh", "norm_act.cuh")
+
+
+def conv_source_sha(files=CONV_SOURCES):
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "video_vae_causal_gb300", "csrc", f), "rb") as fh:
@@ -87,7 +90,7 @@ def conv_source_sha(files=("conv3d_tcgen05.cu", "ptx.cuh")):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name, kernel="conv3d_tcgen05", files=("conv3d_tcgen05.cu", "ptx.cuh")):
+def profiled_traffic(name, kernel="conv3d_tcgen05", files=CONV_SOURCES):
     """DRAM bytes per launch of `kernel` in workload `name` from its committed
     ncu summary, if there is one taken on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{name}.md")
@@ -611,7 +614,7 @@ def bench_conv(args):
     narrow = not up and not upt and ci >= 32 and ci % 32 == 0 and ci <= 128 and co <= 3 and k == 3
     kname = "conv3d_narrow" if narrow else "conv3d_tcgen05"
     traffic = None if args.frames else profiled_traffic(
-        name, kname, (kname + ".cu", "ptx.cuh"))
+        name, kname, ("conv3d_narrow.cu", "ptx.cuh") if narrow else CONV_SOURCES)
     main.update({"kernel": kname + "_kernel", "traffic": traffic,
                  "peak_source": peaks["source"] + (" bf16 burst" if main is tensor else " HBM copy"),
                  "arith_intensity_flop_per_byte": flop / nbytes, "ridge_flop_per_byte": ridge})
