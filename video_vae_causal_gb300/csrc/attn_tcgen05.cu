@@ -422,26 +422,47 @@ attn_tcgen05_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constan
 
 // v [F][N][D] -> vt [F][D][ldn] (ldn >= N, a multiple of 8 so that rows
 // start on 16 bytes): V as the K-major B operand of O += P V, keys along K.
-// 32 x 32 tiles through shared memory (padded against bank conflicts).
+// A CTA moves a 64 (positions) x 64 (dims) tile: 16-byte loads of 8 dims of
+// a position into shared memory, then 16-byte stores of 8 positions of a dim
+// (gathered from the tile's column).  Positions past N are not written.
+constexpr int kTp = 64;
 __global__ void __launch_bounds__(256)
 transpose_v_kernel(const __nv_bfloat16 *__restrict__ v, __nv_bfloat16 *__restrict__ vt, int N,
                    int D, int ldn) {
     griddep_launch_dependents();
     griddep_wait();
-    __shared__ __nv_bfloat16 tile[32][33];
+    __shared__ uint16_t tile[kTp][kTp + 2];  // [position][dim], padded rows
     const int f = blockIdx.z;
-    const int n0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-    const __nv_bfloat16 *src = v + (int64_t)f * N * D;
-    __nv_bfloat16 *dst = vt + (int64_t)f * D * ldn;
-    for (int i = ty; i < 32; i += 8) {
-        const int n = n0 + i, d = d0 + tx;
-        if (n < N && d < D) tile[i][tx] = src[(int64_t)n * D + d];
+    const int n0 = blockIdx.x * kTp, d0 = blockIdx.y * kTp;
+    const uint16_t *src = reinterpret_cast<const uint16_t *>(v) + (int64_t)f * N * D;
+    uint16_t *dst = reinterpret_cast<uint16_t *>(vt) + (int64_t)f * D * ldn;
+    for (int e = threadIdx.x; e < kTp * kTp / 8; e += blockDim.x) {
+        const int i = e >> 3, c8 = (e & 7) * 8;  // position row, first dim
+        const int n = n0 + i;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N) w = __ldg(reinterpret_cast<const uint4 *>(src + (int64_t)n * D + d0 + c8));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            tile[i][c8 + 2 * k] = (uint16_t)(ws[k] & 0xffffu);
+            tile[i][c8 + 2 * k + 1] = (uint16_t)(ws[k] >> 16);
+        }
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int d = d0 + i, n = n0 + tx;
-        if (d < D && n < N) dst[(int64_t)d * ldn + n] = tile[tx][i];
+    for (int e = threadIdx.x; e < kTp * kTp / 8; e += blockDim.x) {
+        const int j = e >> 3, p8 = (e & 7) * 8;  // dim row, first position
+        const int n = n0 + p8;
+        if (n >= N) continue;
+        uint16_t *out = dst + (int64_t)(d0 + j) * ldn + n;
+        if (n + 8 <= N) {
+            uint32_t ws[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                ws[k] = (uint32_t)tile[p8 + 2 * k][j] | ((uint32_t)tile[p8 + 2 * k + 1][j] << 16);
+            *reinterpret_cast<uint4 *>(out) = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+        } else {
+            for (int k = 0; n + k < N; ++k) out[k] = tile[p8 + k][j];
+        }
     }
 }
 
@@ -451,7 +472,8 @@ int frame_attention_ldn(int N) { return (N + 7) / 8 * 8; }
 
 cudaError_t launch_transpose_v(const void *v, void *vt, int F, int N, int D,
                                const LaunchCtx &ctx) {
-    const dim3 grid((unsigned)((N + 31) / 32), (unsigned)((D + 31) / 32), (unsigned)F);
+    if (D % kTp) return cudaErrorInvalidValue;  // (D is 128, 256 or 384)
+    const dim3 grid((unsigned)((N + kTp - 1) / kTp), (unsigned)(D / kTp), (unsigned)F);
     return launch_pdl(transpose_v_kernel, grid, dim3(256), 0, ctx,
                       static_cast<const __nv_bfloat16 *>(v), static_cast<__nv_bfloat16 *>(vt), N, D,
                       frame_attention_ldn(N));
