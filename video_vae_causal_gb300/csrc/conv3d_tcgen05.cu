@@ -243,37 +243,18 @@ struct Plan {
     int fuse;  // the input norm fused into the halo loads (conv3d_transform warps)
 };
 
-// SMs of the current device (looked up once per device).
-int device_sms() {
-    constexpr int kMaxDev = 64;
-    static std::atomic<int> sms[kMaxDev];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 148;
-    int n = sms[dev].load(std::memory_order_relaxed);
-    if (n == 0) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-            n = 148;
-        sms[dev].store(n, std::memory_order_relaxed);
-    }
-    return n;
-}
-
 // Halo tiles (16 x 8 patches, one halo load per temporal tap and channel
 // chunk feeding all nine spatial taps) move ~6x fewer A bytes and 9x fewer A
-// loads than per-tap im2col.  Chosen when the patches tile the frame exactly,
-// and for calls of at most about one wave of tiles (a frame-by-frame decode
-// call) when ragged patches add at most 1/8 to the area: measured faster
-// there (720p streaming call 0.229 -> 0.215 ms), slower for many waves of
-// ragged tiles (the latent-size clip).  The kernel-variant setting
-// (set_kernel_variant) can force either.
+// loads than per-tap im2col, but cover H x W in whole patches: chosen when the
+// patches tile the frame exactly.  The choice depends on the frame, never on
+// T, so that a clip run frame by frame and run whole use the same tiles (and
+// give the same bits).  The kernel-variant setting (set_kernel_variant) can
+// force either.
 int halo_choice(const ConvSpec &s) {
     if (s.k != 3) return 0;
     const int v = g_variant[kVarHalo].load(std::memory_order_relaxed);
     if (v == 0 || v == 1) return v;
-    if (s.H % 16 == 0 && s.W % 8 == 0) return 1;
-    const int64_t ph = (s.H + 15) / 16, pw = (s.W + 7) / 8;
-    const int64_t tiles = (int64_t)s.B * s.T * ph * pw;
-    return tiles <= 2 * device_sms() && 8 * ph * 16 * pw * 8 <= 9 * (int64_t)s.H * s.W;
+    return s.H % 16 == 0 && s.W % 8 == 0;
 }
 
 // CTA pairs halve each CTA's share of the B (weight) operand -- half the
@@ -285,15 +266,15 @@ int pair_choice() {
 
 // Wide halo tiles (16 x 16 patches, two accumulators per CTA) where the
 // patches tile the frame, the layer is narrow enough (make_plan checks c_out
-// and the shortcut) and there are enough of them to fill the GPU (a tiny clip
-// spreads better as twice as many 16 x 8 tiles).  The kernel-variant setting
-// can force either.
+// and the shortcut) and a frame holds at least 16 of them across the batch: a
+// small frame spreads better over the SMs as twice as many 16 x 8 tiles (the
+// 16 x 16 tiny clip: 0.034 -> 0.027 ms).  Per frame, not per clip (see
+// halo_choice).  The kernel-variant setting can force either.
 int wide_choice(const ConvSpec &s, int halo) {
     if (!halo) return 0;
     const int v = g_variant[kVarWide].load(std::memory_order_relaxed);
     if (v == 0 || v == 1) return v;
-    const int64_t tiles = (int64_t)s.B * s.T * (s.H / 16) * (s.W / 16);
-    return s.H % 16 == 0 && s.W % 16 == 0 && tiles >= device_sms();
+    return s.H % 16 == 0 && s.W % 16 == 0 && (int64_t)s.B * (s.H / 16) * (s.W / 16) >= 16;
 }
 
 bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
