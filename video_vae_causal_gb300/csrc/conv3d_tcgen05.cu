@@ -727,6 +727,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.wait_ns = ctx.wait_ns;
     a.fuse = pl.fuse;
     a.epi_warps = pl.fuse ? 4 : kEpiWarps;
+    // Two MMA issuers wherever the accumulators split in two: the sub-tiles
+    // of a wide halo tile, or two N pieces.
+    a.issuers = (a.nq == 2 || pl.n_pieces == 2) ? 2 : 1;
     if (pl.fuse) {
         a.nl_L = nact_lanes(s.c_in);
         a.nl_vpt = (s.c_in / 8) / a.nl_L;

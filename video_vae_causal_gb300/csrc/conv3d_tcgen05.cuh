@@ -29,9 +29,10 @@
 // matrix, one tiled TMA box per (chunk, N-piece).  Both land in smem with the
 // hardware swizzle that the UMMA descriptors name.
 //
-// Warp roles (192 threads, one persistent CTA per SM): warp 0 = TMA producer,
-// warp 1 = MMA issuer (and TMEM owner), warps 2-5 = epilogue, one TMEM lane
-// quarter each.  An mbarrier ring of `stages` smem buffers links producer and
+// Warp roles (352 threads, one persistent CTA per SM): warp 0 = TMA producer,
+// warp 1 = MMA issuer (and TMEM owner), warps 2-9 = epilogue, two per TMEM
+// lane quarter, warp 10 = second MMA issuer where the accumulators split
+// between two.  An mbarrier ring of `stages` smem buffers links producer and
 // MMA; up to two accumulators in TMEM let the epilogue of tile i overlap the
 // MMAs of tile i+1 when 2 * c_out fits in TMEM's 512 columns.  Every wait is
 // bounded (ptx.cuh).
@@ -51,7 +52,16 @@ namespace conv {
 
 constexpr int kBlockM = 128;
 constexpr int kEpiWarps = 8;  // two warps per TMEM lane quarter, each half the columns
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// The second MMA issuer (after the producer, the first issuer and the
+// epilogue warps).  Every shared-memory access by an issuing thread -- a
+// barrier wait, even a plain load -- returns only after the operand reads of
+// the MMAs it already issued, and the tensor core then runs dry until the
+// thread issues again.  Two issuers that own separate accumulators (the two
+// sub-tiles of a wide tile, or the two N pieces of a wide layer) each wait
+// for every stage themselves, so one keeps the tensor core fed while the
+// other waits.
+constexpr int kIssuer2Warp = 2 + kEpiWarps;
+constexpr int kThreads = 32 * (kIssuer2Warp + 1);
 constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 rows x 32 bf16 channels
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kMaxItb = 4;  // im2col: most taps per stage (the upsampler's 2 x 2)
@@ -83,6 +93,7 @@ struct ConvArgs {
     int up_t;            // temporal upsampler: frame phases, taps t-1 and t at the centre pixel
     int fuse;            // input norm fused: warps 2 + epi_warps .. 9 build every halo
     int epi_warps;       // epilogue warps: 8 (two per TMEM lane quarter), 4 when fused
+    int issuers;         // MMA issuers: 2 = one per sub-tile (nq = 2) or per N piece, else 1
     int nl_L, nl_vpt;    // fused norm: lanes per pixel, 16-byte vectors per lane
     float sqrt_c_in;     // fused norm: sqrt(c_in)
     const float *gamma_in;
@@ -721,7 +732,8 @@ __device__ void conv_transform(const CUtensorMap *mapA, const CUtensorMap *mapC,
 template <int kPair, int KK, int NSUB, int NP>
 __device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc, uint64_t a0,
                                                uint64_t b0, uint32_t b_sub16, uint32_t a_sub16,
-                                               uint32_t a_kk16, uint32_t idesc, bool first) {
+                                               uint32_t a_kk16, uint32_t idesc, bool first,
+                                               int np_run) {
     const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
     auto mma = [&](int s, int kk, int ks, int j) {
         const uint64_t ad = a0 + (uint64_t)(s * a_sub16 + kk * a_kk16);
@@ -744,7 +756,7 @@ __device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc,
         const int kk_n = p.sw / 16;
         for (int s = 0; s < p.nsub; ++s)
             for (int kk = 0; kk < kk_n; ++kk)
-                for (int j = 0; j < p.n_pieces; ++j) mma(s, kk, s * kk_n + kk, j);
+                for (int j = 0; j < np_run; ++j) mma(s, kk, s * kk_n + kk, j);
     }
 }
 
@@ -753,10 +765,11 @@ __device__ __forceinline__ void issue_tap_halo(const ConvArgs &p, uint32_t dacc,
 // unrolled and every descriptor is the stage's base plus a constant (the
 // issuing thread must not spend more cycles between two MMAs than one MMA
 // takes on the tensor core).  KK == 0 selects the run-time-bounded form for
-// shapes without a specialisation.
+// shapes without a specialisation, over np_run pieces.
 template <int kPair, int KK, int NSUB, int NP>
 __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, uint64_t a0,
-                                            uint64_t b0, uint32_t idesc, bool first) {
+                                            uint64_t b0, uint32_t idesc, bool first,
+                                            int np_run) {
     const uint32_t a_sub16 = p.a_sub_bytes >> 4, b_sub16 = p.b_sub_bytes >> 4;
     const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * (uint32_t)p.sw * 2u >> 4;
     if (KK > 0) {
@@ -782,7 +795,7 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
             for (int kk = 0; kk < p.sw / 16; ++kk) {
                 const uint64_t ad = a0 + (uint64_t)(s * a_sub16 + 2 * kk);
                 const uint32_t accum = (first && s == 0 && kk == 0) ? 0u : 1u;
-                for (int j = 0; j < p.n_pieces; ++j) {
+                for (int j = 0; j < np_run; ++j) {
                     const uint64_t bd = b0 + (uint64_t)(s * b_sub16 + j * piece16 + 2 * kk);
                     const uint32_t d = dacc + (uint32_t)(j * p.piece_n);
                     if (kPair == 2)
@@ -800,11 +813,13 @@ __device__ __forceinline__ void issue_stage(const ConvArgs &p, uint32_t dacc, ui
 // each of the nq sub-tiles (one TMEM accumulator each); the halo buffer is
 // released after the ninth tap.  Descriptors are the ring bases plus
 // offsets, so nothing but the stage bookkeeping sits between two stages'
-// MMAs.
+// MMAs.  With two issuers (p.issuers == 2) issuer `part` runs every stage for
+// sub-tile `part` (nq == 2) or for N piece `part`: the same MMAs, in the same
+// order per accumulator, split by accumulator.
 template <int kPair, int KK, int NSUB, int NP, bool kUp>
 __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base,
                               const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
-                              int num_units) {
+                              int num_units, int part) {
     const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
     const uint32_t row_bytes = (uint32_t)p.sw * 2u;
     const uint32_t b_sub16 = p.b_sub_bytes >> 4;
@@ -823,6 +838,18 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
                     : sdesc_plain(sbase + p.off_a, p.plane_bytes, (uint32_t)p.halo_w * 16u);
     const bool tb3 = p.tb == 3, tb4 = kUp && p.tb == 4;
     const int nst = p.tb == 1 ? p.sp_taps : (tb3 ? 3 : 1);  // weight stages per (kt, chunk)
+    // This issuer's share: a sub-tile (its accumulator and its halo window
+    // 8 pixels along), or an N piece (its accumulator columns and its rows of
+    // every weight stage).
+    const bool split_q = p.issuers == 2 && p.nq == 2;
+    const bool split_n = p.issuers == 2 && p.nq != 2;
+    const int nq_run = split_q ? 1 : p.nq;
+    const int np_run = split_n ? 1 : p.n_pieces;
+    const uint32_t piece16 = (uint32_t)(p.piece_n / kPair) * row_bytes >> 4;
+    const uint32_t d_part =
+        split_q ? (uint32_t)(part * p.acc_cols) : (split_n ? (uint32_t)(part * p.piece_n) : 0u);
+    const uint64_t a_part = split_q ? (uint64_t)(8 * part) * px16 : 0u;
+    const uint64_t b_part = split_n ? (uint64_t)part * piece16 : 0u;
     FullRing<kPair == 2> ring;
     int ia = 0, it = 0;
     bool ok = true;
@@ -832,45 +859,54 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
         else
             mma_commit(bar);
     };
-    // One stage: taps kw = 0 .. NTAP-1 of row kh (or the single tap `tap0`),
-    // for every sub-tile.  NQ and NTAP are compile-time so the whole stage
-    // is one straight run of MMAs.
     // One stage: NTAP taps from (kh, kw0), NW to a tap row (3 x 1 of a plain
-    // conv's row, 2 x 2 of an upsampler phase, or one tap), for every
-    // sub-tile.  All compile-time, so the whole stage is one straight run of
-    // MMAs.
-    auto stage = [&](auto nq_c, auto ntap_c, auto nw_c, uint32_t dacc, uint64_t abase, int kh,
-                     int kw0, bool first) {
+    // conv's row, 2 x 2 of an upsampler phase, or one tap), for NQ sub-tiles
+    // and NPc N pieces.  All compile-time, so the whole stage is one straight
+    // run of MMAs.
+    auto stage = [&](auto nq_c, auto ntap_c, auto nw_c, auto np_c, uint32_t dacc, uint64_t abase,
+                     int kh, int kw0, bool first) {
         constexpr int NQ = decltype(nq_c)::value, NTAP = decltype(ntap_c)::value;
-        constexpr int NW = decltype(nw_c)::value;
-        const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16);
+        constexpr int NW = decltype(nw_c)::value, NPc = decltype(np_c)::value;
+        const uint64_t b0 = bdesc0 + (uint64_t)(ring.stage * stage16) + b_part;
         const uint64_t ah = abase + (uint64_t)(kh * hrow16 + kw0 * px16);
 #pragma unroll
         for (int j = 0; j < NTAP; ++j)
 #pragma unroll
             for (int sq = 0; sq < NQ; ++sq)
-                issue_tap_halo<kPair, KK, NSUB, NP>(
+                issue_tap_halo<kPair, KK, NSUB, NPc>(
                     p, dacc + (uint32_t)(sq * p.acc_cols),
                     ah + (uint64_t)((j / NW) * hrow16 + (j % NW + 8 * sq) * px16),
                     b0 + (uint64_t)(j * tap_b16), b_sub16, a_sub16, a_kk16, idesc,
-                    first && j == 0);
+                    first && j == 0, np_run);
     };
     using I1 = std::integral_constant<int, 1>;
     using I2 = std::integral_constant<int, 2>;
     using I3 = std::integral_constant<int, 3>;
     using I4 = std::integral_constant<int, 4>;
+    // (4-tap stages exist in the upsampler's kernels only)
+    auto any_stage = [&](auto np_c, uint32_t dacc, uint64_t abase, int kh, int kw0, bool first) {
+        if (nq_run == 2) {
+            if (tb3) stage(I2{}, I3{}, I3{}, np_c, dacc, abase, kh, kw0, first);
+            else if (kUp && tb4) stage(I2{}, I4{}, I2{}, np_c, dacc, abase, kh, kw0, first);
+            else stage(I2{}, I1{}, I1{}, np_c, dacc, abase, kh, kw0, first);
+        } else {
+            if (tb3) stage(I1{}, I3{}, I3{}, np_c, dacc, abase, kh, kw0, first);
+            else if (kUp && tb4) stage(I1{}, I4{}, I2{}, np_c, dacc, abase, kh, kw0, first);
+            else stage(I1{}, I1{}, I1{}, np_c, dacc, abase, kh, kw0, first);
+        }
+    };
     for (int u = unit0; ok && u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
         if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
-        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
+        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride) + d_part;
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
         const TapBase tbase = kUp ? unit_tap_base(u, p) : TapBase{0, 0};
         bool first = true;
         for (int kt = kt0; ok && kt < 3; ++kt) {
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
-                const uint64_t abase = adesc0 + (uint64_t)(ia * astride16);
+                const uint64_t abase = adesc0 + (uint64_t)(ia * astride16) + a_part;
                 // the first stage of (kt, cc) also carries the halo; the
                 // stage's first tap (kh, kw0) steps by tb along rows of sp_w
                 int kh = tbase.kh, kw0 = tbase.kw;
@@ -880,15 +916,11 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
                         break;
                     }
                     tc_fence_after();
-                    // (4-tap stages exist in the upsampler's kernels only)
-                    if (p.nq == 2) {
-                        if (tb3) stage(I2{}, I3{}, I3{}, dacc, abase, kh, kw0, first);
-                        else if (kUp && tb4) stage(I2{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
-                        else stage(I2{}, I1{}, I1{}, dacc, abase, kh, kw0, first);
+                    if constexpr (NP == 2) {
+                        if (split_n) any_stage(I1{}, dacc, abase, kh, kw0, first);
+                        else any_stage(I2{}, dacc, abase, kh, kw0, first);
                     } else {
-                        if (tb3) stage(I1{}, I3{}, I3{}, dacc, abase, kh, kw0, first);
-                        else if (kUp && tb4) stage(I1{}, I4{}, I2{}, dacc, abase, kh, kw0, first);
-                        else stage(I1{}, I1{}, I1{}, dacc, abase, kh, kw0, first);
+                        any_stage(std::integral_constant<int, NP>{}, dacc, abase, kh, kw0, first);
                     }
                     first = false;
                     commit(bars.empty(ring.stage));
@@ -911,11 +943,18 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
             }
             tc_fence_after();
             // x patch in the A buffer, swizzled like the weights: the stage
-            // issue routine of the im2col path applies unchanged.
+            // issue routine of the im2col path applies unchanged.  (Plans with
+            // a shortcut have one sub-tile, so a split is by N piece.)
             const uint32_t abuf = sbase + p.off_a + (uint32_t)ia * p.a_stride;
             const uint32_t sb = sbase + p.a_bytes + (uint32_t)ring.stage * p.stage_bytes;
-            issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(abuf, row_bytes, p.layout),
-                                             sdesc_kmajor(sb, row_bytes, p.layout), idesc, first);
+            const uint64_t ad = sdesc_kmajor(abuf, row_bytes, p.layout);
+            const uint64_t bd = sdesc_kmajor(sb, row_bytes, p.layout) + b_part;
+            if constexpr (NP == 2) {
+                if (split_n) issue_stage<kPair, KK, NSUB, 1>(p, dacc, ad, bd, idesc, first, 1);
+                else issue_stage<kPair, KK, NSUB, 2>(p, dacc, ad, bd, idesc, first, 2);
+            } else {
+                issue_stage<kPair, KK, NSUB, NP>(p, dacc, ad, bd, idesc, first, np_run);
+            }
             first = false;
             commit(bars.empty(ring.stage));
             commit(bars.emptya(ia));
@@ -934,12 +973,18 @@ __device__ void conv_mma_halo(const ConvArgs &p, uint32_t sbase, uint32_t tmem_b
     mbar_wait<kPair == 2>(bars.drain(), 0u, dc);
 }
 
-// MMA issuer (one thread of the leader CTA).
+// MMA issuer (one thread of the leader CTA).  With two issuers, issuer
+// `part` runs every stage for N piece `part` (its accumulator columns and its
+// rows of each weight stage).
 template <int kPair, int KK, int NSUB, int NP>
 __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, const Bars &bars,
-                         const WaitCtl &wc, int unit0, int unit_stride, int num_units) {
+                         const WaitCtl &wc, int unit0, int unit_stride, int num_units, int part) {
     const uint32_t idesc = idesc_bf16_f32(kBlockM * kPair, p.piece_n);
     const uint32_t row_bytes = (uint32_t)p.sw * 2u;
+    const bool split_n = p.issuers == 2;
+    const uint32_t d_part = split_n ? (uint32_t)(part * p.piece_n) : 0u;
+    const uint64_t b_part =
+        split_n ? (uint64_t)((uint32_t)(p.piece_n / kPair) * row_bytes >> 4) * (uint64_t)part : 0u;
     FullRing<kPair == 2> ring;
     int it = 0;
     bool ok = true;
@@ -948,7 +993,7 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
         if (!mbar_wait<kPair == 2>(bars.acce(a), aph ^ 1u, wc)) break;
         tc_fence_after();
-        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride);
+        const uint32_t dacc = tmem_base + (uint32_t)(a * p.acc_stride) + d_part;
         const int nst = unit_stages<kPair>(unit_tile(u, p), p);
         for (int k = 0; k < nst; ++k) {
             if (!ring.acquire(bars, wc)) {
@@ -957,9 +1002,15 @@ __device__ void conv_mma(const ConvArgs &p, uint32_t sbase, uint32_t tmem_base, 
             }
             tc_fence_after();
             const uint32_t sa = sbase + (uint32_t)ring.stage * p.stage_bytes;
-            issue_stage<kPair, KK, NSUB, NP>(p, dacc, sdesc_kmajor(sa, row_bytes, p.layout),
-                                             sdesc_kmajor(sa + p.a_bytes, row_bytes, p.layout),
-                                             idesc, k == 0);
+            const uint64_t ad = sdesc_kmajor(sa, row_bytes, p.layout);
+            const uint64_t bd = sdesc_kmajor(sa + p.a_bytes, row_bytes, p.layout) + b_part;
+            if constexpr (NP == 2) {
+                if (split_n) issue_stage<kPair, KK, NSUB, 1>(p, dacc, ad, bd, idesc, k == 0, 1);
+                else issue_stage<kPair, KK, NSUB, 2>(p, dacc, ad, bd, idesc, k == 0, 2);
+            } else {
+                issue_stage<kPair, KK, NSUB, NP>(p, dacc, ad, bd, idesc, k == 0,
+                                                 split_n ? 1 : p.n_pieces);
+            }
             // Frees the smem stage (in both CTAs of a pair) when these MMAs finish.
             if (kPair == 2)
                 mma_commit_pair_mc(bars.empty(ring.stage), (uint16_t)0x3);
@@ -1467,17 +1518,19 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     const int num_units = p.tile_units * p.nphase;
 
     if (threadIdx.x == 0) {
+        // every issuer's commit arrives on the barriers the MMAs release
+        const uint32_t ni = (uint32_t)p.issuers;
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(bars.full(s), kFuse ? 2 : 1);  // (fused: the weights' and the halo's)
-            mbar_init(bars.empty(s), 1);
+            mbar_init(bars.empty(s), ni);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(bars.accf(a), 1);
+            mbar_init(bars.accf(a), ni);
             mbar_init(bars.acce(a), p.epi_warps * kPair);
         }
-        mbar_init(bars.drain(), 1);
+        mbar_init(bars.drain(), ni);
         mbar_init(bars.resf(), 1);
-        for (int i = 0; i < 4; ++i) mbar_init(bars.emptya(i), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bars.emptya(i), ni);
         if (kFuse)
             for (int i = 0; i < 4; ++i) mbar_init(bars.peer(i), 1);
         *abort_flag = 0;
@@ -1531,14 +1584,15 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                 conv_producer<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
                                      unit0, unit_stride, num_units, rank);
         }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
+    } else if (warp == 1 || warp == kIssuer2Warp) {
+        const int part = warp == 1 ? 0 : 1;
+        if (lane == 0 && rank == 0 && part < p.issuers) {
             if (p.halo)
                 conv_mma_halo<kPair, KK, NSUB, NP, kUp>(p, sbase, tmem_base, bars, wc, unit0,
-                                                   unit_stride, num_units);
+                                                        unit_stride, num_units, part);
             else
                 conv_mma<kPair, KK, NSUB, NP>(p, sbase, tmem_base, bars, wc, unit0, unit_stride,
-                                              num_units);
+                                              num_units, part);
         }
     } else if (kFuse && warp >= 2 + p.epi_warps) {
         conv_transform<kPair>(&mapA, &mapC, p, sbase, bars, wc, unit0, unit_stride, num_units,
