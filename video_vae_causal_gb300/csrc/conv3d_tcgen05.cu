@@ -292,11 +292,18 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         if (sw2 < sw) sw = sw2;
     }
     pl.sw = sw;
-    // Halo layout: 64-channel chunks as one 128-byte swizzled row per pixel
-    // (one TMA row per pixel and chunk), narrower ones as 8-channel planes
-    // (measured faster for them).  A rows region: 18 x halo_w rows.
-    pl.halo_rows = sw == 64;
-    pl.sub_stride = ((uint32_t)(kHaloH * pl.halo_w) * (uint32_t)sw * 2u + 1023u) & ~1023u;
+    // Halo layout: 64- and 32-channel chunks as one 128- or 64-byte swizzled
+    // row per pixel, 16-channel ones as 8-channel planes of 16 bytes per
+    // pixel.  TMA moves about one box row per clock per SM whatever its width
+    // (measured: planes 16 B/clk, 64-byte rows 64, 128-byte rows ~108), so the
+    // widest rows keep the halo loads off the critical path.  A rows region:
+    // 18 x halo_w rows, aligned to its swizzle pattern (1024 B for 128-byte
+    // rows, 512 B for 64-byte rows).
+    pl.halo_rows = sw == 64 || sw == 32;
+    {
+        const uint32_t atom = sw == 64 ? 1023u : 511u;
+        pl.sub_stride = ((uint32_t)(kHaloH * pl.halo_w) * (uint32_t)sw * 2u + atom) & ~atom;
+    }
     // N split into equal pieces of at most 256 columns, each a multiple of
     // 16 * pair (a pair splits every piece's rows between its two CTAs).
     // Narrow layers (c_out < 16) pad N to 16 rows per CTA; their weight rows
@@ -391,7 +398,9 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.na = 2;
         if (s.up2d && 3u * pl.a_stride + 3u * pl.stage_bytes + reserve <= (uint32_t)kSmemBudget)
             pl.na = 3;
-        pl.a_bytes = (uint32_t)pl.na * pl.a_stride;  // the weight ring starts here
+        // the weight ring starts here, 1024-aligned (64-byte-row halos are
+        // only 512-aligned)
+        pl.a_bytes = ((uint32_t)pl.na * pl.a_stride + 1023u) & ~1023u;
         pl.stages = (int)((kSmemBudget - reserve - pl.a_bytes) / pl.stage_bytes);
         if (pl.stages > 8) pl.stages = 8;
         if (pl.stages < 2) return false;

@@ -111,7 +111,7 @@ struct ConvArgs {
     int patches_w;       // patches per frame row (halo mode)
     int nq;              // 128-row sub-tiles per CTA tile (halo mode: 1, or 2 for 16x16 patches)
     int halo_w;          // halo width in pixels: 8 * nq + 2
-    int halo_rows;         // halo as swizzled pixel rows (sw = 64) instead of 8-channel planes
+    int halo_rows;         // halo as swizzled pixel rows (sw = 64, 32) instead of 8-channel planes
     uint32_t sub_stride;   // rows: bytes between the halo's sw-channel regions (1024-aligned)
     uint32_t plane_bytes;  // planes: one 8-channel plane of the halo, 18 * halo_w * 16
     int tb;              // spatial taps per weight stage (halo mode: 1, 3)
@@ -555,14 +555,19 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
 }
 
 // Shared-memory address of the 16-byte vector j (channels 8j .. 8j + 7) of
-// halo pixel `pix` in an A buffer: one 128-byte swizzled row per pixel and
-// 64-channel region (the layout TMA's 128-byte swizzle writes), or 8-channel
-// planes of 16 bytes per pixel.
+// halo pixel `pix` in an A buffer: one swizzled row per pixel and sw-channel
+// region -- 128-byte rows (sw = 64) with the 16-byte column XOR pix & 7, or
+// 64-byte rows (sw = 32) with the column XOR (pix >> 1) & 3, the layouts
+// TMA's 128- and 64-byte swizzles write into regions aligned to their
+// 1024- and 512-byte pattern -- or 8-channel planes of 16 bytes per pixel.
 __device__ __forceinline__ uint32_t halo_vec_addr(const ConvArgs &p, uint32_t abuf, int pix,
                                                   int j) {
-    if (p.halo_rows)
+    if (p.halo_rows && p.sw == 64)
         return abuf + (uint32_t)(j >> 3) * p.sub_stride + (uint32_t)pix * 128u +
                ((uint32_t)((j & 7) ^ (pix & 7)) << 4);
+    if (p.halo_rows)
+        return abuf + (uint32_t)(j >> 2) * p.sub_stride + (uint32_t)pix * 64u +
+               ((uint32_t)((j & 3) ^ ((pix >> 1) & 3)) << 4);
     return abuf + (uint32_t)j * p.plane_bytes + (uint32_t)pix * 16u;
 }
 
