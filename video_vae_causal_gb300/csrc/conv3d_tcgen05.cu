@@ -205,14 +205,15 @@ bool encode_patch(CUtensorMap *m, const void *base, int C, int W, int H, int fra
 // The upsampler's output y [frames][2H][2W][C] seen per sub-pixel phase
 // (a, b): as (b C + c, j, a, i, frame), the element at phase coordinates
 // b C + c (dimension 0 spans both column phases' channels), column j, row
-// phase a, row i is y[frame][2i + a][2j + b][c].  A (16, 8, 1, 4, 1) box is
-// one epilogue warp's 4 x 8 low-res pixels of one phase, 16 channels each.
-bool encode_phase_view(CUtensorMap *m, const void *base, int C, int W, int H, int frames) {
+// phase a, row i is y[frame][2i + a][2j + b][c].  A (box_c, 8, 1, 4, 1) box is
+// one epilogue warp's 4 x 8 low-res pixels of one phase, box_c channels each.
+bool encode_phase_view(CUtensorMap *m, const void *base, int C, int W, int H, int frames,
+                       int box_c) {
     cuuint64_t dims[5] = {(cuuint64_t)2 * C, (cuuint64_t)W, 2, (cuuint64_t)H,
                           (cuuint64_t)frames};
     cuuint64_t strides[4] = {(cuuint64_t)2 * C * 2, (cuuint64_t)2 * W * C * 2,
                              (cuuint64_t)4 * W * C * 2, (cuuint64_t)4 * H * W * C * 2};
-    cuuint32_t box[5] = {16, 8, 1, 4, 1};
+    cuuint32_t box[5] = {(cuuint32_t)box_c, 8, 1, 4, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -221,6 +222,14 @@ bool encode_phase_view(CUtensorMap *m, const void *base, int C, int W, int H, in
 }
 
 int pick_sw(int c) { return c % 64 == 0 ? 64 : (c % 32 == 0 ? 32 : 16); }
+
+// Channels per phase-view store box of the upsampler's epilogue: 48 where
+// both column halves of the eight-warp split are multiples of 48 (one box per
+// warp and sub-tile at c_out = 96), else 16.
+int up_box_channels(int c_out) {
+    const int c_split = (c_out / 2 + 15) / 16 * 16;
+    return (c_split % 48 == 0 && (c_out - c_split) % 48 == 0) ? 48 : 16;
+}
 
 struct Plan {
     int pair;  // 1: one CTA per 128-row tile; 2: CTA pair per 256 rows (cta_group::2)
@@ -234,6 +243,7 @@ struct Plan {
     int itb;   // im2col: taps per stage
     int tb;  // spatial taps per weight stage (halo mode)
     int nq, halo_w;  // sub-tiles per CTA tile, halo width in pixels (halo mode)
+    uint32_t stg_warp;  // epilogue staging bytes per warp
     int narrow, npad;  // c_out < 16: N padded to npad
     uint32_t sub_stride;  // halo rows: bytes between sw-channel regions
     int halo_rows;        // halo layout: swizzled pixel rows (sw = 64) or 8-channel planes
@@ -345,8 +355,16 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         if (3u * ((sb1 + 1023u) & ~1023u) + fixed + stage_tile <= (uint32_t)kSmemBudget)
             pl.staged = 1;
     }
-    const uint32_t reserve =
-        fixed + (pl.staged ? stage_tile : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
+    // Epilogue staging per warp: 32 rows x 32 channels, or for the
+    // upsampler's phase-view stores on halo tiles the warp's whole channel
+    // share of a sub-tile (its boxes leave by TMA after the last chunk).
+    {
+        const uint32_t c_split = (uint32_t)((s.c_out / 2 + 15) / 16 * 16);
+        pl.stg_warp = (s.up2d && halo && 64u * c_split > kStageBytesPerWarp)
+                          ? 64u * c_split
+                          : kStageBytesPerWarp;
+    }
+    const uint32_t reserve = fixed + (pl.staged ? stage_tile : (uint32_t)kEpiWarps * pl.stg_warp);
     const int need_stages = pl.staged ? 3 : min_stages;
     if (halo) {
         // Halo ring (2 buffers of 18 x halo_w pixels x chunk channels) + a ring of
@@ -412,7 +430,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
         pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                         (s.up2d ? 128u : 0u) /*staging alignment for TMA stores*/ +
-                        (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
+                        (pl.staged ? 0u : (uint32_t)kEpiWarps * pl.stg_warp);
         // The input norm can ride on the halo loads when one chunk holds every
         // channel of a pixel (its norm is then complete in one halo), with no
         // shortcut segment and two accumulators (four epilogue warps keep up).
@@ -476,7 +494,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 14);
     pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
     pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
-                    (pl.staged ? 0u : (uint32_t)(kEpiWarps * kStageBytesPerWarp));
+                    (pl.staged ? 0u : (uint32_t)kEpiWarps * pl.stg_warp);
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
     if (pl.smem_bytes < 120u * 1024u) pl.smem_bytes = 120u * 1024u;
     return pl.smem_bytes <= (uint32_t)kSmemBudget;
@@ -657,7 +675,9 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
             if (s.epi == kEpiResidual) ok = ok && encode_frames(&mR, s.resid, s.c_out, HW, frames);
         }
     }
-    if (s.up2d && pl.halo) ok = ok && encode_phase_view(&mY, s.out, s.c_out, s.W, s.H, frames);
+    if (s.up2d && pl.halo)
+        ok = ok && encode_phase_view(&mY, s.out, s.c_out, s.W, s.H, frames,
+                                     up_box_channels(s.c_out));
     if (!ok) return cudaErrorInvalidValue;
 
     ConvArgs a;
@@ -693,6 +713,8 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     a.a_stride = pl.a_stride;
     a.na = pl.na;
     a.up_tma = s.up2d && pl.halo;
+    a.stg_warp = pl.stg_warp;
+    a.up_box = up_box_channels(s.c_out);
     a.a_tx = pl.a_tx;
     a.tiles_per_frame = pl.halo ? ((s.H + 15) / 16) * a.patches_w : (HW + kBlockM - 1) / kBlockM;
     a.num_tiles = a.tiles_per_frame * frames;

@@ -90,6 +90,8 @@ struct ConvArgs {
     int segs_per_kt;     // im2col: stages per temporal tap and channel chunk, sp_taps / itb
     int na;              // halo mode: buffers in the A (halo) ring, 2 to 4
     int up_tma;          // upsampler on halo tiles: TMA stores through the phase view of y
+    int up_box;          // channels per phase-view store box (48, else 16)
+    uint32_t stg_warp;   // bytes of each epilogue warp's staging buffer
     int up_t;            // temporal upsampler: frame phases, taps t-1 and t at the centre pixel
     int fuse;            // input norm fused: warps 2 + epi_warps .. 9 build every halo
     int epi_warps;       // epilogue warps: 8 (two per TMEM lane quarter), 4 when fused
@@ -1129,7 +1131,6 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
     const int c_split = p.epi_warps == 8 ? ((p.c_out / 2) + 15) / 16 * 16 : p.c_out;
     const int c_begin = half ? c_split : 0, c_end = half ? p.c_out : c_split;
     int it = 0;
-    uint32_t nst = 0;  // staging half of this warp's next TMA store (upsampler)
     for (int u = unit0; u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
@@ -1254,35 +1255,45 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
                 if (kUp && p.up_tma) {
                     // Upsampler on halo tiles: the warp's 4 x 8 low-res pixels
-                    // are one box of the phase view of y (its pixels 2 apart),
-                    // 16 channels per store, staged through two 1 KB halves of
-                    // the warp's buffer; the view clips what lies past W or H.
-                    const int ph = unit_phase(u, p);
+                    // are boxes of the phase view of y (its pixels 2 apart),
+                    // up_box channels each.  The whole sub-tile's channels are
+                    // staged ([box][pixel][up_box channels]) and leave by TMA
+                    // stores after its last chunk; the buffer is reused once
+                    // the previous sub-tile's stores have read it.
+                    if (c == c_begin) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+                    }
+                    const int box_bytes = 64 * p.up_box;  // 32 pixels x up_box x 2 B
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (16 * h < n) {
-                            uint8_t *buf = stg + (nst & 1) * 1024;
-                            if (lane == 0) bulk_wait_read_but1();  // its last store has read it
-                            __syncwarp();
-                            uint4 *d = reinterpret_cast<uint4 *>(buf + lane * 32);
+                            const int cc = c - c_begin + 16 * h;
+                            uint4 *d = reinterpret_cast<uint4 *>(
+                                stg + (cc / p.up_box) * box_bytes + lane * 2 * p.up_box +
+                                2 * (cc % p.up_box));
                             d[0] = make_uint4(o[8 * h], o[8 * h + 1], o[8 * h + 2], o[8 * h + 3]);
                             d[1] = make_uint4(o[8 * h + 4], o[8 * h + 5], o[8 * h + 6],
                                               o[8 * h + 7]);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            const uint32_t src = smem_u32(buf);
-                            if (lane == 0 && !ti.dummy && ti.h0 + 4 * q < p.H &&
-                                ti.w0 + 8 * sub < p.W) {  // (a box past the frame: nothing)
+                        }
+                    }
+                    if (c + 32 >= c_end) {  // the sub-tile's last chunk: store it
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        const int ph = unit_phase(u, p);
+                        if (lane == 0 && !ti.dummy && ti.h0 + 4 * q < p.H &&
+                            ti.w0 + 8 * sub < p.W) {  // (a box past the frame: nothing)
+                            for (int k = 0; k * p.up_box < c_end - c_begin; ++k) {
+                                const uint32_t src = smem_u32(stg + k * box_bytes);
                                 if (src & 127u) {  // a bulk tensor copy needs 128-byte alignment
                                     atomicOr(p.err, kDevErrAlign);
-                                } else {
-                                    tma_store_5d(mapY, src, (ph & 1) * p.c_out + c + 16 * h,
-                                                 ti.w0 + 8 * sub, ph >> 1, ti.h0 + 4 * q,
-                                                 ti.frame);
-                                    bulk_commit();
+                                    break;
                                 }
+                                tma_store_5d(mapY, src,
+                                             (ph & 1) * p.c_out + c_begin + k * p.up_box,
+                                             ti.w0 + 8 * sub, ph >> 1, ti.h0 + 4 * q, ti.frame);
                             }
-                            ++nst;
+                            bulk_commit();
                         }
                     }
                 } else if (kUp) {
@@ -1320,7 +1331,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         if (lane == 0) {
             // Accumulator drained: tell the MMA issuer (in the leader CTA).
             if (kPair == 2)
-                mbar_arrive_cluster(mapa_shared(bars.acce(a), 0));
+                mbar_arrive_remote(mapa_shared(bars.acce(a), 0));
             else
                 mbar_arrive(bars.acce(a));
         }
@@ -1428,7 +1439,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
         if (lane == 0) {
             // TMEM read out: the MMA warp may start the next tile now.
             if (kPair == 2)
-                mbar_arrive_cluster(mapa_shared(bars.acce(0), 0));
+                mbar_arrive_remote(mapa_shared(bars.acce(0), 0));
             else
                 mbar_arrive(bars.acce(0));
         }
@@ -1609,7 +1620,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
                                         unit_stride, num_units, rank);
         else
             conv_epilogue<kPair, kUp>(p, tmem_base, s_bias, s_gamma, s_part,
-                                 s_stage + (threadIdx.x / 32 - 2) * kStageBytesPerWarp, &mapY,
+                                 s_stage + (threadIdx.x / 32 - 2) * p.stg_warp, &mapY,
                                  bars, wc, unit0, unit_stride, num_units, rank);
     }
     __syncwarp();

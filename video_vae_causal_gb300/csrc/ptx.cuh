@@ -93,6 +93,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                  : "memory");
 }
 
+// Same, for a hand-back that follows only TMEM reads already completed by
+// tcgen05.wait::ld (and a tcgen05.fence::before_thread_sync): the default
+// CTA-scope release.  A cluster-scope release first waits until every earlier
+// store of the thread -- global stores, bulk tensor stores -- is performed
+// cluster-wide, which measured thousands of cycles per hand-back.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
