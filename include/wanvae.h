@@ -316,8 +316,9 @@ wanvae_status wanvae_resblock_forward_static(const wanvae_resblock_params *p, co
 wanvae_status wanvae_sync_status(wanvae_stream stream);
 
 /* Upper bound, in nanoseconds, of every device-side wait in later launches
- * (default 1e9, i.e. one second).  0 makes the first wait that is not
- * already satisfied give up at once: a test hook for the timeout path.
+ * (default 1e9, i.e. one second).  0 makes every bounded wait give up at
+ * once, before it looks at its barrier: a deterministic test hook for the
+ * timeout path (the cleanup waits after a give-up keep their own bound).
  * Host-side setting, process-wide. */
 void wanvae_set_wait_limit_ns(uint64_t ns);
 

@@ -564,8 +564,8 @@ def test_streaming_720p_21_calls_sampled(cuda_lib):
 
 # ------------------------------------------------------------------ failure path
 def test_bounded_wait_timeout_reports_and_context_survives(cuda_lib):
-    """A zero wait bound makes the conv's first unsatisfied wait give up: the
-    kernel drains its in-flight copies, frees TMEM, returns, and the host
+    """A zero wait bound makes every bounded wait of the conv give up at once:
+    the kernel drains its in-flight copies, frees TMEM, returns, and the host
     reads WANVAE_ERR_TIMEOUT.  The context must stay usable."""
     B, T, H, W, ci, co = 1, 2, 16, 16, 64, 64
     x, w, b = conv_inputs(B, T, H, W, ci, co, 3, seed=70)

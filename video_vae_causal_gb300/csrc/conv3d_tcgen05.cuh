@@ -1134,6 +1134,8 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
     for (int u = unit0; u < num_units; u += unit_stride, ++it) {
         const int a = it % p.nacc;
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
+        // (the unit's tile, worked out while its MMAs still run)
+        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         const bool got = mbar_wait_warp<kPair == 2>(bars.accf(a), aph, wc);
         if (p.epi == kEpiNormSilu) {
             // The norm's halves meet at a named barrier below, so all epilogue
@@ -1143,7 +1145,6 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
             break;
         }
         tc_fence_after();
-        const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         for (int sub = 0; sub < p.nq; ++sub) {
         // This warp's 32 rows of sub-tile `sub`; rows outside the frame (or
         // of an empty pair slot) are not stored.
@@ -1231,17 +1232,35 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
             for (int c = c_begin; c < c_end; c += 32) {
                 uint32_t r[32];
                 const int n = c_end - c >= 32 ? 32 : 16;
-                tmem_ld_cols(tb + (uint32_t)c, n, r);
+                // The bias and residual loads go out before the TMEM load
+                // (whose wait the compiler cannot move them across), so
+                // their latencies overlap instead of adding up.
                 float v[32];
 #pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    if (i < n) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(s_bias + c + i);
+                        v[i] = b4.x;
+                        v[i + 1] = b4.y;
+                        v[i + 2] = b4.z;
+                        v[i + 3] = b4.w;
+                    }
+                }
+                uint4 x4[4];
+                if (res && valid) {
+#pragma unroll
+                    for (int vv = 0; vv < 4; ++vv)
+                        if (8 * vv < n) x4[vv] = res[c / 8 + vv];
+                }
+                tmem_ld_cols(tb + (uint32_t)c, n, r);
+#pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    if (i < n) v[i] = __uint_as_float(r[i]) + s_bias[c + i];
+                    if (i < n) v[i] = __uint_as_float(r[i]) + v[i];
                 if (res && valid) {
 #pragma unroll
                     for (int vv = 0; vv < 4; ++vv) {
                         if (8 * vv < n) {
-                            const uint4 x4 = res[c / 8 + vv];
-                            const uint32_t xs[4] = {x4.x, x4.y, x4.z, x4.w};
+                            const uint32_t xs[4] = {x4[vv].x, x4[vv].y, x4[vv].z, x4[vv].w};
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 v[8 * vv + 2 * i] += __uint_as_float(xs[i] << 16);

@@ -135,11 +135,22 @@ __device__ __forceinline__ bool mbar_try_wait_t(uint32_t bar, uint32_t parity) {
     return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
 }
 
+// A zero bound gives up before looking at the barrier: try_wait itself may
+// suspend the thread until the phase completes, so "the first wait not yet
+// satisfied" is not a deterministic test hook on a small problem.
+__device__ __forceinline__ bool give_up_at_once(const WaitCtl &w) {
+    if (w.limit_ns != 0) return false;
+    *w.abort = 1;
+    atomicOr(w.err, w.give_up_bits ? w.give_up_bits : kDevErrTimeout);
+    return true;
+}
+
 // Single-thread bounded wait for the phase of `parity` to complete.  Gives up
 // when another thread of the CTA raised the abort flag, or after limit_ns;
 // in the latter case it raises the abort flag and the device error bit.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w) {
+    if (give_up_at_once(w)) return false;
     if (mbar_try_wait_t<kCluster>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -159,6 +170,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl &w) {
     const int lane = threadIdx.x & 31;
+    if (w.limit_ns == 0) {  // (uniform across the warp)
+        if (lane == 0) give_up_at_once(w);
+        __syncwarp();
+        return false;
+    }
     bool ok = mbar_try_wait_t<kCluster>(bar, parity);
     if (!__all_sync(0xffffffffu, ok)) {
         const uint64_t t0 = globaltimer_ns();
