@@ -427,7 +427,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
         if (pl.staged) off += stage_tile;
         pl.off_bars = off;
         pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 14);
-        pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
+        pl.off_vec = (pl.off_misc + 24u + 15u) & ~15u;  // TMEM slot, abort flag, producer state
         pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                         (s.up2d ? 128u : 0u) /*staging alignment for TMA stores*/ +
                         (pl.staged ? 0u : (uint32_t)kEpiWarps * pl.stg_warp);
@@ -492,7 +492,7 @@ bool make_plan(const ConvSpec &s, Plan &pl, int pair, int halo, int wide) {
     if (pl.staged) off += stage_tile;
     pl.off_bars = off;
     pl.off_misc = pl.off_bars + 8u * (2 * pl.stages + 14);
-    pl.off_vec = (pl.off_misc + 8u + 15u) & ~15u;
+    pl.off_vec = (pl.off_misc + 24u + 15u) & ~15u;  // TMEM slot, abort flag, producer state
     pl.smem_bytes = 1024u + pl.off_vec + 2u * 4u * s.c_out + 4u * 4u * kBlockM +
                     (pl.staged ? 0u : (uint32_t)kEpiWarps * pl.stg_warp);
     // One CTA per SM: the TMEM allocation assumes it has the SM to itself.
@@ -761,6 +761,7 @@ cudaError_t launch_conv3d(const ConvSpec &s, const LaunchCtx &ctx) {
     // Two MMA issuers wherever the accumulators split in two: the sub-tiles
     // of a wide halo tile, or two N pieces.
     a.issuers = (a.nq == 2 || pl.n_pieces == 2) ? 2 : 1;
+    a.producers = pl.halo ? 1 : 2;  // (a halo producer's fills each carry far more MMAs)
     if (pl.fuse) {
         a.nl_L = nact_lanes(s.c_in);
         a.nl_vpt = (s.c_in / 8) / a.nl_L;

@@ -29,10 +29,10 @@
 // matrix, one tiled TMA box per (chunk, N-piece).  Both land in smem with the
 // hardware swizzle that the UMMA descriptors name.
 //
-// Warp roles (352 threads, one persistent CTA per SM): warp 0 = TMA producer,
+// Warp roles (384 threads, one persistent CTA per SM): warp 0 = TMA producer,
 // warp 1 = MMA issuer (and TMEM owner), warps 2-9 = epilogue, two per TMEM
 // lane quarter, warp 10 = second MMA issuer where the accumulators split
-// between two.  An mbarrier ring of `stages` smem buffers links producer and
+// between two, warp 11 = second TMA producer of im2col tiles.  An mbarrier ring of `stages` smem buffers links producer and
 // MMA; up to two accumulators in TMEM let the epilogue of tile i overlap the
 // MMAs of tile i+1 when 2 * c_out fits in TMEM's 512 columns.  Every wait is
 // bounded (ptx.cuh).
@@ -61,7 +61,12 @@ constexpr int kEpiWarps = 8;  // two warps per TMEM lane quarter, each half the 
 // for every stage themselves, so one keeps the tensor core fed while the
 // other waits.
 constexpr int kIssuer2Warp = 2 + kEpiWarps;
-constexpr int kThreads = 32 * (kIssuer2Warp + 1);
+// The second TMA producer of im2col tiles, for the same reason: each fill
+// costs its producer a shared-memory round trip behind the tensor core's
+// operand reads (the empty-slot wait), longer than the few MMAs of a
+// one-tap stage, so two producers take alternate fills of the ring.
+constexpr int kProducer2Warp = kIssuer2Warp + 1;
+constexpr int kThreads = 32 * (kProducer2Warp + 1);
 constexpr uint32_t kStageBytesPerWarp = 32 * 64;  // 32 rows x 32 bf16 channels
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kMaxItb = 4;  // im2col: most taps per stage (the upsampler's 2 x 2)
@@ -96,6 +101,7 @@ struct ConvArgs {
     int fuse;            // input norm fused: warps 2 + epi_warps .. 9 build every halo
     int epi_warps;       // epilogue warps: 8 (two per TMEM lane quarter), 4 when fused
     int issuers;         // MMA issuers: 2 = one per sub-tile (nq = 2) or per N piece, else 1
+    int producers;       // TMA producers: 2 (alternate fills) for im2col tiles, 1 for halo tiles
     int nl_L, nl_vpt;    // fused norm: lanes per pixel, 16-byte vectors per lane
     float sqrt_c_in;     // fused norm: sqrt(c_in)
     const float *gamma_in;
@@ -261,16 +267,24 @@ struct FullRing {
 // TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
 // 128-row A tile and its half of every B piece; all loads complete on the
 // leader CTA's `full` barrier, which the leader arms for both CTAs' bytes.
+//
+// With two producers (p.producers == 2) both walk the whole fill sequence and
+// producer `part` issues the fills whose index is `part` modulo 2.  Each
+// publishes the index of its last issued fill in prod[part] and then sets
+// prod[2 + part]; after an abort both are needed to tell which fill is the
+// newest of its stage, the one a drain may wait for.
 template <int kPair, bool kUp>
 __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                               const CUtensorMap *mapB, const CUtensorMap *mapSA,
                               const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
                               const Bars &bars, const WaitCtl &wc, int unit0, int unit_stride,
-                              int num_units, uint32_t rank) {
+                              int num_units, uint32_t rank, int part, volatile int *prod) {
     const int frames = p.num_tiles / p.tiles_per_frame;  // B*T
     const int M = frames * p.HW;
+    const uint32_t np = (uint32_t)p.producers;
     int stage = 0;
     uint32_t phase = 0, fills = 0;
+    int last_mine = -1;
     bool ok = true;
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
         const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
@@ -329,6 +343,14 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
             const int ph = kUp ? unit_phase(u, p) : 0;  // upsampler: its weights
             const CUtensorMap *bm = shortcut ? mapSB : mapB;
             for (int kc = 0; kc < nkc; ++kc) {
+                if (fills % np != (uint32_t)part) {  // the other producer's fill
+                    ++fills;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
+                }
                 if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) {
                     ok = false;
                     break;
@@ -375,6 +397,7 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                             tma_load_4d(db, bm, fb, bk, 0, ph * p.ph_c2, ph * p.ph_c3);
                     }
                 }
+                last_mine = (int)fills;
                 ++fills;
                 if (++stage == p.stages) {
                     stage = 0;
@@ -383,14 +406,38 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
             }
         }
     }
-    if (!ok && rank == 0) {
+    prod[part] = last_mine;
+    __threadfence_block();
+    prod[2 + part] = 1;
+    if ((!ok || *wc.abort) && rank == 0) {
         // Aborted: let the newest fill of every stage land before the CTA
-        // (and its shared memory) goes away.
+        // (and its shared memory) goes away.  A fill is the newest of its
+        // stage unless a fill `stages` (or a multiple) later was issued, by
+        // either producer; waiting on an older phase would never return.
         volatile int no_abort = 0;
         const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
-        const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
-        for (uint32_t f = fills - n; f < fills; ++f)
-            mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
+        if (np == 2) {  // the other producer's last fill, once it has stopped
+            const uint64_t t0 = globaltimer_ns();
+            while (prod[2 + (1 - part)] == 0) {
+                if (globaltimer_ns() - t0 >= kDrainNs) {
+                    atomicOr(wc.err, kDevErrTimeout | kDevErrDrain);
+                    break;
+                }
+            }
+        }
+        const int last0 = prod[0], last1 = np == 2 ? prod[1] : -1;
+        const int newest = last0 > last1 ? last0 : last1;
+        for (int f = last_mine; f >= 0 && f > last_mine - (int)np * p.stages; f -= (int)np) {
+            bool superseded = false;
+            for (int g = f + p.stages; g <= newest; g += p.stages)
+                if (g <= ((g & 1) && np == 2 ? last1 : last0)) {
+                    superseded = true;
+                    break;
+                }
+            if (!superseded)
+                mbar_wait<kPair == 2>(bars.full(f % p.stages), (uint32_t)(f / p.stages) & 1u,
+                                      dc);
+        }
     }
 }
 
@@ -1517,7 +1564,7 @@ __device__ void conv_epilogue_staged(const ConvArgs &p, uint32_t tmem_base, cons
     }
 }
 
-// (kThreads = 10 warps, one CTA per SM: three warps share a sub-partition's
+// (kThreads = 12 warps, one CTA per SM: three warps share a sub-partition's
 // 16K registers, so at most 168 registers a thread)
 template <int kPair, int KK, int NSUB, int NP, bool kUp, bool kFuse = false>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -1537,6 +1584,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     const Bars bars{sbase + p.off_bars, p.stages};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_misc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + p.off_misc + 4);
+    // the producers' last issued fills and done flags (conv_producer)
+    volatile int *prod_state = reinterpret_cast<volatile int *>(smem + p.off_misc + 8);
     float *s_bias = reinterpret_cast<float *>(smem + p.off_vec);
     float *s_gamma = s_bias + p.c_out;
     float *s_part = s_gamma + p.c_out;  // [2 sub-tiles][2][128] partial sums of squares
@@ -1569,6 +1618,8 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
         if (kFuse)
             for (int i = 0; i < 4; ++i) mbar_init(bars.peer(i), 1);
         *abort_flag = 0;
+        prod_state[0] = prod_state[1] = -1;
+        prod_state[2] = prod_state[3] = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1609,15 +1660,16 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{p.wait_ns, p.err, abort_flag, 0u};
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (warp == 0 || warp == kProducer2Warp) {
+        const int part = warp == 0 ? 0 : 1;
+        if (lane == 0 && part < p.producers) {
             if (p.halo)
                 conv_producer_halo<kPair, kUp, kFuse>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p,
                                                       sbase, bars, wc, unit0, unit_stride,
                                                       num_units, rank);
             else
                 conv_producer<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
-                                     unit0, unit_stride, num_units, rank);
+                                          unit0, unit_stride, num_units, rank, part, prod_state);
         }
     } else if (warp == 1 || warp == kIssuer2Warp) {
         const int part = warp == 1 ? 0 : 1;
