@@ -519,6 +519,36 @@ def test_streaming_720p_whole_tensor(cuda_lib):
             what="stream_720p whole")
 
 
+HALO_IM2COL_SAME = [
+    # (c_in = c_out, B, T, H, W): frames whose 16 x 8 patches are ragged, so
+    # that one-frame calls pick halo tiles and longer calls im2col tiles
+    (384, 1, 2, 20, 24),
+    (192, 1, 2, 18, 40),
+    (96, 2, 1, 20, 16),
+]
+
+
+@pytest.mark.parametrize("c,B,T,H,W", HALO_IM2COL_SAME)
+def test_halo_and_im2col_tiles_give_the_same_bits(cuda_lib, c, B, T, H, W):
+    """im2col tiles walk each temporal tap chunk by chunk, the nine spatial taps
+    within a chunk, which is the halo tiles' order: with the same channel
+    chunks both tilings add the same products in the same order, so the block
+    gives the same bits either way.  This is what lets a frame-by-frame call
+    take halo tiles on a ragged frame while the whole clip takes im2col ones
+    (and stay bit-exact with it)."""
+    dims = (B, T, H, W)
+    x, p = synth.make_resblock_inputs(dims, c, c, seed=11, device=DEV)
+    outs = []
+    try:
+        for halo in (1, 0):
+            cuda_lib.set_kernel_variant(halo=halo, wide=0)
+            outs.append(cuda_lib.resblock_forward(x, p))
+            cuda_lib.sync_status()
+    finally:
+        cuda_lib.set_kernel_variant()
+    assert torch.equal(outs[0], outs[1])
+
+
 # ------------------------------------------------------------------ full sizes, sampled
 FULL = [
     ("latent_fullT", 48),

@@ -264,6 +264,46 @@ struct FullRing {
     }
 };
 
+// A producer's exit: publish its last issued fill (prod[part]) and that it
+// has stopped (prod[2 + part]), and after an abort (rank 0) let the newest
+// fill of every stage it issued land before the CTA and its shared memory go
+// away.  A fill is the newest of its stage unless a fill `stages` (or a
+// multiple) later was issued, by either producer (fill f is producer f mod
+// p.producers's); waiting on an older phase would never return.
+template <int kPair>
+__device__ void producer_finish(const ConvArgs &p, const Bars &bars, const WaitCtl &wc,
+                                uint32_t rank, int part, int last_mine, volatile int *prod,
+                                bool ok) {
+    const int np = p.producers;
+    prod[part] = last_mine;
+    __threadfence_block();
+    prod[2 + part] = 1;
+    if ((ok && !*wc.abort) || rank != 0) return;
+    volatile int no_abort = 0;
+    const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
+    if (np == 2) {  // the other producer's last fill, once it has stopped
+        const uint64_t t0 = globaltimer_ns();
+        while (prod[2 + (1 - part)] == 0) {
+            if (globaltimer_ns() - t0 >= kDrainNs) {
+                atomicOr(wc.err, kDevErrTimeout | kDevErrDrain);
+                break;
+            }
+        }
+    }
+    const int last0 = prod[0], last1 = np == 2 ? prod[1] : -1;
+    const int newest = last0 > last1 ? last0 : last1;
+    for (int f = last_mine; f >= 0 && f > last_mine - np * p.stages; f -= np) {
+        bool superseded = false;
+        for (int g = f + p.stages; g <= newest; g += p.stages)
+            if (g <= ((g & 1) && np == 2 ? last1 : last0)) {
+                superseded = true;
+                break;
+            }
+        if (!superseded)
+            mbar_wait<kPair == 2>(bars.full(f % p.stages), (uint32_t)(f / p.stages) & 1u, dc);
+    }
+}
+
 // TMA producer (one thread per CTA).  In a CTA pair each CTA loads its own
 // 128-row A tile and its half of every B piece; all loads complete on the
 // leader CTA's `full` barrier, which the leader arms for both CTAs' bytes.
@@ -286,12 +326,77 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
     uint32_t phase = 0, fills = 0;
     int last_mine = -1;
     bool ok = true;
+    // One fill of a plain k = 3 conv with one tap per stage: the tap's
+    // weights and its im2col rows of channel chunk kc.
+    auto fill_tap = [&](const CUtensorMap *am, int fidx, int tap, int kc, int w0, int h0) -> bool {
+        if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) return false;
+        const uint32_t fb_local = bars.full(stage);
+        if (rank == 0) mbar_arrive_expect_tx(fb_local, p.stage_tx * kPair);
+        const uint32_t fb = kPair == 2 ? mapa_shared(fb_local, 0) : fb_local;
+        const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
+        const uint32_t sb = sa + p.a_bytes;
+        const int kh = (tap / 3) % 3, kw = tap % 3;
+        for (int s2 = 0; s2 < p.nsub; ++s2) {
+            const int c0 = (kc * p.nsub + s2) * p.sw;
+            const uint32_t da = sa + (uint32_t)s2 * p.a_sub_bytes;
+            const uint32_t db = sb + (uint32_t)s2 * p.b_sub_bytes;
+            if (kPair == 2) {
+                tma_load_im2col_4d_pair(da, am, fb, c0, w0 - 1, h0 - 1, fidx, (uint16_t)kw,
+                                        (uint16_t)kh);
+                tma_load_4d_pair(db, mapB, fb, tap * p.c_in + c0, (int)rank * p.bc_row,
+                                 (int)rank * p.bc_rank, 0);
+            } else {
+                tma_load_im2col_4d(da, am, fb, c0, w0 - 1, h0 - 1, fidx, (uint16_t)kw,
+                                   (uint16_t)kh);
+                tma_load_4d(db, mapB, fb, tap * p.c_in + c0, 0, 0, 0);
+            }
+        }
+        last_mine = (int)fills;
+        return true;
+    };
+    auto advance_fill = [&]() {
+        ++fills;
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    };
+    // Plain k = 3 convs with one tap per stage walk each temporal tap chunk by
+    // chunk, the nine spatial taps within a chunk: the K order of the halo
+    // tiles, so that either tiling gives the same sums (and the same bits).
+    const bool chunk_major = !kUp && p.taps == 27 && p.itb == 1;
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
         const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
+        if (chunk_major) {
+            for (int kt = kt0; ok && kt < 3; ++kt) {
+                const int tt = ti.t + kt - 2;
+                const CUtensorMap *am = mapA;
+                int fidx = frames;  // out of range: zeros
+                if (!ti.dummy) {
+                    if (tt >= 0) {
+                        fidx = ti.n * p.T + tt;
+                    } else if (p.has_cache) {
+                        am = mapC;
+                        fidx = ti.n * 2 + tt + 2;
+                    }
+                }
+                for (int kc = 0; ok && kc < p.kc_main; ++kc)
+                    for (int sp = 0; ok && sp < 9; ++sp) {
+                        if (fills % np == (uint32_t)part &&
+                            !fill_tap(am, fidx, kt * 9 + sp, kc, ti.w0, ti.h0)) {
+                            ok = false;
+                            break;
+                        }
+                        advance_fill();
+                    }
+            }
+            if (!ok || p.kc_short == 0) continue;
+        }
         // A segment is itb consecutive taps (one tap unless c_in is small),
-        // each stage of it itb taps x nch channel sub-tiles.
-        const int nseg = p.taps == 27 ? (3 - kt0) * p.segs_per_kt : 1;
+        // each stage of it itb taps x nch channel sub-tiles.  (In chunk-major
+        // order only the shortcut segment is left for this loop.)
+        const int nseg = chunk_major ? 0 : (p.taps == 27 ? (3 - kt0) * p.segs_per_kt : 1);
         const TapBase tbase = kUp ? unit_tap_base(u, p) : TapBase{0, 0};
         const int segs = nseg + (p.kc_short > 0 ? 1 : 0);
         const int row0 = ti.dummy ? M : ti.row0;
@@ -406,39 +511,7 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
             }
         }
     }
-    prod[part] = last_mine;
-    __threadfence_block();
-    prod[2 + part] = 1;
-    if ((!ok || *wc.abort) && rank == 0) {
-        // Aborted: let the newest fill of every stage land before the CTA
-        // (and its shared memory) goes away.  A fill is the newest of its
-        // stage unless a fill `stages` (or a multiple) later was issued, by
-        // either producer; waiting on an older phase would never return.
-        volatile int no_abort = 0;
-        const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
-        if (np == 2) {  // the other producer's last fill, once it has stopped
-            const uint64_t t0 = globaltimer_ns();
-            while (prod[2 + (1 - part)] == 0) {
-                if (globaltimer_ns() - t0 >= kDrainNs) {
-                    atomicOr(wc.err, kDevErrTimeout | kDevErrDrain);
-                    break;
-                }
-            }
-        }
-        const int last0 = prod[0], last1 = np == 2 ? prod[1] : -1;
-        const int newest = last0 > last1 ? last0 : last1;
-        for (int f = last_mine; f >= 0 && f > last_mine - (int)np * p.stages; f -= (int)np) {
-            bool superseded = false;
-            for (int g = f + p.stages; g <= newest; g += p.stages)
-                if (g <= ((g & 1) && np == 2 ? last1 : last0)) {
-                    superseded = true;
-                    break;
-                }
-            if (!superseded)
-                mbar_wait<kPair == 2>(bars.full(f % p.stages), (uint32_t)(f / p.stages) & 1u,
-                                      dc);
-        }
-    }
+    producer_finish<kPair>(p, bars, wc, rank, part, last_mine, prod, ok);
 }
 
 // 5-D tiled load (x = c0 innermost).
@@ -484,18 +557,41 @@ __device__ __forceinline__ void load4(uint32_t dst, const CUtensorMap *m, uint32
 // spatial taps each (B ring); the halo completes on the barrier of the first
 // of those stages, so the MMA issuer waits once per stage.  Then the shortcut
 // segment's chunks (x patch into the A ring + its weights, one stage each).
+//
+// With two producers (p.producers == 2: one-tap weight stages, whose few MMAs
+// leave one producer's per-fill round trip exposed) producer `part` issues the
+// fills whose index is `part` modulo 2, the halo load with the first fill of
+// its (kt, chunk) group; both walk the whole sequence, stages and halo
+// buffers alike (conv_producer has the same scheme).
 template <int kPair, bool kUp, bool kFuse>
 __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *mapC,
                                    const CUtensorMap *mapB, const CUtensorMap *mapSA,
                                    const CUtensorMap *mapSB, const ConvArgs &p, uint32_t sbase,
                                    const Bars &bars, const WaitCtl &wc, int unit0,
-                                   int unit_stride, int num_units, uint32_t rank) {
+                                   int unit_stride, int num_units, uint32_t rank, int part,
+                                   volatile int *prod) {
     const int frames = p.num_tiles / p.tiles_per_frame;
     const int chunk = p.nsub * p.sw;  // channels per halo / per weight sub-stage
     const int groups = p.sp_taps / p.tb;
+    const uint32_t np = (uint32_t)p.producers;
     int stage = 0, ia = 0;
     uint32_t phase = 0, pha = 0, fills = 0;
+    int last_mine = -1;
     bool ok = true;
+    auto mine = [&]() { return fills % np == (uint32_t)part; };
+    auto skip_stage = [&]() {  // the other producer's fill
+        ++fills;
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    };
+    auto skip_abuf = [&]() {
+        if (++ia == p.na) {
+            ia = 0;
+            pha ^= 1u;
+        }
+    };
     // Next B stage, armed for `tx` bytes per CTA (both CTAs' loads complete
     // on the leader's barrier).  With the input norm fused a stage completes
     // on two arrivals: a halo's first stage gets its second from the
@@ -510,6 +606,7 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         }
         fb = kPair == 2 ? mapa_shared(fl, 0) : fl;
         dst = sbase + p.a_bytes + (uint32_t)stage * p.stage_bytes;
+        last_mine = (int)fills;
         ++fills;
         if (++stage == p.stages) {
             stage = 0;
@@ -544,15 +641,18 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
             for (int cc = 0; ok && cc < p.kc_main; ++cc) {
                 uint32_t da = 0;
                 if (kFuse) {  // the transform warps fill the A buffer
-                    if (++ia == p.na) {
-                        ia = 0;
-                        pha ^= 1u;
-                    }
+                    skip_abuf();
+                } else if (!mine()) {  // the group's first fill, so its halo: the other's
+                    skip_abuf();
                 } else if (!next_abuf(da)) {
                     ok = false;
                     break;
                 }
                 for (int g = 0; g < groups; ++g) {
+                    if (!mine()) {
+                        skip_stage();
+                        continue;
+                    }
                     uint32_t db, fb;
                     if (!next_stage(p.stage_tx + (g == 0 && !kFuse ? p.a_tx : 0u),
                                     kFuse && g > 0, db, fb)) {
@@ -582,6 +682,11 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
         const uint32_t sub_a = (uint32_t)kBlockM * p.sw * 2u;
         for (int cc = 0; ok && cc < p.kc_short; ++cc) {
             uint32_t da, db, fb;
+            if (!mine()) {
+                skip_abuf();
+                skip_stage();
+                continue;
+            }
             if (!next_abuf(da) || !next_stage(p.nsub * (sub_a + p.b_sub_bytes), kFuse, db, fb)) {
                 ok = false;
                 break;
@@ -592,15 +697,9 @@ __device__ void conv_producer_halo(const CUtensorMap *mapA, const CUtensorMap *m
             load5<kPair>(db, mapSB, fb, cc * chunk, 0, (int)rank, 0, 0);
         }
     }
-    if (!ok && rank == 0) {
-        // Aborted: let the newest fill of every stage (halo loads included)
-        // land before the CTA and its shared memory go away.
-        volatile int no_abort = 0;
-        const WaitCtl dc{kDrainNs, wc.err, &no_abort, kDevErrTimeout | kDevErrDrain};
-        const uint32_t n = fills < (uint32_t)p.stages ? fills : (uint32_t)p.stages;
-        for (uint32_t f = fills - n; f < fills; ++f)
-            mbar_wait<kPair == 2>(bars.full((int)(f % p.stages)), (f / p.stages) & 1u, dc);
-    }
+    // (a halo load completes on its group's first stage, so draining the
+    // newest fill of every stage covers the halos too)
+    producer_finish<kPair>(p, bars, wc, rank, part, last_mine, prod, ok);
 }
 
 // Shared-memory address of the 16-byte vector j (channels 8j .. 8j + 7) of
@@ -1666,7 +1765,7 @@ conv3d_tcgen05_kernel(const __grid_constant__ CUtensorMap mapA,
             if (p.halo)
                 conv_producer_halo<kPair, kUp, kFuse>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p,
                                                       sbase, bars, wc, unit0, unit_stride,
-                                                      num_units, rank);
+                                                      num_units, rank, part, prod_state);
             else
                 conv_producer<kPair, kUp>(&mapA, &mapC, &mapB, &mapSA, &mapSB, p, sbase, bars, wc,
                                           unit0, unit_stride, num_units, rank, part, prod_state);
