@@ -326,16 +326,17 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
     uint32_t phase = 0, fills = 0;
     int last_mine = -1;
     bool ok = true;
-    // One fill of a plain k = 3 conv with one tap per stage: the tap's
-    // weights and its im2col rows of channel chunk kc.
-    auto fill_tap = [&](const CUtensorMap *am, int fidx, int tap, int kc, int w0, int h0) -> bool {
+    // One fill with one tap per stage: weight tap wtap (of phase ph, for the
+    // temporal upsampler) and the im2col rows of channel chunk kc at spatial
+    // offset (kh, kw).
+    auto fill_tap = [&](const CUtensorMap *am, int fidx, int wtap, int kh, int kw, int ph, int kc,
+                        int w0, int h0) -> bool {
         if (!mbar_wait<kPair == 2>(bars.empty(stage), phase ^ 1u, wc)) return false;
         const uint32_t fb_local = bars.full(stage);
         if (rank == 0) mbar_arrive_expect_tx(fb_local, p.stage_tx * kPair);
         const uint32_t fb = kPair == 2 ? mapa_shared(fb_local, 0) : fb_local;
         const uint32_t sa = sbase + (uint32_t)stage * p.stage_bytes;
         const uint32_t sb = sa + p.a_bytes;
-        const int kh = (tap / 3) % 3, kw = tap % 3;
         for (int s2 = 0; s2 < p.nsub; ++s2) {
             const int c0 = (kc * p.nsub + s2) * p.sw;
             const uint32_t da = sa + (uint32_t)s2 * p.a_sub_bytes;
@@ -343,12 +344,12 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
             if (kPair == 2) {
                 tma_load_im2col_4d_pair(da, am, fb, c0, w0 - 1, h0 - 1, fidx, (uint16_t)kw,
                                         (uint16_t)kh);
-                tma_load_4d_pair(db, mapB, fb, tap * p.c_in + c0, (int)rank * p.bc_row,
-                                 (int)rank * p.bc_rank, 0);
+                tma_load_4d_pair(db, mapB, fb, wtap * p.c_in + c0, (int)rank * p.bc_row,
+                                 (int)rank * p.bc_rank + ph * p.ph_c2, ph * p.ph_c3);
             } else {
                 tma_load_im2col_4d(da, am, fb, c0, w0 - 1, h0 - 1, fidx, (uint16_t)kw,
                                    (uint16_t)kh);
-                tma_load_4d(db, mapB, fb, tap * p.c_in + c0, 0, 0, 0);
+                tma_load_4d(db, mapB, fb, wtap * p.c_in + c0, 0, ph * p.ph_c2, ph * p.ph_c3);
             }
         }
         last_mine = (int)fills;
@@ -364,7 +365,10 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
     // Plain k = 3 convs with one tap per stage walk each temporal tap chunk by
     // chunk, the nine spatial taps within a chunk: the K order of the halo
     // tiles, so that either tiling gives the same sums (and the same bits).
+    // The temporal upsampler walks its two taps (frames t - 1 and t, centre
+    // pixel) within each chunk in the same way.
     const bool chunk_major = !kUp && p.taps == 27 && p.itb == 1;
+    const bool chunk_major_t = kUp && p.up_t && p.taps == 27 && p.itb == 1;
     for (int u = unit0; ok && u < num_units; u += unit_stride) {
         const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
         const int kt0 = unit_first_kt<kPair>(unit_tile(u, p), p);
@@ -383,8 +387,9 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                 }
                 for (int kc = 0; ok && kc < p.kc_main; ++kc)
                     for (int sp = 0; ok && sp < 9; ++sp) {
+                        const int tap = kt * 9 + sp;
                         if (fills % np == (uint32_t)part &&
-                            !fill_tap(am, fidx, kt * 9 + sp, kc, ti.w0, ti.h0)) {
+                            !fill_tap(am, fidx, tap, (tap / 3) % 3, tap % 3, 0, kc, ti.w0, ti.h0)) {
                             ok = false;
                             break;
                         }
@@ -392,6 +397,32 @@ __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                     }
             }
             if (!ok || p.kc_short == 0) continue;
+        }
+        if (chunk_major_t) {
+            const CUtensorMap *am[2] = {mapA, mapA};
+            int fidx[2] = {frames, frames};  // out of range: zeros
+            for (int q = 0; q < 2; ++q) {
+                const int tt = ti.t + q - 1;  // kt = 1 + q
+                if (!ti.dummy) {
+                    if (tt >= 0) {
+                        fidx[q] = ti.n * p.T + tt;
+                    } else if (p.has_cache) {
+                        am[q] = mapC;
+                        fidx[q] = ti.n * 2 + tt + 2;
+                    }
+                }
+            }
+            const int ph = unit_phase(u, p);
+            for (int kc = 0; ok && kc < p.kc_main; ++kc)
+                for (int q = 0; ok && q < 2; ++q) {
+                    if (fills % np == (uint32_t)part &&
+                        !fill_tap(am[q], fidx[q], q, 1, 1, ph, kc, ti.w0, ti.h0)) {
+                        ok = false;
+                        break;
+                    }
+                    advance_fill();
+                }
+            continue;  // (no shortcut segment)
         }
         // A segment is itb consecutive taps (one tap unless c_in is small),
         // each stage of it itb taps x nch channel sub-tiles.  (In chunk-major
