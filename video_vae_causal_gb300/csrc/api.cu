@@ -505,11 +505,14 @@ static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *
         g_launches++;
         e = launch_conv3d(sA, ctx);
     }
-    if (e == cudaSuccess && cache) {
+    // The feat_cache updates: conv A's reads the input norm's output (fused:
+    // recomputes it from x) and conv B never reads conv A's cache, so without
+    // the fused norm both run in one launch after conv B, off the path between
+    // the convs.
+    if (e == cudaSuccess && cache && fused) {
         g_launches++;
-        e = fused ? launch_cache_update_norm(cache->convA_in, x, p->gamma1, (int)d.B, (int)d.T,
-                                             d.H * d.W, (int)p->c_in, p->eps, ctx)
-                  : launch_cache_update(cache->convA_in, a1, (int)d.B, (int)d.T, frA, ctx);
+        e = launch_cache_update_norm(cache->convA_in, x, p->gamma1, (int)d.B, (int)d.T,
+                                     d.H * d.W, (int)p->c_in, p->eps, ctx);
     }
     if (e == cudaSuccess) e = rec(2);
     if (e == cudaSuccess) {
@@ -518,7 +521,9 @@ static wanvae_status resblock_impl(const wanvae_resblock_params *p, const void *
     }
     if (e == cudaSuccess && cache) {
         g_launches++;
-        e = launch_cache_update(cache->convB_in, a2, (int)d.B, (int)d.T, frB, ctx);
+        e = fused ? launch_cache_update(cache->convB_in, a2, (int)d.B, (int)d.T, frB, ctx)
+                  : launch_cache_update2(cache->convA_in, a1, frA, cache->convB_in, a2, frB,
+                                         (int)d.B, (int)d.T, ctx);
     }
     if (e == cudaSuccess) e = rec(3);
     return from_cuda(e);

@@ -59,6 +59,10 @@ cudaError_t launch_attention_core(const void *q, const void *k, const void *vt, 
 // tensors of frame_bytes bytes per frame (a multiple of 16).
 cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,
                                 const LaunchCtx &ctx);
+// The same for two (cache, src) pairs in one launch.
+cudaError_t launch_cache_update2(void *cache0, const void *src0, int64_t frame_bytes0,
+                                 void *cache1, const void *src1, int64_t frame_bytes1, int B,
+                                 int T, const LaunchCtx &ctx);
 
 // Sub-pixel weights of the upsampler conv: w [Co][3][3][Ci] ->
 // w2 [4 phases][Co][2][2][Ci] (bf16), see rmsnorm_silu.cu.

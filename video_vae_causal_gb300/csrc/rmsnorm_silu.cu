@@ -200,6 +200,33 @@ __global__ void cache_update_kernel(uint4 *__restrict__ cache, const uint4 *__re
     }
 }
 
+// Both convs' feat_cache updates in one launch (blockIdx.y picks the pair):
+// the same copy as cache_update_kernel for (cache0, src0) and (cache1, src1).
+__global__ void cache_update2_kernel(uint4 *__restrict__ cache0, const uint4 *__restrict__ src0,
+                                     int64_t fv0, uint4 *__restrict__ cache1,
+                                     const uint4 *__restrict__ src1, int64_t fv1, int B, int T) {
+    griddep_launch_dependents();
+    griddep_wait();
+    uint4 *cache = blockIdx.y ? cache1 : cache0;
+    const uint4 *src = blockIdx.y ? src1 : src0;
+    const int64_t fv = blockIdx.y ? fv1 : fv0;
+    const int64_t total = (int64_t)B * fv;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i / fv, e = i - b * fv;
+        uint4 *c = cache + b * 2 * fv + e;
+        const uint4 *sp = src + b * (int64_t)T * fv + e;
+        if (T >= 2) {
+            c[0] = sp[(int64_t)(T - 2) * fv];
+            c[fv] = sp[(int64_t)(T - 1) * fv];
+        } else {
+            const uint4 keep = c[fv];
+            c[0] = keep;
+            c[fv] = sp[0];
+        }
+    }
+}
+
 // feat_cache update of a conv whose input norm is fused (its input a1 =
 // SiLU(RMS_norm(x)) is never written out): cache[b] <- the last two frames of
 // concat(cache[b], a1(src[b])).  A group of L lanes owns a pixel, lane `sub`
@@ -370,6 +397,20 @@ cudaError_t launch_cache_update_norm(void *cache, const void *src, const float *
                                   dim3(threads), 0, ctx, c, x, gamma, B, T, HW, C, L, eps, sc);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_cache_update2(void *cache0, const void *src0, int64_t frame_bytes0,
+                                 void *cache1, const void *src1, int64_t frame_bytes1, int B,
+                                 int T, const LaunchCtx &ctx) {
+    const int64_t fv0 = frame_bytes0 / 16, fv1 = frame_bytes1 / 16;
+    const int threads = 256;
+    const int64_t fv = fv0 > fv1 ? fv0 : fv1;
+    int64_t blocks = ((int64_t)B * fv + threads - 1) / threads;
+    const int64_t cap = (int64_t)ctx.num_sms * 4;  // x 2 pairs
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(cache_update2_kernel, dim3((unsigned)blocks, 2), dim3(threads), 0, ctx,
+                      static_cast<uint4 *>(cache0), static_cast<const uint4 *>(src0), fv0,
+                      static_cast<uint4 *>(cache1), static_cast<const uint4 *>(src1), fv1, B, T);
 }
 
 cudaError_t launch_cache_update(void *cache, const void *src, int B, int T, int64_t frame_bytes,
