@@ -246,7 +246,7 @@ struct Plan {
     uint32_t stg_warp;  // epilogue staging bytes per warp
     int narrow, npad;  // c_out < 16: N padded to npad
     uint32_t sub_stride;  // halo rows: bytes between sw-channel regions
-    int halo_rows;        // halo layout: swizzled pixel rows (sw = 64) or 8-channel planes
+    int halo_rows;        // halo layout: swizzled pixel rows (sw = 64, 32) or 8-channel planes
     int acc_stride;
     uint32_t off_a, a_stride, a_tx;
     int na;  // halo mode: A ring buffers

@@ -10,10 +10,11 @@
 //                                  * in[b, t+kt-2, y+kh-1, x+kw-1, c]
 // with zeros (or the feat_cache frames) for t+kt-2 < 0 and zeros outside H, W.
 // GEMM view: M = B*T*H*W output voxels, N = c_out, K = 27 * c_in; the K loop
-// walks the 27 taps, each tap in chunks of channels.
+// walks the three temporal taps, each in chunks of channels, and within a
+// chunk the nine spatial taps (the same order for im2col and halo tiles).
 //
-// Tiling.  A CTA tile is 128 consecutive voxels of ONE frame (b, t) -- the
-// frames are tiled separately, the last tile of a frame is ragged -- by all
+// Tiling.  A CTA tile is 128 voxels of ONE frame (b, t): 128 consecutive ones
+// (im2col; the last tile of a frame is ragged) or a 16 x 8 patch (halo) -- by all
 // c_out channels (the accumulator is 128 TMEM lanes x c_out fp32 columns, so
 // an epilogue thread owns every channel of one voxel, which is what lets the
 // next RMS_norm run inside the epilogue).  Because a tile never spans frames,
@@ -32,10 +33,11 @@
 // Warp roles (384 threads, one persistent CTA per SM): warp 0 = TMA producer,
 // warp 1 = MMA issuer (and TMEM owner), warps 2-9 = epilogue, two per TMEM
 // lane quarter, warp 10 = second MMA issuer where the accumulators split
-// between two, warp 11 = second TMA producer of im2col tiles.  An mbarrier ring of `stages` smem buffers links producer and
-// MMA; up to two accumulators in TMEM let the epilogue of tile i overlap the
-// MMAs of tile i+1 when 2 * c_out fits in TMEM's 512 columns.  Every wait is
-// bounded (ptx.cuh).
+// between two, warp 11 = second TMA producer where fills carry few MMAs
+// (im2col tiles, one-tap halo stages).  An mbarrier ring of `stages` smem
+// buffers links producers and MMA; up to two accumulators in TMEM let the
+// epilogue of tile i overlap the MMAs of tile i+1 when 2 * c_out fits in
+// TMEM's 512 columns.  Every wait is bounded (ptx.cuh).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -312,7 +314,11 @@ __device__ void producer_finish(const ConvArgs &p, const Bars &bars, const WaitC
 // producer `part` issues the fills whose index is `part` modulo 2.  Each
 // publishes the index of its last issued fill in prod[part] and then sets
 // prod[2 + part]; after an abort both are needed to tell which fill is the
-// newest of its stage, the one a drain may wait for.
+// newest of its stage, the one a drain may wait for.  A parity wait cannot
+// tell phase m from phase m - 2, so a producer must never wait for fill f
+// before fill f - 2 * stages is released: the issuers release fills in order
+// and consume every stage, so the producer's own wait for fill f - 2 (which
+// needed fill f - 2 - stages released) already implies it when stages >= 2.
 template <int kPair, bool kUp>
 __device__ void conv_producer(const CUtensorMap *mapA, const CUtensorMap *mapC,
                               const CUtensorMap *mapB, const CUtensorMap *mapSA,
