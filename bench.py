@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -83,10 +84,17 @@ CONV_SOURCES = ("conv3d_tcgen05.cu", "conv3d_tcgen05.cuh", "ptx.cuh", "norm_act.
 
 
 def conv_source_sha(files=CONV_SOURCES):
+    """Hash of the kernel sources with comments and blank lines removed (no
+    string literal in them holds a comment marker), so that an edited comment
+    does not count as a changed kernel."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "video_vae_causal_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "video_vae_causal_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 
