@@ -1319,6 +1319,7 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
         const uint32_t aph = (uint32_t)(it / p.nacc) & 1u;
         // (the unit's tile, worked out while its MMAs still run)
         const TileInfo ti = tile_info(unit_tile(u, p) * kPair + (int)rank, p);
+        bool handed_back = false;  // (the bias and residual epilogue hands back early)
         const bool got = mbar_wait_warp<kPair == 2>(bars.accf(a), aph, wc);
         if (p.epi == kEpiNormSilu) {
             // The norm's halves meet at a named barrier below, so all epilogue
@@ -1436,6 +1437,21 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
                         if (8 * vv < n) x4[vv] = res[c / 8 + vv];
                 }
                 tmem_ld_cols(tb + (uint32_t)c, n, r);
+                if (sub == p.nq - 1 && c + 32 >= c_end) {
+                    // The unit's last TMEM load: hand the accumulator back
+                    // now, not after the stores -- the issuer's next MMAs
+                    // into it wait for this, so the stores' latency would
+                    // otherwise sit between two units' MMAs.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kPair == 2)
+                            mbar_arrive_remote(mapa_shared(bars.acce(a), 0));
+                        else
+                            mbar_arrive(bars.acce(a));
+                    }
+                    handed_back = true;
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     if (i < n) v[i] = __uint_as_float(r[i]) + v[i];
@@ -1528,14 +1544,16 @@ __device__ void conv_epilogue(const ConvArgs &p, uint32_t tmem_base, const float
             }
         }
         }  // sub-tiles
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            // Accumulator drained: tell the MMA issuer (in the leader CTA).
-            if (kPair == 2)
-                mbar_arrive_remote(mapa_shared(bars.acce(a), 0));
-            else
-                mbar_arrive(bars.acce(a));
+        if (!handed_back) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                // Accumulator drained: tell the MMA issuer (in the leader CTA).
+                if (kPair == 2)
+                    mbar_arrive_remote(mapa_shared(bars.acce(a), 0));
+                else
+                    mbar_arrive(bars.acce(a));
+            }
         }
     }
     if (kUp && p.up_tma && lane == 0) bulk_wait_all();  // stores done before the CTA leaves
