@@ -83,13 +83,15 @@ def load_peaks():
 CONV_SOURCES = ("conv3d_tcgen05.cu", "conv3d_tcgen05.cuh", "ptx.cuh", "norm_act.cuh")
 
 
-def conv_source_sha(files=CONV_SOURCES):
-    """Hash of the kernel sources with comments and blank lines removed (no
-    string literal in them holds a comment marker), so that an edited comment
-    does not count as a changed kernel."""
+def conv_source_sha(files=CONV_SOURCES, root=None):
+    """Hash of the kernel sources (in `root`, by default the package's csrc/)
+    with comments and blank lines removed (no string literal in them holds a
+    comment marker), so that an edited comment does not count as a changed
+    kernel."""
+    root = root or os.path.join(ROOT, "video_vae_causal_gb300", "csrc")
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "video_vae_causal_gb300", "csrc", f)) as fh:
+        with open(os.path.join(root, f)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
@@ -337,6 +339,20 @@ def bench_reference_conv(args):
 
 TIMED_REGION_S = 1.5  # default length of the timed region (clock samples every 100 ms)
 MAX_STEPS = 4000
+
+
+def e2e_chunk_frames(T, H, W, streaming):
+    """Frames per chunk of the end-to-end host pipeline.  Large frames: the
+    copies outweigh the block, and only the first chunk's copy-in and the last
+    chunk's copy-out overlap nothing, so chunks of about 1/27 of the clip (3
+    frames of 81: 818-857 M voxels/s against 587 M with 11-frame chunks, on one
+    box).  Small frames: a chunk must still fill the GPU with tiles, so an
+    eighth of the clip.  Frame-by-frame decode: one frame."""
+    if streaming:
+        return 1
+    if H * W >= 65536:
+        return max(1, -(-T // 27))
+    return max(1, -(-T // 8))
 
 
 def default_steps(args, step_ms):
@@ -783,17 +799,7 @@ def bench_ours(args):
         x_cpu = x.cpu()
     x_host = x_cpu.pin_memory()
     y_host = torch.empty((B, T, H, W, co), dtype=torch.bfloat16).pin_memory()
-    # Large frames: the copies outweigh the block, and only the first chunk's
-    # copy-in and the last chunk's copy-out overlap nothing, so chunks of about
-    # 1/27 of the clip (3 frames of 81: 818-857 M voxels/s against 587 M with
-    # 11-frame chunks, on one box).  Small frames: a chunk must still fill the
-    # GPU with tiles, so an eighth of the clip.
-    if streaming:
-        chunk = 1
-    elif H * W >= 65536:
-        chunk = max(1, -(-T // 27))
-    else:
-        chunk = max(1, -(-T // 8))
+    chunk = e2e_chunk_frames(T, H, W, streaming)
     hws = torch.empty(wanvae.resblock_forward_host_workspace_size(dims, ci, co, chunk),
                       dtype=torch.uint8, device=dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
