@@ -549,6 +549,34 @@ def test_halo_and_im2col_tiles_give_the_same_bits(cuda_lib, c, B, T, H, W):
     assert torch.equal(outs[0], outs[1])
 
 
+STREAM_RAGGED = [
+    # (c, B, T, H, W): frames whose 16 x 8 patches are ragged, decoded frame by
+    # frame (halo tiles, two producers) and whole (im2col tiles)
+    (384, 2, 4, 20, 24),
+    (96, 2, 3, 18, 40),
+]
+
+
+@pytest.mark.parametrize("c,B,T,H,W", STREAM_RAGGED)
+def test_streaming_ragged_frames_bit_exact(cuda_lib, c, B, T, H, W):
+    """Frame-by-frame decode of a batch of two on ragged frames, where each
+    one-frame call takes halo tiles and the whole clip im2col tiles: the same
+    bits, frame by frame and in the caches, and the oracle's values."""
+    dims = (B, T, H, W)
+    x, p = synth.make_resblock_inputs(dims, c, c, seed=23)
+    xd, pd = x.to(DEV), dev(p)
+    cA = torch.zeros((B, 2, H, W, c), dtype=torch.bfloat16, device=DEV)
+    cB = torch.zeros((B, 2, H, W, c), dtype=torch.bfloat16, device=DEV)
+    ws = cuda_lib.make_workspace((B, 1, H, W), c, c)
+    y = torch.cat([cuda_lib.resblock_forward(xd[:, t:t + 1].contiguous(), pd, cache=(cA, cB),
+                                             workspace=ws) for t in range(T)], dim=1)
+    full = cuda_lib.resblock_forward(xd, pd)
+    cuda_lib.sync_status()
+    assert torch.equal(y, full)
+    compare(to_f64(full), oracle.resblock_forward(x, oracle.Params.from_dict(p)),
+            what="streaming ragged")
+
+
 # ------------------------------------------------------------------ full sizes, sampled
 FULL = [
     ("latent_fullT", 48),
